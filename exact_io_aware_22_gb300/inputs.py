@@ -1,0 +1,46 @@
+"""Seeded synthetic inputs for exact attention.
+
+This module holds no attention arithmetic: it only draws random tensors, so
+that the CUDA path and the CPU oracle can be fed the very same values.
+
+Recipe: one CPU ``torch.Generator`` seeded per workload; draws in the fixed
+order Q, K, V, dO, each i.i.d. N(0, 1) in fp32 of shape (B, H, N, d); Q and K
+are then multiplied by ``qk_std`` (4 for the large-row-maximum stress case);
+finally every tensor is rounded to the 16-bit dtype.  The oracle consumes the
+rounded values upcast exactly to fp64.
+"""
+from __future__ import annotations
+
+import torch
+
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+def make_inputs(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int = 0,
+                qk_std: float = 1.0):
+    """Return dict(q, k, v, do) of CPU tensors (B, H, N, d) in ``dtype``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    shape = (B, H, N, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    do = torch.randn(shape, generator=g, dtype=torch.float32)
+    if qk_std != 1.0:
+        q = q * qk_std
+        k = k * qk_std
+    t = DTYPES[dtype]
+    return {"q": q.to(t), "k": k.to(t), "v": v.to(t), "do": do.to(t)}
+
+
+# Workloads: (name, B, H, N, d, dtype, causal, qk_std)
+WORKLOADS = {
+    "tiny_full_d64_fp16": (1, 1, 128, 64, "fp16", False, 1.0),
+    "ragged_causal_d32_fp16": (4, 8, 1000, 32, "fp16", True, 1.0),
+    "ragged_causal_d32_fp16_stress": (4, 8, 1000, 32, "fp16", True, 4.0),
+    "gpt2m_causal_d64_fp16": (8, 16, 1024, 64, "fp16", True, 1.0),
+    "n4k_full_d128_bf16": (2, 16, 4096, 128, "bf16", False, 1.0),
+    "n4k_causal_d128_bf16": (2, 16, 4096, 128, "bf16", True, 1.0),
+    "n8k_causal_d128_bf16": (1, 32, 8192, 128, "bf16", True, 1.0),
+    "n16k_causal_d128_bf16": (1, 32, 16384, 128, "bf16", True, 1.0),
+}

@@ -1,0 +1,163 @@
+"""fp64 CPU oracle for exact attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+and reference legs import this package.  The product path (the CUDA library
+and its Python binding) never imports, links or calls it, and it imports
+nothing from the product package.
+
+Contents
+  * ``fwd``/``bwd``: the plain definition of attention and its gradients,
+    written in C (``fa_oracle.c``), fp64, one query row at a time, OpenMP over
+    (batch, head).  Definitions follow the "flash-attn-triton" docs page,
+    section "The argument" (S = QK^T/sqrt(d), row softmax, P V), with causal
+    masking lower-triangular (FlashAttention note, "Key Mechanisms").
+  * ``fwd_online``/``row_partial``/``merge``: the separate naive online-softmax
+    oracle of the docs page's Fig. 3 and the two-partial merge of the tutorial
+    page ("Softmax in pieces").
+  * ``iomodel``: byte and FLOP counts of the pages' arithmetic (footprint
+    calculator, Fig. 2; HBM access counts, Table 2).
+
+Inputs are numpy arrays convertible to fp64 (callers pass the 16-bit values
+upcast exactly).  Nothing here rounds to 16 bits.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libfa_oracle.so")
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _SO) -> str:
+    """Compile the C oracle with gcc (fp64, no fast-math, OpenMP)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp", "-fPIC",
+               "-shared", src, "-o", tmp, "-lm"]
+        subprocess.check_call(cmd)
+        os.replace(tmp, out)
+    return out
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+class Oracle:
+    """ctypes view of one compiled copy of ``fa_oracle.c``."""
+
+    def __init__(self, so_path: str):
+        lib = ctypes.CDLL(so_path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        i, dbl = ctypes.c_int, ctypes.c_double
+        lib.oracle_fwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dbl]
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, dbl]
+        lib.oracle_fwd_online.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dbl, i, i]
+        lib.oracle_row_partial.argtypes = [dp, dp, dp, i, i, i, i, i, dbl, i, i, dp, dp]
+        lib.oracle_row_partial.restype = dbl
+        lib.oracle_merge.argtypes = [dbl, dbl, dp, dbl, dbl, dp, i, i, dp, dp]
+        lib.oracle_merge.restype = dbl
+        lib.oracle_num_threads.restype = ctypes.c_int
+        self.lib = lib
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def fwd(self, q, k, v, causal: bool, scale: float):
+        """O, L for (B,H,N,d) inputs.  L is the natural-log logsumexp of scaled scores."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, N, d = q.shape
+        o = np.empty_like(q)
+        lse = np.empty((B, H, N), dtype=np.float64)
+        self.lib.oracle_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d, int(causal),
+                            float(scale))
+        return o, lse
+
+    def bwd(self, q, k, v, do, causal: bool, scale: float):
+        """dQ, dK, dV and D = rowsum(dO o O) from the plain definition."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+        B, H, N, d = q.shape
+        dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+        D = np.empty((B, H, N), dtype=np.float64)
+        self.lib.oracle_bwd(_p(q), _p(k), _p(v), _p(do), _p(dq), _p(dk), _p(dv), _p(D),
+                            B, H, N, d, int(causal), float(scale))
+        return dq, dk, dv, D
+
+    def fwd_online(self, q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):
+        """O, L by the per-tile online update (docs page Fig. 3), key tiles of ``tile``."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, N, d = q.shape
+        o = np.empty_like(q)
+        lse = np.empty((B, H, N), dtype=np.float64)
+        self.lib.oracle_fwd_online(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d,
+                                   int(causal), float(scale), int(tile), int(base2))
+        return o, lse
+
+    def row_partial(self, qi, k, v, i: int, j0: int, j1: int, causal: bool, scale: float,
+                    tile: int, base2: bool = False):
+        """(m, l, acc) of query row i over keys [j0, j1) of one head (k, v: (N, d))."""
+        qi, k, v = _f64(qi), _f64(k), _f64(v)
+        d = k.shape[1]
+        acc = np.empty(d, dtype=np.float64)
+        l = ctypes.c_double()
+        m = self.lib.oracle_row_partial(_p(qi), _p(k), _p(v), d, i, j0, j1, int(causal),
+                                        float(scale), int(tile), int(base2), ctypes.byref(l),
+                                        _p(acc))
+        return m, l.value, acc
+
+    def merge(self, p1, p2, base2: bool = False):
+        """Merge two partial states (m, l, acc) of one row."""
+        m1, l1, a1 = p1
+        m2, l2, a2 = p2
+        a1, a2 = _f64(a1), _f64(a2)
+        out = np.empty_like(a1)
+        l = ctypes.c_double()
+        m = self.lib.oracle_merge(float(m1), float(l1), _p(a1), float(m2), float(l2), _p(a2),
+                                  a1.shape[0], int(base2), ctypes.byref(l), _p(out))
+        return m, l.value, out
+
+
+_default = None
+
+
+def get() -> Oracle:
+    """The oracle compiled from this directory's ``fa_oracle.c``."""
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def num_threads() -> int:
+    return get().num_threads()
+
+
+def fwd(q, k, v, causal: bool, scale: float):
+    return get().fwd(q, k, v, causal, scale)
+
+
+def bwd(q, k, v, do, causal: bool, scale: float):
+    return get().bwd(q, k, v, do, causal, scale)
+
+
+def fwd_online(q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):
+    return get().fwd_online(q, k, v, causal, scale, tile, base2)
+
+
+def row_partial(qi, k, v, i, j0, j1, causal, scale, tile, base2=False):
+    return get().row_partial(qi, k, v, i, j0, j1, causal, scale, tile, base2)
+
+
+def merge(p1, p2, base2: bool = False):
+    return get().merge(p1, p2, base2)

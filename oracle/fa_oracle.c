@@ -1,0 +1,264 @@
+/*
+ * fa_oracle.c -- plain, slow, fp64 CPU oracle for exact attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only the tests, the package's smoke check and the CPU
+ * baseline leg of the benchmark do.  It shares no code, header or constant
+ * with the CUDA kernels.
+ *
+ * What it computes (all arithmetic in fp64, on the 16-bit input values
+ * upcast exactly by the caller):
+ *
+ *   Exact attention, "flash-attn-triton" docs page, section "The argument"
+ *   (ordinary attention: S = Q K^T / sqrt(d), softmax by rows, P V) and the
+ *   FlashAttention note (narrativegoldmine), section "Key Mechanisms"
+ *   (causal = lower-triangular mask).  With a caller-given scale:
+ *       S_ij = scale * <q_i, k_j>,  j allowed iff (!causal || j <= i)
+ *       m_i  = max_j S_ij,  l_i = sum_j exp(S_ij - m_i)
+ *       P_ij = exp(S_ij - m_i) / l_i,  O_i = sum_j P_ij v_j
+ *       L_i  = m_i + ln(l_i)        (natural-log logsumexp of scaled scores)
+ *   A row with no allowed key (never produced by square causal masks) gets
+ *   O_i = 0 and L_i = -inf: the tutorial page ("Start with a safe softmax")
+ *   asks for fully masked rows to be handled but fixes no convention.
+ *
+ *   Backward: the docs page, section "Scope", says the backward rebuilds P
+ *   from the saved L; the pages print no gradient formulas.  The oracle uses
+ *   the plain chain rule of the definition above with upstream gradient dO:
+ *       dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,
+ *       dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+ *   (Pinned by finite differences in the tests.)
+ *
+ *   A separate, naive online-softmax oracle follows the per-tile update of
+ *   the docs page, section "Tiling softmax is exact algebra", Fig. 3
+ *   (running max m, running sum l, correction alpha = exp(m_old - m_new)
+ *   applied to l and acc together, one divide after the loop), in base e or
+ *   in base 2 with log2(e) folded into the scale.  A partial-state merge
+ *   (tutorial page, "Softmax in pieces": merging two partial results) is
+ *   exposed for the merge pins.
+ *
+ * Layout: Q, K, V, O, dO, dQ, dK, dV are dense row-major (B, H, N, d) fp64;
+ * L and D are (B, H, N) fp64.  Heads are independent; OpenMP runs over the
+ * B*H (batch, head) pairs, each pair owned by one thread.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double dot(const double* a, const double* b, int d)
+{
+    double s = 0.0;
+    for (int c = 0; c < d; ++c) s += a[c] * b[c];
+    return s;
+}
+
+static int n_allowed(int i, int N, int causal) { return causal ? (i + 1 < N ? i + 1 : N) : N; }
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Scores of row i against its allowed keys, then the softmax statistics.
+ * s[0..nk) receives S_ij; returns m, writes l.  nk == 0 -> m = -inf, l = 0. */
+static double row_scores(const double* qi, const double* k, int nk, int d, double scale,
+                         double* s, double* l_out)
+{
+    double m = -INFINITY;
+    for (int j = 0; j < nk; ++j) {
+        s[j] = scale * dot(qi, k + (long)j * d, d);
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int j = 0; j < nk; ++j) l += exp(s[j] - m);
+    *l_out = l;
+    return m;
+}
+
+void oracle_fwd(const double* Q, const double* K, const double* V, double* O, double* L,
+                int B, int H, int N, int d, int causal, double scale)
+{
+    long BH = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh) {
+        const double* q = Q + bh * N * d;
+        const double* k = K + bh * N * d;
+        const double* v = V + bh * N * d;
+        double* o = O + bh * N * d;
+        double* lse = L + bh * N;
+        double* s = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
+        for (int i = 0; i < N; ++i) {
+            int nk = n_allowed(i, N, causal);
+            double l;
+            double m = row_scores(q + (long)i * d, k, nk, d, scale, s, &l);
+            double* oi = o + (long)i * d;
+            for (int c = 0; c < d; ++c) oi[c] = 0.0;
+            if (nk == 0) { lse[i] = -INFINITY; continue; }
+            for (int j = 0; j < nk; ++j) {
+                double p = exp(s[j] - m) / l;
+                const double* vj = v + (long)j * d;
+                for (int c = 0; c < d; ++c) oi[c] += p * vj[c];
+            }
+            lse[i] = m + log(l);
+        }
+        free(s);
+    }
+}
+
+void oracle_bwd(const double* Q, const double* K, const double* V, const double* dO,
+                double* dQ, double* dK, double* dV, double* Dout,
+                int B, int H, int N, int d, int causal, double scale)
+{
+    long BH = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh) {
+        const double* q = Q + bh * N * d;
+        const double* k = K + bh * N * d;
+        const double* v = V + bh * N * d;
+        const double* dout = dO + bh * N * d;
+        double* dq = dQ + bh * N * d;
+        double* dk = dK + bh * N * d;
+        double* dv = dV + bh * N * d;
+        double* Dh = Dout + bh * N;
+        memset(dk, 0, sizeof(double) * N * d);
+        memset(dv, 0, sizeof(double) * N * d);
+        double* s = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
+        double* oi = (double*)malloc(sizeof(double) * (d > 0 ? d : 1));
+        for (int i = 0; i < N; ++i) {
+            int nk = n_allowed(i, N, causal);
+            const double* qi = q + (long)i * d;
+            const double* doi = dout + (long)i * d;
+            double* dqi = dq + (long)i * d;
+            for (int c = 0; c < d; ++c) { dqi[c] = 0.0; oi[c] = 0.0; }
+            if (nk == 0) { Dh[i] = 0.0; continue; }
+            double l;
+            double m = row_scores(qi, k, nk, d, scale, s, &l);
+            /* s[j] <- P_ij, and O_i = sum_j P_ij v_j */
+            for (int j = 0; j < nk; ++j) {
+                s[j] = exp(s[j] - m) / l;
+                const double* vj = v + (long)j * d;
+                for (int c = 0; c < d; ++c) oi[c] += s[j] * vj[c];
+            }
+            double Di = dot(doi, oi, d);
+            Dh[i] = Di;
+            for (int j = 0; j < nk; ++j) {
+                double pij = s[j];
+                double dpij = dot(doi, v + (long)j * d, d);
+                double dsij = pij * (dpij - Di);
+                const double* kj = k + (long)j * d;
+                double* dkj = dk + (long)j * d;
+                double* dvj = dv + (long)j * d;
+                for (int c = 0; c < d; ++c) {
+                    dqi[c] += scale * dsij * kj[c];
+                    dkj[c] += scale * dsij * qi[c];
+                    dvj[c] += pij * doi[c];
+                }
+            }
+        }
+        free(oi);
+        free(s);
+    }
+}
+
+/* ---- naive online-softmax oracle (Fig. 3 of the docs page) -------------- */
+
+/* Partial state of one query row over keys [j0, j1): running max m, running
+ * sum l of exp(s - m) and the undivided output acc (length d).  base2 != 0
+ * works in base 2 with the scale already multiplied by log2(e), as the docs
+ * page's Fig. 3 does; m is then in the log2 domain.  Tiles of size T walk the
+ * range in order.  Returns m; l and acc are written. */
+double oracle_row_partial(const double* qi, const double* K, const double* V, int d,
+                          int i, int j0, int j1, int causal, double scale, int T, int base2,
+                          double* l_out, double* acc)
+{
+    const double log2e = 1.4426950408889634073599246810019;
+    double c = base2 ? scale * log2e : scale;
+    double m = -INFINITY, l = 0.0;
+    for (int t = 0; t < d; ++t) acc[t] = 0.0;
+    if (T < 1) T = 1;
+    double* s = (double*)malloc(sizeof(double) * T);
+    for (int t0 = j0; t0 < j1; t0 += T) {
+        int t1 = t0 + T < j1 ? t0 + T : j1;
+        double mt = -INFINITY;
+        for (int j = t0; j < t1; ++j) {
+            int masked = causal && j > i;
+            s[j - t0] = masked ? -INFINITY : c * dot(qi, K + (long)j * d, d);
+            if (s[j - t0] > mt) mt = s[j - t0];
+        }
+        double m_new = mt > m ? mt : m;
+        if (m_new == -INFINITY) continue;       /* nothing allowed seen yet */
+        double alpha = base2 ? exp2(m - m_new) : exp(m - m_new);   /* m = -inf -> 0 */
+        double psum = 0.0;
+        for (int t = 0; t < d; ++t) acc[t] *= alpha;
+        for (int j = t0; j < t1; ++j) {
+            double p = base2 ? exp2(s[j - t0] - m_new) : exp(s[j - t0] - m_new);
+            psum += p;
+            if (p != 0.0) {
+                const double* vj = V + (long)j * d;
+                for (int t = 0; t < d; ++t) acc[t] += p * vj[t];
+            }
+        }
+        l = l * alpha + psum;
+        m = m_new;
+    }
+    free(s);
+    *l_out = l;
+    return m;
+}
+
+/* Merge two partial states of the same row (same domain).  exp(-inf - (-inf))
+ * is taken as 0 so that an empty partial merges as the identity. */
+double oracle_merge(double m1, double l1, const double* acc1,
+                    double m2, double l2, const double* acc2,
+                    int d, int base2, double* l_out, double* acc_out)
+{
+    double m = m1 > m2 ? m1 : m2;
+    double a1, a2;
+    if (m == -INFINITY) { a1 = 0.0; a2 = 0.0; }
+    else {
+        a1 = base2 ? exp2(m1 - m) : exp(m1 - m);
+        a2 = base2 ? exp2(m2 - m) : exp(m2 - m);
+    }
+    for (int t = 0; t < d; ++t) acc_out[t] = a1 * acc1[t] + a2 * acc2[t];
+    *l_out = a1 * l1 + a2 * l2;
+    return m;
+}
+
+/* Whole forward by the online update with key tiles of size T (T need not
+ * divide N).  Finishes with one divide per row and L = m + ln(l) (base e), or
+ * L = (m + log2(l)) * ln(2) when the state is in base 2, so that L is the
+ * natural-log logsumexp in both cases. */
+void oracle_fwd_online(const double* Q, const double* K, const double* V, double* O, double* L,
+                       int B, int H, int N, int d, int causal, double scale, int T, int base2)
+{
+    const double ln2 = 0.69314718055994530941723212145818;
+    long BH = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh) {
+        const double* q = Q + bh * N * d;
+        const double* k = K + bh * N * d;
+        const double* v = V + bh * N * d;
+        double* o = O + bh * N * d;
+        double* lse = L + bh * N;
+        for (int i = 0; i < N; ++i) {
+            double l;
+            double* oi = o + (long)i * d;
+            double m = oracle_row_partial(q + (long)i * d, k, v, d, i, 0, N, causal, scale, T,
+                                          base2, &l, oi);
+            if (l == 0.0) {
+                for (int t = 0; t < d; ++t) oi[t] = 0.0;
+                lse[i] = -INFINITY;
+                continue;
+            }
+            for (int t = 0; t < d; ++t) oi[t] /= l;
+            lse[i] = base2 ? (m + log2(l)) * ln2 : m + log(l);
+        }
+    }
+}

@@ -1,0 +1,262 @@
+"""Pins that tie the fp64 oracle to facts other than itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with a closed form, an invariant, a library special case,
+finite differences or a size printed on the pages.  ``tests/test_oracle.py``
+runs them on the real oracle; ``tests/test_oracle_mutations.py`` runs them on
+copies of the oracle with one planted mistake each and expects a failure.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    if a.size == 0:
+        return
+    fin = np.isfinite(b)
+    assert np.array_equal(np.isfinite(a), fin), f"{what}: finiteness differs"
+    err = float(np.max(np.abs(a[fin] - b[fin]))) if fin.any() else 0.0
+    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.1e}"
+    assert np.array_equal(a[~fin], b[~fin]), f"{what}: non-finite values differ"
+
+
+def pin_rows_sum_to_one(orc):
+    """With V = I (d = N), O equals P itself: rows sum to 1, entries >= 0, and under the
+    causal mask the strict upper triangle is exactly 0 (docs page, 'Tiling softmax is exact
+    algebra'; FlashAttention note, causal masking)."""
+    rng = np.random.default_rng(1)
+    N = 37
+    q = _rand(rng, 1, 2, N, N)
+    k = _rand(rng, 1, 2, N, N)
+    v = np.broadcast_to(np.eye(N), (1, 2, N, N)).copy()
+    for causal in (False, True):
+        P, _ = orc.fwd(q, k, v, causal, 1.0 / math.sqrt(N))
+        _close(P.sum(-1), np.ones((1, 2, N)), 1e-12, "row sums of P")
+        assert (P >= 0).all(), "P has negative entries"
+        if causal:
+            upper = np.triu(np.ones((N, N), dtype=bool), 1)
+            assert (P[..., upper] == 0).all(), "causal P leaks above the diagonal"
+        else:
+            assert (P > 0).all(), "full P has zero entries"
+
+
+def pin_constant_keys(orc):
+    """All keys equal: P is uniform over the allowed keys.  Full: O_i = mean(V) and
+    L_i = scale q_i.k + ln N.  Causal: O_i = mean(V_0..V_i), L_i = scale q_i.k + ln(i+1).
+    The gradient w.r.t. Q vanishes and dV_j collects dO_i / (#allowed keys of row i)."""
+    rng = np.random.default_rng(2)
+    B, H, N, d = 2, 3, 29, 8
+    scale = 0.37
+    q = _rand(rng, B, H, N, d)
+    kv = _rand(rng, B, H, 1, d)
+    k = np.repeat(kv, N, axis=2)
+    v = _rand(rng, B, H, N, d)
+    do = _rand(rng, B, H, N, d)
+    qk = scale * np.einsum("bhnd,bhd->bhn", q, kv[:, :, 0])
+    for causal in (False, True):
+        o, lse = orc.fwd(q, k, v, causal, scale)
+        if causal:
+            cnt = np.arange(1, N + 1, dtype=np.float64)
+            o_ref = np.cumsum(v, axis=2) / cnt[None, None, :, None]
+            l_ref = qk + np.log(cnt)[None, None, :]
+            dv_ref = np.cumsum((do / cnt[None, None, :, None])[:, :, ::-1], axis=2)[:, :, ::-1]
+        else:
+            o_ref = np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape)
+            l_ref = qk + math.log(N)
+            dv_ref = np.broadcast_to(do.mean(axis=2, keepdims=True), o.shape)
+        _close(o, o_ref, 1e-12, f"O with constant K (causal={causal})")
+        _close(lse, l_ref, 1e-12, f"L with constant K (causal={causal})")
+        dq, dk, dv, _ = orc.bwd(q, k, v, do, causal, scale)
+        _close(dq, np.zeros_like(dq), 1e-12, "dQ with constant K")
+        _close(dv, dv_ref, 1e-12, "dV with constant K")
+
+
+def pin_causal_first_row(orc):
+    """Causal row 0 sees only key 0: O_0 = V_0 and L_0 = scale q_0.k_0."""
+    rng = np.random.default_rng(3)
+    B, H, N, d = 1, 4, 17, 16
+    scale = 0.25
+    q, k, v = _rand(rng, B, H, N, d), _rand(rng, B, H, N, d), _rand(rng, B, H, N, d)
+    o, lse = orc.fwd(q, k, v, True, scale)
+    _close(o[:, :, 0], v[:, :, 0], 1e-13, "causal O_0")
+    _close(lse[:, :, 0], scale * np.sum(q[:, :, 0] * k[:, :, 0], -1), 1e-13, "causal L_0")
+
+
+def pin_online_matches_safe(orc):
+    """The per-tile online update (docs page Fig. 3) equals the safe softmax for any tile
+    size, including sizes that do not divide N and T = 1, in base e and in base 2."""
+    rng = np.random.default_rng(4)
+    B, H, N, d = 1, 2, 50, 12
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = 3 * _rand(rng, B, H, N, d), 3 * _rand(rng, B, H, N, d), _rand(rng, B, H, N, d)
+    for causal in (False, True):
+        o_ref, l_ref = orc.fwd(q, k, v, causal, scale)
+        for T in (1, 3, 7, 16, 49, 50, 64):
+            for base2 in (False, True):
+                o, lse = orc.fwd_online(q, k, v, causal, scale, T, base2)
+                _close(o, o_ref, 1e-12, f"online O (T={T}, base2={base2}, causal={causal})")
+                _close(lse, l_ref, 1e-12, f"online L (T={T}, base2={base2}, causal={causal})")
+
+
+def pin_L_is_logsumexp(orc):
+    """L is the natural-log logsumexp of the scaled, masked scores (scipy's logsumexp on
+    scores formed by a numpy matmul)."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(5)
+    B, H, N, d = 2, 2, 33, 20
+    scale = 0.4
+    q, k, v = 2 * _rand(rng, B, H, N, d), 2 * _rand(rng, B, H, N, d), _rand(rng, B, H, N, d)
+    s = scale * np.einsum("bhid,bhjd->bhij", q, k)
+    for causal in (False, True):
+        sm = s.copy()
+        if causal:
+            sm[..., np.triu(np.ones((N, N), dtype=bool), 1)] = -np.inf
+        _, lse = orc.fwd(q, k, v, causal, scale)
+        _close(lse, logsumexp(sm, axis=-1), 1e-12, f"L vs logsumexp (causal={causal})")
+
+
+def pin_merge(orc):
+    """Two partial results merge into the whole (tutorial page, 'Softmax in pieces'): any
+    split point, any order, associatively; an empty partial is the identity."""
+    rng = np.random.default_rng(6)
+    N, d = 41, 9
+    scale = 0.5
+    qi = 2 * _rand(rng, d)
+    k, v = 2 * _rand(rng, N, d), _rand(rng, N, d)
+    i = N - 1
+    for base2 in (False, True):
+        whole = orc.row_partial(qi, k, v, i, 0, N, False, scale, 5, base2)
+        for a in (1, 13, 40):
+            p1 = orc.row_partial(qi, k, v, i, 0, a, False, scale, 4, base2)
+            p2 = orc.row_partial(qi, k, v, i, a, N, False, scale, 6, base2)
+            for m in (orc.merge(p1, p2, base2), orc.merge(p2, p1, base2)):
+                assert abs(m[0] - whole[0]) <= 1e-12, "merged max differs"
+                assert abs(m[1] / whole[1] - 1) <= 1e-12, "merged sum differs"
+                _close(m[2] / m[1], whole[2] / whole[1], 1e-12, "merged output differs")
+        p1 = orc.row_partial(qi, k, v, i, 0, 10, False, scale, 3, base2)
+        p2 = orc.row_partial(qi, k, v, i, 10, 30, False, scale, 3, base2)
+        p3 = orc.row_partial(qi, k, v, i, 30, N, False, scale, 3, base2)
+        left = orc.merge(orc.merge(p1, p2, base2), p3, base2)
+        right = orc.merge(p1, orc.merge(p2, p3, base2), base2)
+        perm = orc.merge(orc.merge(p3, p1, base2), p2, base2)
+        for m in (left, right, perm):
+            assert abs(m[0] - whole[0]) <= 1e-12
+            assert abs(m[1] / whole[1] - 1) <= 1e-12
+            _close(m[2] / m[1], whole[2] / whole[1], 1e-12, "3-way merge output")
+        empty = (-math.inf, 0.0, np.zeros(d))
+        m = orc.merge(empty, whole, base2)
+        assert m[0] == whole[0] and m[1] == whole[1]
+        _close(m[2], whole[2], 0.0, "merge with the empty partial")
+        m = orc.merge(empty, empty, base2)
+        assert m[0] == -math.inf and m[1] == 0.0 and not np.isnan(m[2]).any()
+    # the finished row equals the forward's row (base e: L = m + ln l)
+    whole = orc.row_partial(qi, k, v, i, 0, N, False, scale, 5, False)
+    q = np.zeros((1, 1, N, d))
+    q[0, 0, i] = qi
+    o, lse = orc.fwd(q, k[None, None], v[None, None], False, scale)
+    _close(whole[2] / whole[1], o[0, 0, i], 1e-12, "finished partial vs forward")
+    assert abs(whole[0] + math.log(whole[1]) - lse[0, 0, i]) <= 1e-12
+
+
+def _loss(orc, q, k, v, do, causal, scale):
+    o, _ = orc.fwd(q, k, v, causal, scale)
+    return float(np.sum(o * do))
+
+
+def pin_finite_differences(orc):
+    """Central differences of loss = sum(O o dO) match dQ, dK, dV (relative error < 1e-6)
+    on tiny shapes; D equals rowsum(dO o O)."""
+    rng = np.random.default_rng(7)
+    h = 1e-6
+    for N in (1, 2, 5, 7):
+        for d in (1, 3, 4):
+            for causal in (False, True):
+                scale = 0.9
+                q, k, v, do = (_rand(rng, 1, 1, N, d) for _ in range(4))
+                dq, dk, dv, D = orc.bwd(q, k, v, do, causal, scale)
+                o, _ = orc.fwd(q, k, v, causal, scale)
+                _close(D, np.sum(o * do, -1), 1e-13, "D = rowsum(dO o O)")
+                for name, x, g in (("dQ", q, dq), ("dK", k, dk), ("dV", v, dv)):
+                    fd = np.zeros_like(x)
+                    for idx in np.ndindex(x.shape):
+                        xp, xm = x.copy(), x.copy()
+                        xp[idx] += h
+                        xm[idx] -= h
+                        args_p = {"q": q, "k": k, "v": v}
+                        args_m = dict(args_p)
+                        key = name[1].lower()
+                        args_p[key], args_m[key] = xp, xm
+                        fd[idx] = (_loss(orc, args_p["q"], args_p["k"], args_p["v"], do, causal,
+                                         scale)
+                                   - _loss(orc, args_m["q"], args_m["k"], args_m["v"], do, causal,
+                                           scale)) / (2 * h)
+                    ref = max(float(np.max(np.abs(fd))), 1e-3)
+                    err = float(np.max(np.abs(fd - g))) / ref
+                    assert err < 1e-6, f"finite differences {name} N={N} d={d} causal={causal}: {err:.2e}"
+
+
+def pin_gradient_invariants(orc):
+    """Rows of dS sum to 0, so the dK rows sum to 0; rows of P sum to 1, so the dV rows sum
+    to the dO rows."""
+    rng = np.random.default_rng(8)
+    B, H, N, d = 2, 2, 45, 16
+    q, k, v, do = (_rand(rng, B, H, N, d) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv, _ = orc.bwd(q, k, v, do, causal, 0.3)
+        _close(dk.sum(axis=2), np.zeros((B, H, d)), 1e-11, "sum_j dK_j")
+        _close(dv.sum(axis=2), do.sum(axis=2), 1e-11, "sum_j dV_j")
+
+
+def pin_torch_sdpa(orc, shapes=((1, 1, 128, 64, False), (2, 3, 100, 32, True),
+                                (4, 8, 1000, 32, True))):
+    """Library special case: torch's scaled_dot_product_attention in fp64 on the CPU, with
+    autograd for the gradients."""
+    import torch
+    rng = np.random.default_rng(9)
+    for B, H, N, d, causal in shapes:
+        scale = 1.0 / math.sqrt(d)
+        q, k, v, do = (_rand(rng, B, H, N, d) for _ in range(4))
+        tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal,
+                                                              scale=scale)
+        to.backward(torch.tensor(do, dtype=torch.float64))
+        o, _ = orc.fwd(q, k, v, causal, scale)
+        dq, dk, dv, _ = orc.bwd(q, k, v, do, causal, scale)
+        _close(o, to.detach().numpy(), 1e-10, f"O vs SDPA {B, H, N, d, causal}")
+        _close(dq, tq.grad.numpy(), 1e-10, f"dQ vs SDPA {B, H, N, d, causal}")
+        _close(dk, tk.grad.numpy(), 1e-10, f"dK vs SDPA {B, H, N, d, causal}")
+        _close(dv, tv.grad.numpy(), 1e-10, f"dV vs SDPA {B, H, N, d, causal}")
+
+
+def pin_page_sizes(iomodel):
+    """Sizes the pages print (tests/golden/page_sizes.json) from the byte model."""
+    with open(os.path.join(GOLDEN, "page_sizes.json")) as f:
+        cases = json.load(f)["cases"]
+    c0, c1, c2, c3 = cases
+    assert iomodel.score_matrix_bytes(c0["B"], c0["H"], c0["N"], c0["elem_bytes"]) == c0["bytes"]
+    assert c0["bytes"] == 128 * 2**20
+    e = iomodel.score_entries(c1["N"])
+    assert abs(e / c1["entries_approx"] - 1) <= c1["rel_tol"]
+    assert iomodel.tile_bytes(c2["block_m"], c2["block_n"], c2["elem_bytes"]) == c2["bytes"]
+    assert c2["bytes"] == 32 * 2**10
+    r = iomodel.tiled_hbm_ratio(c3["d"], c3["sram_bytes"])
+    assert abs(r / c3["ratio_approx"] - 1) <= c3["rel_tol"]
+
+
+ORACLE_PINS = [pin_rows_sum_to_one, pin_constant_keys, pin_causal_first_row,
+               pin_online_matches_safe, pin_L_is_logsumexp, pin_merge, pin_finite_differences,
+               pin_gradient_invariants, pin_torch_sdpa]

@@ -1,0 +1,60 @@
+"""Each planted mistake in a copy of the oracle must fail at least one pin.
+
+The mistakes are the plausible ones: a dropped term, a wrong sign, a shifted
+index, a transposed operand, a wrong log base.  Every mutant is compiled from
+a textual edit of ``oracle/fa_oracle.c`` into a temporary directory; the real
+oracle is untouched.
+"""
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "fa_oracle.c")
+
+MUTANTS = {
+    "dK drops the scale": ("dkj[c] += scale * dsij * qi[c];", "dkj[c] += dsij * qi[c];"),
+    "dQ drops the scale": ("dqi[c] += scale * dsij * kj[c];", "dqi[c] += dsij * kj[c];"),
+    "dS sign flipped": ("double dsij = pij * (dpij - Di);", "double dsij = pij * (dpij + Di);"),
+    "dS drops D": ("double dsij = pij * (dpij - Di);", "double dsij = pij * dpij;"),
+    "dV transposed operand": ("dvj[c] += pij * doi[c];",
+                              "dvj[c] += pij * dout[(long)j * d + c];"),
+    "causal mask shifted": ("causal ? (i + 1 < N ? i + 1 : N) : N",
+                            "causal ? (i + 2 < N ? i + 2 : N) : N"),
+    "L in log2": ("lse[i] = m + log(l);", "lse[i] = m + log2(l);"),
+    "sum without max subtraction": ("for (int j = 0; j < nk; ++j) l += exp(s[j] - m);",
+                                    "for (int j = 0; j < nk; ++j) l += exp(s[j]);"),
+    "online: alpha not applied to l": ("l = l * alpha + psum;", "l = l + psum;"),
+    "online: alpha not applied to acc": ("for (int t = 0; t < d; ++t) acc[t] *= alpha;",
+                                         "for (int t = 0; t < d; ++t) acc[t] *= 1.0;"),
+    "merge: wrong weight": ("*l_out = a1 * l1 + a2 * l2;", "*l_out = a1 * l1 + a1 * l2;"),
+    "scores transposed (k_i . q_j)": (
+        "double m = row_scores(q + (long)i * d, k, nk, d, scale, s, &l);\n            double* oi = o",
+        "double m = row_scores(k + (long)i * d, q, nk, d, scale, s, &l);\n            double* oi = o"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    before, after = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(before) == 1, f"mutation anchor not unique: {before!r}"
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(before, after))
+    so = oracle.build(force=True, src=str(src), out=str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(so)
+    failures = []
+    for pin in pins.ORACLE_PINS:
+        if pin is pins.pin_torch_sdpa:
+            try:
+                pin(orc, shapes=((1, 2, 37, 8, False), (1, 2, 37, 8, True)))
+            except AssertionError as e:
+                failures.append(pin.__name__)
+            continue
+        try:
+            pin(orc)
+        except AssertionError:
+            failures.append(pin.__name__)
+    assert failures, f"no pin caught the planted mistake '{name}'"
