@@ -1,0 +1,387 @@
+#!/usr/bin/env python
+"""Benchmark of exact attention forward + backward on GB300.
+
+One step = the whole hot path over one batch of synthetic input: the forward
+(O, L) and the backward (D pre-pass, dK/dV, dQ) of attention for the long-
+context workload B=1, H=32, N=8192, d=128, bf16, causal.  Inputs are resident
+in HBM before timing; the four inputs (256 MiB) and the per-kernel working sets
+exceed the 126 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  FLOPs follow the usual convention: 4*B*H*N^2*d
+forward, 2.5x that backward, halved when causal.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores instead (one
+(batch, head) pair of the same workload per step); it is the slow definition,
+reported for scale, not a target.
+Multi-GPU (torchrun): every rank runs its own full copy of the workload
+(independent problems, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s (N=8K,d=128,bf16,causal); % of GB300 tensor peak"
+WORKLOADS = {
+    # name: (B, H, N, d, dtype, causal)
+    "n8k_causal_d128_bf16": (1, 32, 8192, 128, "bf16", True),
+    "n16k_causal_d128_bf16": (1, 32, 16384, 128, "bf16", True),
+    "n4k_causal_d128_bf16": (2, 16, 4096, 128, "bf16", True),
+    "n4k_full_d128_bf16": (2, 16, 4096, 128, "bf16", False),
+    "gpt2m_causal_d64_fp16": (8, 16, 1024, 64, "fp16", True),
+}
+DEFAULT_WORKLOAD = "n8k_causal_d128_bf16"
+KERNEL_SOURCES = {
+    "fwd_kernel": "exact_io_aware_22_gb300/csrc/fa_fwd.cu",
+    "bwd_pre_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
+    "bwd_dkdv_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
+    "bwd_dq_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
+}
+
+
+def attn_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    if causal:
+        f *= 0.5
+    return f, 2.5 * f
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def traffic_from_profiles(kernel: str, workload: str):
+    """dram bytes per launch recorded in profiles/<kernel>__<workload>.txt, or None when
+    the file is missing or the kernel's source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.txt")
+    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b:
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return float(m_b.group(1)) if sha == m_sha.group(1) else None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str, period_ms: int = 20):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", gpu_id, "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(x, B, H, N, d, causal, scale, budget_s=10.0, max_heads=8):
+    """Time the fp64 oracle as it stands on the host cores over whole (batch, head) pairs
+    of the workload until ``budget_s`` is spent (at least one pair)."""
+    import numpy as np
+    import oracle
+    fwd_f, bwd_f = attn_flops(1, 1, N, d, causal)
+    heads, t_total = 0, 0.0
+    flat = {n: x[n].reshape(B * H, N, d) for n in ("q", "k", "v", "do")}
+    while heads < min(max_heads, B * H) and (heads == 0 or t_total < budget_s):
+        sel = {n: flat[n][heads:heads + 1].double().numpy()[None] for n in flat}
+        t0 = time.perf_counter()
+        oracle.fwd(sel["q"], sel["k"], sel["v"], causal, scale)
+        oracle.bwd(sel["q"], sel["k"], sel["v"], sel["do"], causal, scale)
+        t_total += time.perf_counter() - t0
+        heads += 1
+    value = heads * (fwd_f + bwd_f) / t_total / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{heads} of {B * H} (batch, head) pairs, full N={N}, fwd+bwd, "
+                      f"{t_total:.1f} s on host cores"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from exact_io_aware_22_gb300 import inputs
+    B, H, N, d, dtype, causal = WORKLOADS[args.workload]
+    scale = 1.0 / math.sqrt(d)
+    x = inputs.make_inputs(B, H, N, d, dtype, seed=0)
+    flat = {n: x[n].reshape(B * H, N, d) for n in ("q", "k", "v", "do")}
+    fwd_f, bwd_f = attn_flops(1, 1, N, d, causal)
+
+    def step(i):
+        h = i % (B * H)
+        sel = {n: flat[n][h:h + 1].double().numpy()[None] for n in flat}
+        oracle.fwd(sel["q"], sel["k"], sel["v"], causal, scale)
+        oracle.bwd(sel["q"], sel["k"], sel["v"], sel["do"], causal, scale)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    ms = dt / args.steps * 1e3
+    value = (fwd_f + bwd_f) / (ms / 1e3) / 1e12
+    sample = f"one (batch, head) pair per step, full N={N}, fwd+bwd, fp64 oracle"
+    out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                      "step_unit": "one (batch, head) pair"},
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import exact_io_aware_22_gb300 as fa
+    from exact_io_aware_22_gb300 import inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    B, H, N, d, dtype, causal = WORKLOADS[args.workload]
+    scale = 1.0 / math.sqrt(d)
+    fwd_f, bwd_f = attn_flops(B, H, N, d, causal)
+    x = inputs.make_inputs(B, H, N, d, dtype, seed=rank)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.bwd_workspace_size(B, H, N, d, causal), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+        fa.bwd(q, k, v, o, lse, do, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.device_status() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout during warm-up")
+
+    try:   # the UUID names this process's GPU whatever CUDA_VISIBLE_DEVICES says
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.2)
+    barrier()
+    torch.cuda.synchronize()
+    fa.trace_enable(True)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    fa.trace_enable(False)
+    clocks = sampler.stop()
+    if fa.device_status() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
+    ms = t0.elapsed_time(t1) / args.steps
+    traced = fa.trace_read()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * (fwd_f + bwd_f) / (ms / 1e3) / 1e12
+    launches = sum(n for _, n in traced.values())
+
+    per = {kname: (tot / n if n else 0.0, n) for kname, (tot, n) in traced.items()}
+    fwd_ms = per["fwd_kernel"][0]
+    bwd_ms = sum(per[kk][0] for kk in ("bwd_pre_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"))
+    peaks = load_peaks()
+    # algorithmic work of one launch of each kernel
+    elem = 2
+    n_bytes = B * H * N * d * elem
+    Np = (N + 127) // 128 * 128
+    alg = {
+        "fwd_kernel": ("tensor", fwd_f),
+        "bwd_dkdv_kernel": ("tensor", 0.8 * bwd_f),     # S, dP recompute, dV, dK: 4 of 5 products
+        "bwd_dq_kernel": ("tensor", 0.2 * bwd_f),       # dQ: 1 of 5 products
+        "bwd_pre_kernel": ("hbm", 2 * n_bytes + 4 * B * H * N + 2 * 4 * B * H * Np),
+    }
+    top = max(traced, key=lambda kk: traced[kk][0])
+    bound, work = alg[top]
+    if bound == "tensor":
+        achieved = work / (per[top][0] / 1e3) / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved = work / (per[top][0] / 1e3) / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    roofline = {"bound": bound, "kernel": top, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": traffic_from_profiles(top, args.workload),
+                "peak_source": f"{peaks['source']} (burst)",
+                "algorithmic_work_per_launch": work,
+                "avg_launch_ms": per[top][0]}
+
+    e2e = None
+    if not args.no_e2e:
+        hx = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        hg = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
+
+        def e2e_step():
+            for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
+                dst.copy_(hx[n], non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            for h_, g_ in zip(hg, (dq, dk, dv)):
+                h_.copy_(g_, non_blocking=True)
+
+        ke = max(1, min(args.steps, 20))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1) / ke
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * (fwd_f + bwd_f) / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 4 * n_bytes, "d2h_bytes_per_step": 4 * n_bytes + 4 * B * H * N,
+               "ms_per_step": ems, "steps": ke}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x, B, H, N, d, causal, scale)
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+               "data": "synthetic",
+               "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d,
+                          "causal": causal, "parallelism": f"replicas x{world}",
+                          "l2": "inputs larger than L2 (256 MiB of Q,K,V,dO), no flush"},
+               "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+               "fwd_tflops": fwd_f / (fwd_ms / 1e3) / 1e12 if fwd_ms else None,
+               "bwd_tflops": bwd_f / (bwd_ms / 1e3) / 1e12 if bwd_ms else None,
+               "frac_of_peak": value / world / peaks["bf16_tflops"],
+               "kernels_ms": {kk: per[kk][0] for kk in per},
+               "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+               "gpu_launches": launches, "clocks": clocks}
+        print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,213 @@
-"""Exact IO-aware attention (FlashAttention-2 forward and backward) for GB300."""
+"""Exact IO-aware attention (FlashAttention-2 forward and backward) for GB300.
+
+Thin ctypes binding over the C ABI in ``include/fa.h`` (``libfa_gb300.so``,
+built for sm_103a by ``exact_io_aware_22_gb300.build``).  This module only
+marshals arguments: it checks tensor devices, dtypes, shapes and contiguity,
+then passes raw device pointers and torch's current CUDA stream to the
+library.  Every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if the library is missing or cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = ["fwd", "bwd", "bwd_workspace_size", "device_status", "set_wait_limit_ns",
+           "selftest_timeout", "trace_enable", "trace_read", "FAError", "library_path", "load_library", "STATUS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libfa_gb300.so")
+
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_UNSUPPORTED",
+          3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+FA_FP16, FA_BF16 = 0, 1
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    """A non-FA_OK status from the library."""
+
+    def __init__(self, code: int, what: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        msg = f"{what}: {self.name}"
+        if code == 4 and _lib is not None:
+            msg += f" (cudaError {_lib.fa_last_cuda_error()})"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load (once) and return the ctypes handle of the CUDA library."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} is missing "
+                           "(run exact_io_aware_22_gb300.build.build())")
+    lib = ctypes.CDLL(p)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_last_cuda_error.restype = i
+    lib.fa_device_status.argtypes = [vp]
+    lib.fa_device_status.restype = i
+    lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.fa_set_wait_limit_ns.restype = i
+    lib.fa_selftest_timeout.argtypes = [ctypes.c_ulonglong, vp]
+    lib.fa_selftest_timeout.restype = i
+    lib.fa_trace_enable.argtypes = [i]
+    lib.fa_trace_enable.restype = i
+    lib.fa_trace_kind_name.argtypes = [i]
+    lib.fa_trace_kind_name.restype = ctypes.c_char_p
+    lib.fa_trace_read.argtypes = [i, ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_longlong)]
+    lib.fa_trace_read.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise FAError(code, what)
+
+
+def _stream():
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return FA_FP16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: fp16 or bf16 expected")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous (B, H, N, d)")
+
+
+def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=None):
+    """O, L = attention(q, k, v) for (B, H, N, d) fp16/bf16 CUDA tensors.
+
+    L is (B, H, N) fp32, the natural-log logsumexp of each row's scaled scores.
+    ``scale`` defaults to 1/sqrt(d).  Runs asynchronously on torch's current stream.
+    """
+    import torch
+    _need_cuda(q, k, v)
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one (B, H, N, d) shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _need_cuda(out, lse)
+    if out.shape != q.shape or out.dtype != q.dtype or lse.shape != (B, H, N) \
+            or lse.dtype != torch.float32:
+        raise ValueError("out must match q; lse must be (B, H, N) fp32")
+    lib = load_library()
+    _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(causal),
+                      float(scale), _dtype_code(q), _stream()), "fa_fwd")
+    return out, lse
+
+
+def bwd_workspace_size(B: int, H: int, N: int, d: int, causal: bool = True) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, H, N, d, int(causal)))
+
+
+def bwd(q, k, v, o, lse, do, causal: bool = True, scale: float | None = None,
+        dq=None, dk=None, dv=None, workspace=None):
+    """dQ, dK, dV of attention for upstream gradient ``do`` (all (B, H, N, d)).
+
+    ``o`` and ``lse`` are the forward's outputs.  ``workspace`` (optional) is a CUDA
+    uint8 tensor of at least ``bwd_workspace_size`` bytes; without it the library
+    takes scratch from the stream-ordered allocator.
+    """
+    import torch
+    _need_cuda(q, k, v, o, lse, do)
+    B, H, N, d = q.shape
+    for t in (k, v, o, do):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("q, k, v, o, do must share one shape and dtype")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32:
+        raise ValueError("lse must be (B, H, N) fp32")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    _need_cuda(dq, dk, dv)
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        _need_cuda(workspace)
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    lib = load_library()
+    _check(lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                      _ptr(dv), ws_ptr, ws_bytes, B, H, N, d, int(causal), float(scale),
+                      _dtype_code(q), _stream()), "fa_bwd")
+    return dq, dk, dv
+
+
+def device_status() -> int:
+    """Synchronise the current stream; return (and clear) the device status code."""
+    return int(load_library().fa_device_status(_stream()))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    _check(load_library().fa_set_wait_limit_ns(int(ns)), "fa_set_wait_limit_ns")
+
+
+def trace_enable(on: bool = True) -> None:
+    """Start (clearing earlier records) or stop the per-kernel CUDA-event trace."""
+    _check(load_library().fa_trace_enable(int(on)), "fa_trace_enable")
+
+
+def trace_read() -> dict:
+    """{kernel name: (total GPU ms, launches)} of the traced launches."""
+    lib = load_library()
+    out = {}
+    k = 0
+    while True:
+        name = lib.fa_trace_kind_name(k)
+        if name is None:
+            break
+        ms, n = ctypes.c_double(), ctypes.c_longlong()
+        _check(lib.fa_trace_read(k, ctypes.byref(ms), ctypes.byref(n)), "fa_trace_read")
+        out[name.decode()] = (ms.value, n.value)
+        k += 1
+    return out
+
+
+def selftest_timeout(limit_ns: int = 1_000_000) -> int:
+    """Run the bounded-wait self test; returns the status code (5 = timeout seen)."""
+    return int(load_library().fa_selftest_timeout(int(limit_ns), _stream()))

@@ -1,0 +1,350 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument validation,
+// TMA tensor-map encoding, workspace handling, the device status word, and
+// dispatch to the forward / backward launchers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+size_t bwd_workspace_bytes(long long BH, int N);
+}
+
+namespace {
+
+// Sticky status word written by kernels whose bounded wait ran out.
+__device__ uint32_t g_status_word;
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+unsigned long long g_wait_limit_ns = 2000000000ull;
+thread_local int g_last_cuda_error = 0;
+
+fa_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return FA_ERR_CUDA;
+}
+
+// Device address of the status word on the current device (resolved once).
+fa_status status_ptr(uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return FA_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+fa_status get_encoder(EncodeTiledFn* fn) {
+  static EncodeTiledFn cached = nullptr;
+  if (!cached) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (q != cudaDriverEntryPointSuccess || !p) return cuda_fail(cudaErrorSymbolNotFound);
+    cached = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  *fn = cached;
+  return FA_OK;
+}
+
+// 3-D map (d, N, B*H) over a dense (B,H,N,d) 16-bit array; box = one 128-row
+// tile of one swizzle width.  Rows >= N of a head read as zeros.
+fa_status make_map(CUtensorMap* m, const void* base, int d, int N, long long BH, bool bf16) {
+  EncodeTiledFn enc;
+  fa_status st = get_encoder(&enc);
+  if (st != FA_OK) return st;
+  const fa::FwdTileInfo ti = fa::fwd_tile_info(d);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(ti.box_cols), static_cast<cuuint32_t>(ti.box_rows),
+                       1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   ti.swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Shared validation of sizes, dtype and scale.
+fa_status check_common(int B, int H, int N, int d, int causal, float scale, int dtype) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_VALUE;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_VALUE;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_VALUE;
+  if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long nblk = (static_cast<long long>(N) + 127) / 128;
+  if (BH > 0x7fffffffLL || nblk * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(N) * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status ctl_for_launch(fa::KernelCtl* ctl) {
+  fa_status st = status_ptr(&ctl->status);
+  if (st != FA_OK) return st;
+  ctl->wait_limit_ns = g_wait_limit_ns;
+  return FA_OK;
+}
+
+__global__ void selftest_wait_kernel(fa::KernelCtl ctl) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = fa::smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    fa::mbar_init(b, 1);
+    fa::fence_mbar_init();
+    // nothing ever arrives: the bounded wait must give up and record it
+    fa::mbar_wait(b, 0, ctl);
+  }
+}
+
+// ---- per-kernel trace: a fixed pool of event pairs, filled in launch order
+constexpr int kTracePool = 4096;
+struct TraceRec {
+  cudaEvent_t start, stop;
+  int kind;
+};
+TraceRec g_trace[kTracePool];
+bool g_trace_created = false;
+bool g_trace_on = false;
+int g_trace_n = 0;
+int g_trace_open = -1;   // record whose stop event is pending
+
+const char* const kTraceNames[fa::TR_NKINDS] = {"fwd_kernel", "bwd_pre_kernel", "bwd_dkdv_kernel",
+                                                "bwd_dq_kernel"};
+
+}  // namespace
+
+namespace fa {
+void trace_begin(int kind, cudaStream_t st) {
+  if (!g_trace_on || g_trace_n >= kTracePool) return;
+  TraceRec& r = g_trace[g_trace_n];
+  if (cudaEventRecord(r.start, st) != cudaSuccess) return;
+  r.kind = kind;
+  g_trace_open = g_trace_n;
+}
+void trace_end(int kind, cudaStream_t st) {
+  if (!g_trace_on || g_trace_open < 0) return;
+  TraceRec& r = g_trace[g_trace_open];
+  g_trace_open = -1;
+  if (r.kind != kind || cudaEventRecord(r.stop, st) != cudaSuccess) return;
+  ++g_trace_n;
+}
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_trace_enable(int on) {
+  if (on) {
+    if (!g_trace_created) {
+      for (int i = 0; i < kTracePool; ++i) {
+        cudaError_t e = cudaEventCreate(&g_trace[i].start);
+        if (e == cudaSuccess) e = cudaEventCreate(&g_trace[i].stop);
+        if (e != cudaSuccess) return cuda_fail(e);
+      }
+      g_trace_created = true;
+    }
+    g_trace_n = 0;
+    g_trace_open = -1;
+  }
+  g_trace_on = on != 0;
+  return FA_OK;
+}
+
+const char* fa_trace_kind_name(int kind) {
+  return (kind >= 0 && kind < fa::TR_NKINDS) ? kTraceNames[kind] : nullptr;
+}
+
+fa_status fa_trace_read(int kind, double* total_ms, long long* launches) {
+  if (!total_ms || !launches || kind < 0 || kind >= fa::TR_NKINDS) return FA_ERR_INVALID_VALUE;
+  double t = 0.0;
+  long long n = 0;
+  for (int i = 0; i < g_trace_n; ++i) {
+    if (g_trace[i].kind != kind) continue;
+    cudaError_t e = cudaEventSynchronize(g_trace[i].stop);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, g_trace[i].start, g_trace[i].stop);
+    if (e != cudaSuccess) return cuda_fail(e);
+    t += ms;
+    ++n;
+  }
+  *total_ms = t;
+  *launches = n;
+  return FA_OK;
+}
+
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_VALUE: return "FA_ERR_INVALID_VALUE: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim, dtype or size not supported";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: pointer alignment rule violated";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call or kernel launch failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up a bounded wait";
+  }
+  return "unknown fa_status";
+}
+
+int fa_last_cuda_error(void) { return g_last_cuda_error; }
+
+fa_status fa_set_wait_limit_ns(unsigned long long ns) {
+  g_wait_limit_ns = ns ? ns : 2000000000ull;
+  return FA_OK;
+}
+
+fa_status fa_device_status(void* stream) {
+  uint32_t* p = nullptr;
+  fa_status st = status_ptr(&p);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const uint32_t zero = 0;
+  e = cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return (v & fa::FA_DEV_TIMEOUT) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+fa_status fa_selftest_timeout(unsigned long long limit_ns, void* stream) {
+  fa::KernelCtl ctl;
+  fa_status st = ctl_for_launch(&ctl);
+  if (st != FA_OK) return st;
+  ctl.wait_limit_ns = limit_ns ? limit_ns : 1000000ull;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ctl);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return fa_device_status(stream);
+}
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                 int N, int d, int causal, float scale, fa_dtype dtype, void* stream) {
+  fa_status st = check_common(B, H, N, d, causal, scale, static_cast<int>(dtype));
+  if (st != FA_OK) return st;
+  if (!Q || !K || !V || !O || !L) return FA_ERR_INVALID_VALUE;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(L, 4))
+    return FA_ERR_MISALIGNED;
+  const long long BH = static_cast<long long>(B) * H;
+  const size_t nbytes = static_cast<size_t>(BH) * N * d * 2, lbytes = static_cast<size_t>(BH) * N * 4;
+  for (const void* in : {Q, K, V})
+    if (overlap(in, nbytes, O, nbytes) || overlap(in, nbytes, L, lbytes)) return FA_ERR_INVALID_VALUE;
+  if (overlap(O, nbytes, L, lbytes)) return FA_ERR_INVALID_VALUE;
+
+  const bool bf16 = dtype == FA_BF16;
+  fa::FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if ((st = make_map(&a.tmQ, Q, d, N, BH, bf16)) != FA_OK) return st;
+  if ((st = make_map(&a.tmK, K, d, N, BH, bf16)) != FA_OK) return st;
+  if ((st = make_map(&a.tmV, V, d, N, BH, bf16)) != FA_OK) return st;
+  if ((st = ctl_for_launch(&a.ctl)) != FA_OK) return st;
+  a.O = O;
+  a.L = L;
+  a.N = N;
+  a.BH = static_cast<int>(BH);
+  a.c_log2 = scale * 1.4426950408889634f;
+  cudaError_t e = fa::launch_fwd(a, d, bf16, causal != 0, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
+  if (check_common(B, H, N, d, causal, 1.0f, FA_FP16) != FA_OK) return 0;
+  return fa::bwd_workspace_bytes(static_cast<long long>(B) * H, N);
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                 size_t workspace_bytes, int B, int H, int N, int d, int causal, float scale,
+                 fa_dtype dtype, void* stream) {
+  fa_status st = check_common(B, H, N, d, causal, scale, static_cast<int>(dtype));
+  if (st != FA_OK) return st;
+  if (!Q || !K || !V || !O || !dO || !L || !dQ || !dK || !dV) return FA_ERR_INVALID_VALUE;
+  for (const void* p : {Q, K, V, O, dO, static_cast<const void*>(dQ), static_cast<const void*>(dK),
+                        static_cast<const void*>(dV)})
+    if (!aligned(p, 16)) return FA_ERR_MISALIGNED;
+  if (!aligned(L, 4) || (workspace && !aligned(workspace, 16))) return FA_ERR_MISALIGNED;
+  const long long BH = static_cast<long long>(B) * H;
+  const size_t need = fa::bwd_workspace_bytes(BH, N);
+  if (workspace && workspace_bytes < need) return FA_ERR_INVALID_VALUE;
+  const size_t nbytes = static_cast<size_t>(BH) * N * d * 2, lbytes = static_cast<size_t>(BH) * N * 4;
+  const void* outs[3] = {dQ, dK, dV};
+  for (int i = 0; i < 3; ++i) {
+    for (const void* in : {Q, K, V, O, dO})
+      if (overlap(in, nbytes, outs[i], nbytes)) return FA_ERR_INVALID_VALUE;
+    if (overlap(L, lbytes, outs[i], nbytes)) return FA_ERR_INVALID_VALUE;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i], nbytes, outs[j], nbytes)) return FA_ERR_INVALID_VALUE;
+    if (workspace && overlap(workspace, need, outs[i], nbytes)) return FA_ERR_INVALID_VALUE;
+  }
+
+  const bool bf16 = dtype == FA_BF16;
+  fa::BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if ((st = make_map(&a.tmQ, Q, d, N, BH, bf16)) != FA_OK) return st;
+  if ((st = make_map(&a.tmK, K, d, N, BH, bf16)) != FA_OK) return st;
+  if ((st = make_map(&a.tmV, V, d, N, BH, bf16)) != FA_OK) return st;
+  if ((st = make_map(&a.tmO, O, d, N, BH, bf16)) != FA_OK) return st;
+  if ((st = make_map(&a.tmdO, dO, d, N, BH, bf16)) != FA_OK) return st;
+  if ((st = ctl_for_launch(&a.ctl)) != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  bool owned = false;
+  if (!ws) {
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    owned = true;
+  }
+  a.O = O;
+  a.dO = dO;
+  a.L = L;
+  a.Dvec = static_cast<float*>(ws);
+  a.dQ = dQ;
+  a.dK = dK;
+  a.dV = dV;
+  a.N = N;
+  a.BH = static_cast<int>(BH);
+  a.scale = scale;
+  a.c_log2 = scale * 1.4426950408889634f;
+  cudaError_t e = fa::launch_bwd(a, d, bf16, causal != 0, s);
+  if (owned) {
+    cudaError_t e2 = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+}  // extern "C"

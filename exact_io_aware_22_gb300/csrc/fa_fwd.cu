@@ -1,0 +1,377 @@
+// fa_fwd.cu -- exact attention forward (FlashAttention-2 order) for sm_103a.
+//
+// Method: "flash-attn-triton" docs page, sections "Tiling softmax is exact
+// algebra" and Fig. 3 (running max m, running sum l, correction alpha applied to
+// l and the accumulator together, one divide after the loop, L = m + log l, exp2
+// with log2(e) folded into the scale), "Scope" (Q in the outer loop, grid split
+// over the sequence, causal mask only on diagonal tiles, ragged N), and Fig. 1
+// (one program per BLOCK_M query rows, K/V streamed BLOCK_N at a time).
+//
+// GB300 mapping (one CTA per SM, 384 threads):
+//   warp 0      TMA producer: both Q tiles once, then K_j / V_j into a ring.
+//   warp 1      TMEM allocator; lane 0 issues every tcgen05.mma and commit.
+//   warps 4-7   softmax warpgroup for Q tile 0 (one thread per query row).
+//   warps 8-11  softmax warpgroup for Q tile 1.
+// TMEM (512 columns): S0 | S1 | O0 | O1.  S_t = Q_t K_j^T lands in fp32; the
+// softmax thread of a row reads its 128 scores, writes P back over the first 64
+// columns of S_t as packed 16-bit pairs, and the P.V MMA reads P straight from
+// TMEM (A operand in tensor memory).  MMA issue order per K/V tile j is
+//   PV0(j), S0(j+1), PV1(j), S1(j+1)
+// so each softmax warpgroup overlaps two MMAs of the other tile.
+//
+// Running max update is lazy: m only moves when the tile maximum exceeds it by
+// more than RESCALE_LOG2 (log2 units), so the O rescale (TMEM load-multiply-
+// store) is skipped on almost every tile.  The result is still exact algebra:
+// numerator and denominator carry the same stale m, and every p <= 2^8.
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr int BM = 128;       // query rows per Q tile (= TMEM lanes)
+constexpr int BN = 128;       // keys per K/V tile
+constexpr int NT = 2;         // Q tiles per CTA
+constexpr int THREADS = 384;
+constexpr float RESCALE_LOG2 = 8.0f;
+
+template <int D>
+struct Cfg {
+  static constexpr int STAGES = D == 128 ? 2 : 3;
+  static constexpr int SW = D == 32 ? 64 : 128;        // swizzle width in bytes
+  static constexpr int ATOM = SW / 2;                  // elements per swizzled row
+  static constexpr int NCHUNK = D / ATOM;              // swizzle-width column blocks per tile
+  static constexpr int CHUNK_BYTES = 128 * SW;         // one column block of a 128-row tile
+  static constexpr int TILE_BYTES = 128 * D * 2;
+  static constexpr uint32_t SWZ = D == 32 ? UMMA_SW64 : UMMA_SW128;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + NT * TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
+  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_full[2], done
+  static constexpr int NBARS = 1 + 4 * STAGES + 7;
+  static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int SMEM_BYTES = SLOT_OFF + 16 + 1024;   // + alignment slack
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int S_COL = 0;                           // S_t at t * 128
+  static constexpr int O_COL = 256;                         // O_t at 256 + t * D
+};
+
+// byte offset of k-step kk (16 elements along K) inside a K-major tile
+template <int D>
+__device__ __forceinline__ uint32_t kmajor_koff(int kk) {
+  using C = Cfg<D>;
+  const int e = kk * 16;
+  return (e / C::ATOM) * C::CHUNK_BYTES + (e % C::ATOM) * 2;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(THREADS, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, void* __restrict__ Out,
+               float* __restrict__ Lout, int N, int n_qblk, float c_log2, KernelCtl ctl) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* sg = smem_raw + (sb - raw);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x / n_qblk;
+  const int qblk = n_qblk - 1 - (blockIdx.x % n_qblk);   // longest causal blocks first
+  const int row0 = qblk * (NT * BM);
+  const int nkv = (N + BN - 1) / BN;
+  int n_t[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int r = row0 + t * BM;
+    if (r >= N) n_t[t] = 0;
+    else if (CAUSAL) n_t[t] = min(nkv, min(r + BM - 1, N - 1) / BN + 1);
+    else n_t[t] = nkv;
+  }
+  const int n_max = max(n_t[0], n_t[1]);
+
+  auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };
+  const int B_QF = 0;
+  auto B_KF = [&](int s) { return 1 + s; };
+  auto B_KE = [&](int s) { return 1 + C::STAGES + s; };
+  auto B_VF = [&](int s) { return 1 + 2 * C::STAGES + s; };
+  auto B_VE = [&](int s) { return 1 + 3 * C::STAGES + s; };
+  auto B_SF = [&](int t) { return 1 + 4 * C::STAGES + t; };
+  auto B_PF = [&](int t) { return 3 + 4 * C::STAGES + t; };
+  auto B_OF = [&](int t) { return 5 + 4 * C::STAGES + t; };
+  const int B_DONE = 7 + 4 * C::STAGES;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBARS; ++i) mbar_init(bar(i), 1);
+    for (int t = 0; t < NT; ++t) mbar_init(bar(B_PF(t)), 128);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + C::SLOT_OFF, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sg + C::SLOT_OFF);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_max > 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(bar(B_QF), NT * C::TILE_BYTES);
+      for (int t = 0; t < NT; ++t)
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(sb + C::Q_OFF + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, bar(B_QF),
+                      c * C::ATOM, row0 + t * BM, bh);
+      int j = 0;
+      for (; j < n_max; ++j) {
+        const int s = j % C::STAGES;
+        const uint32_t ph = (j / C::STAGES) & 1;
+        if (!(ok = mbar_wait(bar(B_KE(s)), ph ^ 1, ctl))) break;
+        mbar_arrive_expect_tx(bar(B_KF(s)), C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(sb + C::K_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmK, bar(B_KF(s)),
+                      c * C::ATOM, j * BN, bh);
+        if (!(ok = mbar_wait(bar(B_VE(s)), ph ^ 1, ctl))) { ++j; break; }
+        mbar_arrive_expect_tx(bar(B_VF(s)), C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(sb + C::V_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV, bar(B_VF(s)),
+                      c * C::ATOM, j * BN, bh);
+      }
+      if (!ok) {
+        // drain: wait (bounded) for every copy this thread issued, so no bulk
+        // copy lands in shared memory after the CTA has gone.
+        mbar_wait(bar(B_QF), 0, ctl);
+        for (int jj = max(0, j - C::STAGES); jj < j; ++jj) {
+          const int s = jj % C::STAGES;
+          const uint32_t ph = (jj / C::STAGES) & 1;
+          mbar_wait(bar(B_KF(s)), ph, ctl);
+          mbar_wait(bar(B_VF(s)), ph, ctl);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_max > 0) {
+      constexpr uint32_t idS = umma_idesc_f16(BM, BN, BF16, false, false);
+      constexpr uint32_t idO = umma_idesc_f16(BM, D, BF16, false, true);
+      auto issue_S = [&](int t, int s) {
+        const uint32_t qa = sb + C::Q_OFF + t * C::TILE_BYTES;
+        const uint32_t ka = sb + C::K_OFF + s * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = kmajor_koff<D>(kk);
+          umma_ss(tmem + C::S_COL + t * BN, umma_sdesc(qa + o, 16, 8 * C::SW, C::SWZ),
+                  umma_sdesc(ka + o, 16, 8 * C::SW, C::SWZ), idS, kk > 0);
+        }
+      };
+      auto issue_PV = [&](int t, int s, bool acc) {
+        const uint32_t va = sb + C::V_OFF + s * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          umma_ts(tmem + C::O_COL + t * D, tmem + C::S_COL + t * BN + kk * 8,
+                  umma_sdesc(va + kk * 16 * C::SW, C::CHUNK_BYTES, 8 * C::SW, C::SWZ), idO,
+                  (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar(B_QF), 0, ctl) && mbar_wait(bar(B_KF(0)), 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < NT; ++t)
+          if (n_t[t] > 0) {
+            issue_S(t, 0);
+            umma_commit(bar(B_SF(t)));
+          }
+        umma_commit(bar(B_KE(0)));
+      }
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int s = j % C::STAGES;
+        const int s1 = (j + 1) % C::STAGES;
+        const uint32_t ph = (j / C::STAGES) & 1, ph1 = ((j + 1) / C::STAGES) & 1;
+        if (!(ok = mbar_wait(bar(B_VF(s)), ph, ctl))) break;
+        bool k_next = false;
+        for (int t = 0; t < NT && ok; ++t) {
+          if (j >= n_t[t]) continue;
+          if (!(ok = mbar_wait(bar(B_PF(t)), j & 1, ctl))) break;
+          tc_fence_after();
+          issue_PV(t, s, j > 0);
+          if (j + 1 < n_t[t]) {
+            if (!k_next) {
+              if (!(ok = mbar_wait(bar(B_KF(s1)), ph1, ctl))) break;
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_S(t, s1);
+            umma_commit(bar(B_SF(t)));
+          } else {
+            umma_commit(bar(B_OF(t)));
+          }
+        }
+        if (!ok) break;
+        umma_commit(bar(B_VE(s)));
+        if (k_next) umma_commit(bar(B_KE(s1)));
+      }
+      // every MMA this thread issued has completed before TMEM is released
+      umma_commit(bar(B_DONE));
+      mbar_wait(bar(B_DONE), 0, ctl);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;
+    const int rit = (warp & 3) * 32 + lane;              // row within the tile (= TMEM lane)
+    const int grow = row0 + t * BM + rit;                // query row
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::S_COL + t * BN;
+    const uint32_t tO = tmem + lane_off + C::O_COL + t * D;
+    const int nt = n_t[t];
+    const int tile_row0 = row0 + t * BM;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      if (!(ok = mbar_wait(bar(B_SF(t)), j & 1, ctl))) break;
+      tc_fence_after();
+      uint32_t sr[BN];
+      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+      const int kbase = j * BN;
+      // masks: causal on the diagonal tile only, key padding on the last tile
+      const bool need_mask = (CAUSAL && kbase + BN - 1 > tile_row0) || (kbase + BN > N);
+      if (need_mask) {
+        const int lim = CAUSAL ? min(grow + 1, N) : N;   // keys < lim are allowed
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (kbase + c >= lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      float mx = __uint_as_float(sr[0]);
+#pragma unroll
+      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      const float m_tile = mx * c_log2;
+      const bool grow_m = m_tile > m_run + RESCALE_LOG2;
+      const float m_use = grow_m ? m_tile : m_run;
+      const float alpha = grow_m ? ex2(m_run - m_use) : 1.f;
+      const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
+      float rs = 0.f;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(__uint_as_float(sr[32 * h + 2 * i]), c_log2, -m_sub));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[32 * h + 2 * i + 1]), c_log2, -m_sub));
+          rs += p0 + p1;
+          pk[i] = pack2<BF16>(p0, p1);
+        }
+        tmem_st16(tS + 16 * h, pk);
+      }
+      l_run = l_run * alpha + rs;
+      if (j > 0 && __any_sync(0xffffffffu, grow_m)) {
+        // O holds sum over tiles < j; PV(j-1) has completed because S(j) was
+        // issued after it and its commit was observed above.
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * cc, o);
+          tmem_ld_wait_regs(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + 32 * cc, o);
+        }
+      }
+      m_run = m_use;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_PF(t)));
+    }
+    if (ok && nt > 0 && mbar_wait(bar(B_OF(t)), 0, ctl)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l_run;
+      const bool valid = grow < N;
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      T* orow = reinterpret_cast<T*>(Out) + (static_cast<size_t>(bh) * N + grow) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * cc, o);
+        tmem_ld_wait_regs(o);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                             __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (valid)
+        Lout[static_cast<size_t>(bh) * N + grow] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+    }
+  }
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
+  using C = Cfg<D>;
+  auto kern = fwd_kernel<D, BF16, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int n_qblk = (a.N + NT * BM - 1) / (NT * BM);
+  const long long grid = static_cast<long long>(n_qblk) * a.BH;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  trace_begin(TR_FWD, st);
+  kern<<<static_cast<unsigned>(grid), THREADS, C::SMEM_BYTES, st>>>(
+      a.tmQ, a.tmK, a.tmV, a.O, a.L, a.N, n_qblk, a.c_log2, a.ctl);
+  trace_end(TR_FWD, st);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+FwdTileInfo fwd_tile_info(int d) {
+  FwdTileInfo t;
+  t.box_cols = d == 32 ? 32 : 64;
+  t.box_rows = 128;
+  t.swizzle_bytes = d == 32 ? 64 : 128;
+  return t;
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
+#define FA_FWD_CASE(DD, BB, CC) \
+  if (d == DD && bf16 == BB && causal == CC) return launch_fwd_t<DD, BB, CC>(a, st);
+  FA_FWD_CASE(32, false, false) FA_FWD_CASE(32, false, true)
+  FA_FWD_CASE(32, true, false) FA_FWD_CASE(32, true, true)
+  FA_FWD_CASE(64, false, false) FA_FWD_CASE(64, false, true)
+  FA_FWD_CASE(64, true, false) FA_FWD_CASE(64, true, true)
+  FA_FWD_CASE(128, false, false) FA_FWD_CASE(128, false, true)
+  FA_FWD_CASE(128, true, false) FA_FWD_CASE(128, true, true)
+#undef FA_FWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

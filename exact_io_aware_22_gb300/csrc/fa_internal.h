@@ -1,0 +1,53 @@
+// fa_internal.h -- host-side interface between the C ABI (fa_api.cu) and the
+// kernel launchers (fa_fwd.cu, fa_bwd.cu).  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+// Kernel kinds for the optional per-kernel CUDA-event trace (fa_trace_* in fa.h).
+enum TraceKind { TR_FWD = 0, TR_BWD_PRE = 1, TR_BWD_DKDV = 2, TR_BWD_DQ = 3, TR_NKINDS = 4 };
+// Record an event before / after one kernel launch on `st` (no-op unless tracing).
+void trace_begin(int kind, cudaStream_t st);
+void trace_end(int kind, cudaStream_t st);
+
+// TMA box of one 128-row tile: box_cols elements (one swizzle width) per row.
+struct FwdTileInfo {
+  int box_cols;
+  int box_rows;
+  int swizzle_bytes;
+};
+FwdTileInfo fwd_tile_info(int d);
+
+struct FwdArgs {
+  CUtensorMap tmQ, tmK, tmV;   // 3-D maps (d, N, B*H) of the 16-bit inputs
+  void* O;
+  float* L;
+  int N, BH;
+  float c_log2;                // scale * log2(e)
+  KernelCtl ctl;
+};
+cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
+
+struct BwdArgs {
+  CUtensorMap tmQ, tmK, tmV, tmO, tmdO;
+  const void* O;
+  const void* dO;
+  const float* L;
+  float* Dvec;                 // workspace: rowsum(dO o O), (B*H, N) fp32
+  void* dQ;
+  void* dK;
+  void* dV;
+  int N, BH;
+  float scale, c_log2;
+  KernelCtl ctl;
+};
+cudaError_t launch_bwd(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
+
+}  // namespace fa

@@ -1,0 +1,124 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * The operation is exact scaled-dot-product attention computed tile by tile
+ * with an online softmax, forward and backward ("flash-attn-triton" docs page:
+ * sections "The argument", "Tiling softmax is exact algebra" with Fig. 3, and
+ * "Scope"; FlashAttention note, "Key Mechanisms").  For each (batch b, head h):
+ *
+ *     S = scale * Q K^T                     (N x N, never stored)
+ *     causal: key j is allowed for query i iff j <= i (lower triangle)
+ *     P = softmax over the allowed keys of each row
+ *     O = P V
+ *     L = logsumexp of the allowed scaled scores of each row (natural log)
+ *
+ * and the backward returns dQ, dK, dV for an upstream gradient dO, rebuilding P
+ * from the saved L instead of storing it (docs page, "Scope"; FlashAttention
+ * note, "Key Mechanisms", backward recomputation).
+ *
+ * Conventions shared by every call
+ *   Layout     Q, K, V, O, dO, dQ, dK, dV: dense row-major (B, H, N, d) arrays of
+ *              16-bit floats (fp16 or bf16, all the same); element (b,h,n,c) at
+ *              ((b*H + h)*N + n)*d + c.  L: dense (B, H, N) fp32.
+ *   Memory     every pointer is CUDA device memory (or managed memory) of the
+ *              current device; the caller owns every buffer; the library keeps
+ *              no pointer after a call returns.  Outputs must not overlap inputs.
+ *   Alignment  16-bit arrays and the workspace: 16-byte aligned; L: 4-byte aligned.
+ *   Streams    `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *              Calls only enqueue work: they return before the GPU finishes and
+ *              never synchronise, except fa_device_status.
+ *   Errors     arguments are validated before anything is launched; a call that
+ *              returns an error has enqueued nothing (launch failures excepted:
+ *              FA_ERR_CUDA, with the CUDA error code from fa_last_cuda_error()).
+ *   Supported  d in {32, 64, 128}; fp16 or bf16; causal 0/1; any N >= 1 (N need
+ *              not be a multiple of the 128-row tile); scale finite and > 0.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_VALUE = 1,  /* NULL pointer, B/H/N < 1, bad scale, short workspace, overlap */
+  FA_ERR_UNSUPPORTED = 2,    /* d not in {32,64,128}, unknown dtype, sizes beyond the limits */
+  FA_ERR_MISALIGNED = 3,     /* a pointer violates the alignment rule above */
+  FA_ERR_CUDA = 4,           /* a CUDA runtime/driver call or a launch failed */
+  FA_ERR_TIMEOUT = 5         /* a kernel gave up a bounded wait (see fa_device_status) */
+} fa_status;
+
+typedef enum fa_dtype { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/* Forward.  Writes O (B,H,N,d) and L (B,H,N) fp32 = natural-log logsumexp of the
+ * allowed scaled scores of each row (docs page Fig. 3: L = m + log l, one float
+ * per row, the only state the backward needs).  Q, K, V are read once per
+ * 128-query-row tile pair; the N x N score matrix never reaches memory. */
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L,
+                 int B, int H, int N, int d, int causal, float scale, fa_dtype dtype,
+                 void* stream);
+
+/* Bytes of device workspace fa_bwd needs for these sizes: the per-row delta
+ * D = rowsum(dO o O) and L * log2(e), both fp32, padded to whole 128-row tiles.
+ * Returns 0 for sizes fa_bwd would reject. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal);
+
+/* Backward.  Given Q, K, V, the forward's O and L, and dO, writes dQ, dK, dV
+ * (16-bit, same layout as Q).  P is rebuilt from L (docs page, "Scope"):
+ *   dV = P^T dO, dP = dO V^T, D = rowsum(dO o O), dS = P o (dP - D),
+ *   dQ = scale dS K, dK = scale dS^T Q.
+ * `workspace` is device memory of at least fa_bwd_workspace_size() bytes, used
+ * as scratch during the call; pass NULL to let the library take it from the
+ * stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`). */
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                 size_t workspace_bytes, int B, int H, int N, int d, int causal, float scale,
+                 fa_dtype dtype, void* stream);
+
+/* Static description of a status code. */
+const char* fa_status_string(fa_status s);
+
+/* CUDA error code (a cudaError_t value) behind the last FA_ERR_CUDA returned on
+ * the calling thread; 0 if none. */
+int fa_last_cuda_error(void);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: FA_ERR_TIMEOUT if any kernel of this library gave up a bounded wait
+ * since the last read, FA_OK otherwise (FA_ERR_CUDA if the read failed). */
+fa_status fa_device_status(void* stream);
+
+/* Bound, in nanoseconds, on any single wait inside the kernels (default 2 s).
+ * ns == 0 restores the default.  Applies to launches made after the call. */
+fa_status fa_set_wait_limit_ns(unsigned long long ns);
+
+/* Failure-detection self test: launches one CTA that waits on a barrier nothing
+ * will complete, bounded by `limit_ns`; the kernel records a timeout and exits.
+ * Synchronises `stream` and returns what fa_device_status then reports
+ * (FA_ERR_TIMEOUT when the bound works).  Faults nothing. */
+fa_status fa_selftest_timeout(unsigned long long limit_ns, void* stream);
+
+/* Per-kernel timing trace (the method's own benchmark harness measures speed
+ * and TFLOP/s: docs page, "Scope" and Table 3).  While enabled, every kernel
+ * launch of this library is bracketed by two CUDA events recorded on its
+ * stream, from a fixed pool of 4096 launches (later launches are not traced).
+ * fa_trace_enable(1) (re)starts recording and clears earlier records (the
+ * first call creates the events); fa_trace_enable(0) stops it.  Not
+ * thread-safe: trace from one host thread. */
+fa_status fa_trace_enable(int on);
+
+/* Name of trace kind `kind` (0: forward kernel, 1: backward pre-pass, 2:
+ * backward dK/dV kernel, 3: backward dQ kernel); NULL when out of range. */
+const char* fa_trace_kind_name(int kind);
+
+/* Waits for the recorded events of kind `kind`, then writes the summed GPU
+ * time in milliseconds and the number of traced launches. */
+fa_status fa_trace_read(int kind, double* total_ms, long long* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

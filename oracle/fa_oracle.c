@@ -37,8 +37,9 @@
  *   exposed for the merge pins.
  *
  * Layout: Q, K, V, O, dO, dQ, dK, dV are dense row-major (B, H, N, d) fp64;
- * L and D are (B, H, N) fp64.  Heads are independent; OpenMP runs over the
- * B*H (batch, head) pairs, each pair owned by one thread.
+ * L and D are (B, H, N) fp64.  Heads and rows are independent: OpenMP runs over
+ * (batch*head, query row) pairs, and for dK/dV over (batch*head, key row) pairs,
+ * each output row written by exactly one thread.
  */
 #include <math.h>
 #include <stdlib.h>
@@ -86,85 +87,114 @@ void oracle_fwd(const double* Q, const double* K, const double* V, double* O, do
                 int B, int H, int N, int d, int causal, double scale)
 {
     long BH = (long)B * H;
-#pragma omp parallel for schedule(dynamic, 1)
-    for (long bh = 0; bh < BH; ++bh) {
-        const double* q = Q + bh * N * d;
-        const double* k = K + bh * N * d;
-        const double* v = V + bh * N * d;
-        double* o = O + bh * N * d;
-        double* lse = L + bh * N;
+    /* every (batch, head, row) is independent */
+#pragma omp parallel
+    {
         double* s = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
-        for (int i = 0; i < N; ++i) {
-            int nk = n_allowed(i, N, causal);
-            double l;
-            double m = row_scores(q + (long)i * d, k, nk, d, scale, s, &l);
-            double* oi = o + (long)i * d;
-            for (int c = 0; c < d; ++c) oi[c] = 0.0;
-            if (nk == 0) { lse[i] = -INFINITY; continue; }
-            for (int j = 0; j < nk; ++j) {
-                double p = exp(s[j] - m) / l;
-                const double* vj = v + (long)j * d;
-                for (int c = 0; c < d; ++c) oi[c] += p * vj[c];
+#pragma omp for collapse(2) schedule(dynamic, 16)
+        for (long bh = 0; bh < BH; ++bh) {
+            for (int i = 0; i < N; ++i) {
+                const double* q = Q + bh * N * d;
+                const double* k = K + bh * N * d;
+                const double* v = V + bh * N * d;
+                double* o = O + bh * N * d;
+                double* lse = L + bh * N;
+                int nk = n_allowed(i, N, causal);
+                double l;
+                double m = row_scores(q + (long)i * d, k, nk, d, scale, s, &l);
+                double* oi = o + (long)i * d;
+                for (int c = 0; c < d; ++c) oi[c] = 0.0;
+                if (nk == 0) { lse[i] = -INFINITY; continue; }
+                for (int j = 0; j < nk; ++j) {
+                    double p = exp(s[j] - m) / l;
+                    const double* vj = v + (long)j * d;
+                    for (int c = 0; c < d; ++c) oi[c] += p * vj[c];
+                }
+                lse[i] = m + log(l);
             }
-            lse[i] = m + log(l);
         }
         free(s);
     }
 }
 
+/* Backward in two passes over the same definition.
+ * Pass 1, one query row i at a time: S_i., the softmax statistics (kept as the
+ * logsumexp L_i), P_i., O_i, D_i = dO_i . O_i, dP_i. = dO_i V^T, dS_i., and
+ * dQ_i = scale sum_j dS_ij k_j.
+ * Pass 2, one key row j at a time: for every query i allowed to see key j,
+ * P_ij = exp(S_ij - L_i), dP_ij = dO_i . v_j, dS_ij = P_ij (dP_ij - D_i);
+ * dK_j = scale sum_i dS_ij q_i and dV_j = sum_i P_ij dO_i. */
 void oracle_bwd(const double* Q, const double* K, const double* V, const double* dO,
                 double* dQ, double* dK, double* dV, double* Dout,
                 int B, int H, int N, int d, int causal, double scale)
 {
     long BH = (long)B * H;
-#pragma omp parallel for schedule(dynamic, 1)
-    for (long bh = 0; bh < BH; ++bh) {
-        const double* q = Q + bh * N * d;
-        const double* k = K + bh * N * d;
-        const double* v = V + bh * N * d;
-        const double* dout = dO + bh * N * d;
-        double* dq = dQ + bh * N * d;
-        double* dk = dK + bh * N * d;
-        double* dv = dV + bh * N * d;
-        double* Dh = Dout + bh * N;
-        memset(dk, 0, sizeof(double) * N * d);
-        memset(dv, 0, sizeof(double) * N * d);
+    double* Lrow = (double*)malloc(sizeof(double) * (BH * N > 0 ? BH * N : 1));
+#pragma omp parallel
+    {
         double* s = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
         double* oi = (double*)malloc(sizeof(double) * (d > 0 ? d : 1));
-        for (int i = 0; i < N; ++i) {
-            int nk = n_allowed(i, N, causal);
-            const double* qi = q + (long)i * d;
-            const double* doi = dout + (long)i * d;
-            double* dqi = dq + (long)i * d;
-            for (int c = 0; c < d; ++c) { dqi[c] = 0.0; oi[c] = 0.0; }
-            if (nk == 0) { Dh[i] = 0.0; continue; }
-            double l;
-            double m = row_scores(qi, k, nk, d, scale, s, &l);
-            /* s[j] <- P_ij, and O_i = sum_j P_ij v_j */
-            for (int j = 0; j < nk; ++j) {
-                s[j] = exp(s[j] - m) / l;
-                const double* vj = v + (long)j * d;
-                for (int c = 0; c < d; ++c) oi[c] += s[j] * vj[c];
-            }
-            double Di = dot(doi, oi, d);
-            Dh[i] = Di;
-            for (int j = 0; j < nk; ++j) {
-                double pij = s[j];
-                double dpij = dot(doi, v + (long)j * d, d);
-                double dsij = pij * (dpij - Di);
-                const double* kj = k + (long)j * d;
-                double* dkj = dk + (long)j * d;
-                double* dvj = dv + (long)j * d;
-                for (int c = 0; c < d; ++c) {
-                    dqi[c] += scale * dsij * kj[c];
-                    dkj[c] += scale * dsij * qi[c];
-                    dvj[c] += pij * doi[c];
+#pragma omp for collapse(2) schedule(dynamic, 16)
+        for (long bh = 0; bh < BH; ++bh) {
+            for (int i = 0; i < N; ++i) {
+                const double* q = Q + bh * N * d;
+                const double* k = K + bh * N * d;
+                const double* v = V + bh * N * d;
+                const double* dout = dO + bh * N * d;
+                int nk = n_allowed(i, N, causal);
+                const double* qi = q + (long)i * d;
+                const double* doi = dout + (long)i * d;
+                double* dqi = dQ + bh * N * d + (long)i * d;
+                for (int c = 0; c < d; ++c) { dqi[c] = 0.0; oi[c] = 0.0; }
+                if (nk == 0) { Dout[bh * N + i] = 0.0; Lrow[bh * N + i] = -INFINITY; continue; }
+                double l;
+                double m = row_scores(qi, k, nk, d, scale, s, &l);
+                Lrow[bh * N + i] = m + log(l);
+                /* s[j] <- P_ij, and O_i = sum_j P_ij v_j */
+                for (int j = 0; j < nk; ++j) {
+                    s[j] = exp(s[j] - m) / l;
+                    const double* vj = v + (long)j * d;
+                    for (int c = 0; c < d; ++c) oi[c] += s[j] * vj[c];
+                }
+                double Di = dot(doi, oi, d);
+                Dout[bh * N + i] = Di;
+                for (int j = 0; j < nk; ++j) {
+                    double dpij = dot(doi, v + (long)j * d, d);
+                    double dsij = s[j] * (dpij - Di);
+                    const double* kj = k + (long)j * d;
+                    for (int c = 0; c < d; ++c) dqi[c] += scale * dsij * kj[c];
                 }
             }
         }
         free(oi);
         free(s);
     }
+#pragma omp parallel for collapse(2) schedule(dynamic, 16)
+    for (long bh = 0; bh < BH; ++bh) {
+        for (int j = 0; j < N; ++j) {
+            const double* q = Q + bh * N * d;
+            const double* k = K + bh * N * d;
+            const double* v = V + bh * N * d;
+            const double* dout = dO + bh * N * d;
+            const double* kj = k + (long)j * d;
+            const double* vj = v + (long)j * d;
+            double* dkj = dK + bh * N * d + (long)j * d;
+            double* dvj = dV + bh * N * d + (long)j * d;
+            for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+            for (int i = causal ? j : 0; i < N; ++i) {
+                const double* qi = q + (long)i * d;
+                const double* doi = dout + (long)i * d;
+                double pij = exp(scale * dot(qi, kj, d) - Lrow[bh * N + i]);
+                double dpij = dot(doi, vj, d);
+                double dsij = pij * (dpij - Dout[bh * N + i]);
+                for (int c = 0; c < d; ++c) {
+                    dkj[c] += scale * dsij * qi[c];
+                    dvj[c] += pij * doi[c];
+                }
+            }
+        }
+    }
+    free(Lrow);
 }
 
 /* ---- naive online-softmax oracle (Fig. 3 of the docs page) -------------- */

@@ -1,0 +1,65 @@
+"""Shared GPU-vs-oracle comparison for the parity tests.
+
+Tolerances (max over every compared element):
+  O:            max|err| <= 2e-3 (fp16), 1.6e-2 (bf16)   for N(0,1) inputs
+  L:            max|err| <= 1e-4 (fp32 output)
+  dQ, dK, dV:   max|err| / max|ref| <= 1e-2 (fp16), 3e-2 (bf16)
+The oracle runs in fp64 on the 16-bit input values upcast exactly; the inputs
+come from the shared seeded generator, never from the CUDA path.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from exact_io_aware_22_gb300 import inputs
+
+TOL_O = {"fp16": 2e-3, "bf16": 1.6e-2}
+TOL_L = 1e-4
+TOL_G = {"fp16": 1e-2, "bf16": 3e-2}
+
+
+def gpu_fwd_bwd(x: dict, causal: bool, scale: float, device="cuda"):
+    import exact_io_aware_22_gb300 as fa
+    q, k, v, do = (x[n].to(device) for n in ("q", "k", "v", "do"))
+    o, lse = fa.fwd(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.bwd(q, k, v, o, lse, do, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0, "a kernel reported a bounded-wait timeout"
+    return {n: t.float().cpu() for n, t in
+            (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+
+
+def _sel(t: torch.Tensor, heads):
+    B, H = t.shape[:2]
+    flat = t.reshape(B * H, *t.shape[2:])
+    if heads is None:
+        return flat.unsqueeze(0)
+    return flat[list(heads)].unsqueeze(0)
+
+
+def compare(B, H, N, d, dtype, causal, qk_std=1.0, heads=None, seed=0, scale=None):
+    """Run the CUDA path on the whole problem and the oracle on ``heads`` (flat b*H+h
+    indices; None = all).  Returns the error report; asserts the tolerances."""
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    x = inputs.make_inputs(B, H, N, d, dtype, seed=seed, qk_std=qk_std)
+    g = gpu_fwd_bwd(x, causal, scale)
+    q, k, v, do = (_sel(x[n].double(), heads).numpy() for n in ("q", "k", "v", "do"))
+    o_ref, l_ref = oracle.fwd(q, k, v, causal, scale)
+    dq_ref, dk_ref, dv_ref, _ = oracle.bwd(q, k, v, do, causal, scale)
+    rep = {}
+    for name, ref in (("o", o_ref), ("lse", l_ref), ("dq", dq_ref), ("dk", dk_ref), ("dv", dv_ref)):
+        got = _sel(g[name], heads).double().numpy()
+        assert np.isfinite(got).all(), f"{name}: non-finite values"
+        err = float(np.max(np.abs(got - ref)))
+        if name in ("dq", "dk", "dv"):
+            err /= max(float(np.max(np.abs(ref))), 1e-30)
+        rep[name] = err
+    assert rep["o"] <= TOL_O[dtype], rep
+    assert rep["lse"] <= TOL_L, rep
+    for n in ("dq", "dk", "dv"):
+        assert rep[n] <= TOL_G[dtype], rep
+    return rep

@@ -1,0 +1,111 @@
+"""The C ABI on the host: the library builds for sm_103a, loads, exports every
+function include/fa.h declares, and rejects invalid arguments with the documented
+status before any CUDA work.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_io_aware_22_gb300 import build
+    import exact_io_aware_22_gb300 as fa
+    path = build.build()
+    return fa.load_library(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string",
+              "fa_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fa.h but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = lib.fa_status_string(code)
+        assert s and s.startswith(b"FA_")
+
+
+A16 = 0x10000  # fake, 16-byte aligned device addresses (never dereferenced on rejection)
+
+
+def fwd(lib, **kw):
+    a = dict(Q=A16, K=2 * A16, V=3 * A16, O=4 * A16, L=5 * A16, B=1, H=1, N=128, d=64,
+             causal=0, scale=0.125, dtype=0)
+    a.update(kw)
+    return lib.fa_fwd(*(ctypes.c_void_p(a[k]) for k in ("Q", "K", "V", "O", "L")), a["B"],
+                      a["H"], a["N"], a["d"], a["causal"], a["scale"], a["dtype"], None)
+
+
+def bwd(lib, **kw):
+    a = dict(Q=A16, K=2 * A16, V=3 * A16, O=4 * A16, dO=5 * A16, L=6 * A16, dQ=7 * A16,
+             dK=8 * A16, dV=9 * A16, ws=10 * A16, ws_bytes=1 << 20, B=1, H=1, N=128, d=64,
+             causal=1, scale=0.125, dtype=1)
+    a.update(kw)
+    ptrs = [ctypes.c_void_p(a[k]) for k in ("Q", "K", "V", "O", "dO", "L", "dQ", "dK", "dV", "ws")]
+    return lib.fa_bwd(*ptrs, a["ws_bytes"], a["B"], a["H"], a["N"], a["d"], a["causal"],
+                      a["scale"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=48), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(d=16), UNSUPPORTED),
+    (dict(dtype=2), UNSUPPORTED), (dict(dtype=-1), UNSUPPORTED),
+    (dict(B=0), INVALID), (dict(H=0), INVALID), (dict(N=0), INVALID), (dict(N=-5), INVALID),
+    (dict(scale=0.0), INVALID), (dict(scale=-0.1), INVALID), (dict(scale=float("nan")), INVALID),
+    (dict(scale=float("inf")), INVALID), (dict(causal=2), INVALID),
+    (dict(Q=0), INVALID), (dict(O=0), INVALID), (dict(L=0), INVALID),
+    (dict(Q=A16 + 8), MISALIGNED), (dict(V=3 * A16 + 2), MISALIGNED), (dict(O=4 * A16 + 4), MISALIGNED),
+    (dict(L=5 * A16 + 2), MISALIGNED),
+    (dict(O=A16 + 64), INVALID),                      # output overlaps Q
+    (dict(L=2 * A16 + 4), INVALID),                   # L inside K
+])
+def test_fwd_rejects(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), UNSUPPORTED), (dict(dtype=7), UNSUPPORTED),
+    (dict(N=0), INVALID), (dict(scale=-1.0), INVALID),
+    (dict(dQ=0), INVALID), (dict(L=0), INVALID), (dict(dO=0), INVALID),
+    (dict(dK=8 * A16 + 8), MISALIGNED), (dict(ws=10 * A16 + 4), MISALIGNED),
+    (dict(ws_bytes=16), INVALID),                     # workspace too small
+    (dict(dK=7 * A16 + 16), INVALID),                 # dK overlaps dQ
+    (dict(dV=A16), INVALID),                          # dV aliases Q
+])
+def test_bwd_rejects(lib, kw, code):
+    assert bwd(lib, **kw) == code
+
+
+def test_workspace_size(lib):
+    f = lib.fa_bwd_workspace_size
+    # D and L*log2(e), fp32, padded to 128-row blocks
+    assert f(1, 1, 128, 64, 0) == 2 * 128 * 4
+    assert f(4, 8, 1000, 32, 1) == 2 * 32 * 1024 * 4
+    assert f(1, 32, 8192, 128, 1) == 2 * 32 * 8192 * 4
+    assert f(1, 1, 1, 32, 1) == 2 * 128 * 4
+    assert f(1, 1, 128, 48, 0) == 0 and f(0, 1, 128, 64, 0) == 0
+
+
+def test_binding_refuses_without_library(tmp_path):
+    import exact_io_aware_22_gb300 as fa
+    with pytest.raises(RuntimeError, match="not built"):
+        fa.load_library(str(tmp_path / "missing.so"))

@@ -1,0 +1,101 @@
+"""GPU runtime behaviour of the C ABI: output guards, determinism, workspace
+handling, streams, and the bounded-wait failure detection (no fault)."""
+import math
+
+import pytest
+import torch
+
+from exact_io_aware_22_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _fa():
+    import exact_io_aware_22_gb300 as fa
+    return fa
+
+
+@pytest.mark.parametrize("N", [1, 129, 1000])
+@pytest.mark.parametrize("causal", [False, True])
+def test_nan_prefill_and_canaries(N, causal):
+    """Outputs pre-filled with NaN are completely overwritten; memory past the end
+    of every output is untouched."""
+    fa = _fa()
+    B, H, d = 1, 2, 64
+    x = inputs.make_inputs(B, H, N, d, "bf16", seed=1)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    n = B * H * N * d
+    pad = 4096
+    canary = -12345.0
+
+    def guarded(count, dtype):
+        buf = torch.full((count + pad,), float("nan"), dtype=dtype, device="cuda")
+        buf[count:] = canary
+        return buf
+
+    ob, lb = guarded(n, torch.bfloat16), guarded(B * H * N, torch.float32)
+    o, lse = ob[:n].view(B, H, N, d), lb[:B * H * N].view(B, H, N)
+    fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
+    gb = [guarded(n, torch.bfloat16) for _ in range(3)]
+    dq, dk, dv = (g[:n].view(B, H, N, d) for g in gb)
+    fa.bwd(q, k, v, o, lse, do, causal=causal, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    for buf, count in [(ob, n), (lb, B * H * N)] + [(g, n) for g in gb]:
+        assert torch.isfinite(buf[:count].float()).all()
+        stored = torch.tensor(canary, dtype=buf.dtype).float().item()   # canary as the dtype holds it
+        assert (buf[count:].float() == stored).all()
+
+
+def test_deterministic():
+    fa = _fa()
+    x = inputs.make_inputs(2, 4, 777, 128, "bf16", seed=2)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    outs = []
+    for _ in range(2):
+        o, lse = fa.fwd(q, k, v, causal=True)
+        dq, dk, dv = fa.bwd(q, k, v, o, lse, do, causal=True)
+        outs.append([t.clone() for t in (o, lse, dq, dk, dv)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_explicit_workspace_and_side_stream():
+    fa = _fa()
+    B, H, N, d = 2, 2, 500, 32
+    x = inputs.make_inputs(B, H, N, d, "fp16", seed=3)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fwd(q, k, v, causal=True)
+    ref = fa.bwd(q, k, v, o, lse, do, causal=True)
+    ws = torch.empty(fa.bwd_workspace_size(B, H, N, d, True), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o2, lse2 = fa.fwd(q, k, v, causal=True)
+        got = fa.bwd(q, k, v, o2, lse2, do, causal=True, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    fa = _fa()
+    assert fa.device_status() == 0
+    assert fa.selftest_timeout(2_000_000) == 5          # FA_ERR_TIMEOUT, no fault
+    assert fa.device_status() == 0                       # read clears the word
+    x = inputs.make_inputs(1, 1, 256, 64, "fp16", seed=4)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o, lse = fa.fwd(q, k, v, causal=False)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o.float()).all() and fa.device_status() == 0
+
+
+def test_errors_raise_before_launch():
+    fa = _fa()
+    q = torch.zeros(1, 1, 64, 48, dtype=torch.float16, device="cuda")
+    with pytest.raises(fa.FAError, match="UNSUPPORTED"):
+        fa.fwd(q, q.clone(), q.clone())
+    q = torch.zeros(1, 1, 64, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(fa.FAError, match="INVALID"):
+        fa.fwd(q, q.clone(), q.clone(), scale=-1.0)

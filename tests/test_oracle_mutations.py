@@ -17,10 +17,16 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "fa_oracle.c")
 MUTANTS = {
     "dK drops the scale": ("dkj[c] += scale * dsij * qi[c];", "dkj[c] += dsij * qi[c];"),
     "dQ drops the scale": ("dqi[c] += scale * dsij * kj[c];", "dqi[c] += dsij * kj[c];"),
-    "dS sign flipped": ("double dsij = pij * (dpij - Di);", "double dsij = pij * (dpij + Di);"),
-    "dS drops D": ("double dsij = pij * (dpij - Di);", "double dsij = pij * dpij;"),
+    "dS sign flipped (dQ pass)": ("double dsij = s[j] * (dpij - Di);",
+                                  "double dsij = s[j] * (dpij + Di);"),
+    "dS drops D (dK/dV pass)": ("double dsij = pij * (dpij - Dout[bh * N + i]);",
+                                "double dsij = pij * dpij;"),
     "dV transposed operand": ("dvj[c] += pij * doi[c];",
                               "dvj[c] += pij * dout[(long)j * d + c];"),
+    "dK/dV pass: causal start shifted": ("for (int i = causal ? j : 0; i < N; ++i)",
+                                        "for (int i = causal ? j + 1 : 0; i < N; ++i)"),
+    "dK/dV pass: P from a log2 L": ("double pij = exp(scale * dot(qi, kj, d) - Lrow[bh * N + i]);",
+                                   "double pij = exp2(scale * dot(qi, kj, d) - Lrow[bh * N + i]);"),
     "causal mask shifted": ("causal ? (i + 1 < N ? i + 1 : N) : N",
                             "causal ? (i + 2 < N ? i + 2 : N) : N"),
     "L in log2": ("lse[i] = m + log(l);", "lse[i] = m + log2(l);"),
@@ -31,8 +37,8 @@ MUTANTS = {
                                          "for (int t = 0; t < d; ++t) acc[t] *= 1.0;"),
     "merge: wrong weight": ("*l_out = a1 * l1 + a2 * l2;", "*l_out = a1 * l1 + a1 * l2;"),
     "scores transposed (k_i . q_j)": (
-        "double m = row_scores(q + (long)i * d, k, nk, d, scale, s, &l);\n            double* oi = o",
-        "double m = row_scores(k + (long)i * d, q, nk, d, scale, s, &l);\n            double* oi = o"),
+        "double m = row_scores(q + (long)i * d, k, nk, d, scale, s, &l);\n                double* oi = o",
+        "double m = row_scores(k + (long)i * d, q, nk, d, scale, s, &l);\n                double* oi = o"),
 }
 
 

@@ -1,0 +1,56 @@
+"""CUDA path vs the fp64 oracle, through the C ABI, on the GPU.
+
+The workload configurations (sizes the oracle finishes in seconds: every head)
+and the full-size long-context ones (sampled heads, each compared in full:
+heads are independent), plus ragged and degenerate sizes."""
+import pytest
+
+from tests.parity_util import compare
+
+pytestmark = pytest.mark.gpu
+
+
+# (B, H, N, d, dtype, causal, qk_std, heads)
+WORKLOAD_CASES = {
+    "tiny_full_d64_fp16": (1, 1, 128, 64, "fp16", False, 1.0, None),
+    "ragged_causal_d32_fp16": (4, 8, 1000, 32, "fp16", True, 1.0, None),
+    "ragged_causal_d32_fp16_stress": (4, 8, 1000, 32, "fp16", True, 4.0, None),
+    "gpt2m_causal_d64_fp16": (8, 16, 1024, 64, "fp16", True, 1.0, None),
+    "n4k_full_d128_bf16": (2, 16, 4096, 128, "bf16", False, 1.0, (0, 8, 31)),
+    "n4k_causal_d128_bf16": (2, 16, 4096, 128, "bf16", True, 1.0, (0, 8, 31)),
+    "n8k_causal_d128_bf16": (1, 32, 8192, 128, "bf16", True, 1.0, (0, 16, 31)),
+    "n16k_causal_d128_bf16": (1, 32, 16384, 128, "bf16", True, 1.0, (0, 16, 31)),
+}
+
+
+@pytest.mark.parametrize("name", list(WORKLOAD_CASES))
+def test_workload(name):
+    B, H, N, d, dt, causal, std, heads = WORKLOAD_CASES[name]
+    rep = compare(B, H, N, d, dt, causal, qk_std=std, heads=heads)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 2, 127, 129, 257, 383])
+def test_ragged_and_degenerate(N, d, dtype, causal):
+    compare(1, 2, N, d, dtype, causal, seed=N)
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_batch_head(d, causal):
+    compare(2, 3, 300, d, "bf16", causal, seed=7)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_stress_row_maxima(dtype):
+    # Q, K ~ N(0, 4^2): large row maxima exercise the running-max update
+    compare(2, 2, 640, 128, dtype, True, qk_std=4.0, seed=3)
+    compare(2, 2, 640, 64, dtype, False, qk_std=4.0, seed=4)
+
+
+def test_non_default_scale():
+    compare(1, 2, 256, 64, "fp16", True, scale=0.05, seed=5)
+    compare(1, 2, 256, 64, "bf16", False, scale=0.4, seed=6)
