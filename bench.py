@@ -60,6 +60,23 @@ def attn_flops(B, H, N, d, causal):
     return f, 2.5 * f
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the slowest rank's time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
+    """Weak scaling: every rank runs its own copy of the workload; the job is done when the
+    slowest rank is."""
+    return world * flops_per_rank / (ms_max / 1e3) / 1e12
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -268,11 +285,8 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
     ms = t0.elapsed_time(t1) / args.steps
     traced = fa.trace_read()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * (fwd_f + bwd_f) / (ms / 1e3) / 1e12
+    ms = max_over_ranks(ms, world, dev)
+    value = whole_job_tflops(fwd_f + bwd_f, world, ms)
     launches = sum(n for _, n in traced.values())
 
     per = {kname: (tot / n if n else 0.0, n) for kname, (tot, n) in traced.items()}
@@ -331,12 +345,8 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = e0.elapsed_time(e1) / ke
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * (fwd_f + bwd_f) / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+        ems = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
+        e2e = {"value": whole_job_tflops(fwd_f + bwd_f, world, ems), "unit": "TFLOP/s",
                "h2d_bytes_per_step": 4 * n_bytes, "d2h_bytes_per_step": 4 * n_bytes + 4 * B * H * N,
                "ms_per_step": ems, "steps": ke}
 

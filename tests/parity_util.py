@@ -4,6 +4,14 @@ Tolerances (max over every compared element):
   O:            max|err| <= 2e-3 (fp16), 1.6e-2 (bf16)   for N(0,1) inputs
   L:            max|err| <= 1e-4 (fp32 output)
   dQ, dK, dV:   max|err| / max|ref| <= 1e-2 (fp16), 3e-2 (bf16)
+Two cases fall outside what those bounds were stated for:
+  * Q, K ~ N(0, 4^2) (the stress inputs): rows are nearly one-hot, so |O| reaches
+    max|V| (about 4.5) and the 16-bit rounding of P and of O grows with it.  The O
+    bound is then multiplied by max(1, max|O_ref|).
+  * N = 1: one key gives P = 1 and dS = dP - D = 0, so the reference dQ and dK are
+    identically zero and the relative error is undefined.  Where max|ref| is below
+    1e-6 of the size of a single term scale * |dP| * |k| (exact cancellation), the
+    error is measured relative to that term size instead.
 The oracle runs in fp64 on the 16-bit input values upcast exactly; the inputs
 come from the shared seeded generator, never from the CUDA path.
 """
@@ -51,14 +59,20 @@ def compare(B, H, N, d, dtype, causal, qk_std=1.0, heads=None, seed=0, scale=Non
     o_ref, l_ref = oracle.fwd(q, k, v, causal, scale)
     dq_ref, dk_ref, dv_ref, _ = oracle.bwd(q, k, v, do, causal, scale)
     rep = {}
+    # size of one dS_ij * k_j term: scale * max|dP| * max|k|, with |dP| <= |dO| |v|
+    term = scale * float(np.max(np.linalg.norm(do, axis=-1)) * np.max(np.linalg.norm(v, axis=-1))
+                         * max(np.max(np.abs(k)), np.max(np.abs(q))))
     for name, ref in (("o", o_ref), ("lse", l_ref), ("dq", dq_ref), ("dk", dk_ref), ("dv", dv_ref)):
         got = _sel(g[name], heads).double().numpy()
         assert np.isfinite(got).all(), f"{name}: non-finite values"
         err = float(np.max(np.abs(got - ref)))
         if name in ("dq", "dk", "dv"):
-            err /= max(float(np.max(np.abs(ref))), 1e-30)
+            mref = float(np.max(np.abs(ref)))
+            err /= mref if mref >= 1e-6 * term else term
         rep[name] = err
-    assert rep["o"] <= TOL_O[dtype], rep
+    o_scale = 1.0 if qk_std == 1.0 else max(1.0, float(np.max(np.abs(o_ref))))
+    rep["o_bound"] = TOL_O[dtype] * o_scale
+    assert rep["o"] <= rep["o_bound"], rep
     assert rep["lse"] <= TOL_L, rep
     for n in ("dq", "dk", "dv"):
         assert rep[n] <= TOL_G[dtype], rep
