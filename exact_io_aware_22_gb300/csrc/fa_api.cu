@@ -348,3 +348,52 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward without allocation.  Some callers cannot call cudaMalloc at all:
+// plugins of a host framework that owns every byte of device memory, and
+// deployments that hand the library a fixed memory budget up front.  They get
+// fa_bwd_noalloc, whose scratch lives in this file-scope array instead of a
+// workspace: every GPU that loads the library holds it until the process exits.
+static constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+static float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  On the host the
+// array's name is only a stand-in, never a device address, so it is looked up
+// once per device, with that device current, and the looked-up pointer is what
+// the kernels receive.
+static fa_status noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return FA_OK;
+}
+
+extern "C" {
+
+fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
+                         int H, int N, int d, int causal, float scale, fa_dtype dtype,
+                         void* stream) {
+  fa_status st = check_common(B, H, N, d, causal, scale, static_cast<int>(dtype));
+  if (st != FA_OK) return st;
+  const size_t need = fa::bwd_workspace_bytes(static_cast<long long>(B) * H, N);
+  if (need > kNoAllocScratchBytes) return FA_ERR_UNSUPPORTED;   // more than the static scratch
+  float* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != FA_OK) return st;
+  // Same validation and kernels as fa_bwd, with the static array as its workspace;
+  // a non-NULL workspace means fa_bwd allocates nothing.
+  return fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, scratch, kNoAllocScratchBytes, B, H, N, d, causal,
+                scale, dtype, stream);
+}
+
+}  // extern "C"

@@ -117,6 +117,26 @@ const char* fa_trace_kind_name(int kind);
  * time in milliseconds and the number of traced launches. */
 fa_status fa_trace_read(int kind, double* total_ms, long long* launches);
 
+/* Backward that allocates nothing.  The pages have no counterpart: this entry
+ * exists for callers, not for the method.  Some callers cannot call cudaMalloc
+ * at all -- a plugin inside a host framework that owns every byte of device
+ * memory, or a deployment handed a fixed memory budget up front -- and fa_bwd
+ * either takes a caller workspace or allocates one.  fa_bwd_noalloc computes
+ * what fa_bwd computes, with the same arguments minus the workspace.  Its
+ * scratch is a 16 MiB device array inside the library, held by every GPU that
+ * loads the library until the process exits; sizes whose scratch need
+ * (fa_bwd_workspace_size) exceeds 16 MiB are rejected with FA_ERR_UNSUPPORTED
+ * before anything is launched.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current; make
+ * that first call before any stream capture.  All calls share the one array and
+ * it keeps the last call's contents: calls that overlap on the GPU (other
+ * streams, other host threads) race on it, so serialise them.  Nothing in it
+ * needs to start at zero: each call writes every scratch value it reads. */
+fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
+                         int H, int N, int d, int causal, float scale, fa_dtype dtype,
+                         void* stream);
+
 #ifdef __cplusplus
 }
 #endif
