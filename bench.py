@@ -50,6 +50,8 @@ KERNEL_SOURCES = {
     "bwd_pre_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
     "bwd_dkdv_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
     "bwd_dq_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
+    "bwd_fused_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd128.cu",
+    "bwd_dq_convert_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd128.cu",
 }
 
 
@@ -289,19 +291,25 @@ def run_ours(args, rank, world, local_rank):
     value = whole_job_tflops(fwd_f + bwd_f, world, ms)
     launches = sum(n for _, n in traced.values())
 
-    per = {kname: (tot / n if n else 0.0, n) for kname, (tot, n) in traced.items()}
+    traced = {kname: v for kname, v in traced.items() if v[1] > 0}
+    per = {kname: (tot / n, n) for kname, (tot, n) in traced.items()}
     fwd_ms = per["fwd_kernel"][0]
-    bwd_ms = sum(per[kk][0] for kk in ("bwd_pre_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"))
+    bwd_ms = sum(t for kname, (t, _) in per.items() if kname.startswith("bwd_"))
     peaks = load_peaks()
     # algorithmic work of one launch of each kernel
     elem = 2
     n_bytes = B * H * N * d * elem
     Np = (N + 127) // 128 * 128
+    acc_bytes = B * H * Np * d * 4 if d == 128 else 0     # fp32 dQ accumulator (head dim 128)
     alg = {
         "fwd_kernel": ("tensor", fwd_f),
+        "bwd_fused_kernel": ("tensor", bwd_f),           # all five backward products
         "bwd_dkdv_kernel": ("tensor", 0.8 * bwd_f),     # S, dP recompute, dV, dK: 4 of 5 products
         "bwd_dq_kernel": ("tensor", 0.2 * bwd_f),       # dQ: 1 of 5 products
-        "bwd_pre_kernel": ("hbm", 2 * n_bytes + 4 * B * H * N + 2 * 4 * B * H * Np),
+        # reads O, dO, L; writes D, L*log2e and (head dim 128) zeroes the accumulator
+        "bwd_pre_kernel": ("hbm", 2 * n_bytes + 4 * B * H * N + 2 * 4 * B * H * Np + acc_bytes),
+        # reads the fp32 accumulator rows < N, writes dQ
+        "bwd_dq_convert_kernel": ("hbm", B * H * N * d * 4 + n_bytes),
     }
     top = max(traced, key=lambda kk: traced[kk][0])
     bound, work = alg[top]

@@ -11,10 +11,6 @@
 #include "../../include/fa.h"
 #include "fa_internal.h"
 
-namespace fa {
-size_t bwd_workspace_bytes(long long BH, int N);
-}
-
 namespace {
 
 // Sticky status word written by kernels whose bounded wait ran out.
@@ -68,11 +64,13 @@ fa_status get_encoder(EncodeTiledFn* fn) {
 
 // 3-D map (d, N, B*H) over a dense (B,H,N,d) 16-bit array; box = one 128-row
 // tile of one swizzle width.  Rows >= N of a head read as zeros.
-fa_status make_map(CUtensorMap* m, const void* base, int d, int N, long long BH, bool bf16) {
+fa_status make_map(CUtensorMap* m, const void* base, int d, int N, long long BH, bool bf16,
+                   int box_rows = 128) {
   EncodeTiledFn enc;
   fa_status st = get_encoder(&enc);
   if (st != FA_OK) return st;
-  const fa::FwdTileInfo ti = fa::fwd_tile_info(d);
+  fa::FwdTileInfo ti = fa::fwd_tile_info(d);
+  ti.box_rows = box_rows;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
@@ -140,8 +138,9 @@ bool g_trace_on = false;
 int g_trace_n = 0;
 int g_trace_open = -1;   // record whose stop event is pending
 
-const char* const kTraceNames[fa::TR_NKINDS] = {"fwd_kernel", "bwd_pre_kernel", "bwd_dkdv_kernel",
-                                                "bwd_dq_kernel"};
+const char* const kTraceNames[fa::TR_NKINDS] = {"fwd_kernel",      "bwd_pre_kernel",
+                                                "bwd_dkdv_kernel", "bwd_dq_kernel",
+                                                "bwd_fused_kernel", "bwd_dq_convert_kernel"};
 
 }  // namespace
 
@@ -282,7 +281,7 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L,
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
   if (check_common(B, H, N, d, causal, 1.0f, FA_FP16) != FA_OK) return 0;
-  return fa::bwd_workspace_bytes(static_cast<long long>(B) * H, N);
+  return fa::bwd_workspace_bytes(static_cast<long long>(B) * H, N, d);
 }
 
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
@@ -297,7 +296,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
     if (!aligned(p, 16)) return FA_ERR_MISALIGNED;
   if (!aligned(L, 4) || (workspace && !aligned(workspace, 16))) return FA_ERR_MISALIGNED;
   const long long BH = static_cast<long long>(B) * H;
-  const size_t need = fa::bwd_workspace_bytes(BH, N);
+  const size_t need = fa::bwd_workspace_bytes(BH, N, d);
   if (workspace && workspace_bytes < need) return FA_ERR_INVALID_VALUE;
   const size_t nbytes = static_cast<size_t>(BH) * N * d * 2, lbytes = static_cast<size_t>(BH) * N * 4;
   const void* outs[3] = {dQ, dK, dV};
@@ -331,6 +330,15 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   a.dO = dO;
   a.L = L;
   a.Dvec = static_cast<float*>(ws);
+  if (d == 128) {
+    const long long Np = (static_cast<long long>(N) + 127) / 128 * 128;
+    a.dQacc = a.Dvec + 2 * BH * Np;
+    if ((st = make_map(&a.tmQ64, Q, d, N, BH, bf16, 64)) != FA_OK ||
+        (st = make_map(&a.tmdO64, dO, d, N, BH, bf16, 64)) != FA_OK) {
+      if (owned) cudaFreeAsync(ws, s);
+      return st;
+    }
+  }
   a.dQ = dQ;
   a.dK = dK;
   a.dV = dV;
@@ -386,7 +394,7 @@ fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void
                          void* stream) {
   fa_status st = check_common(B, H, N, d, causal, scale, static_cast<int>(dtype));
   if (st != FA_OK) return st;
-  const size_t need = fa::bwd_workspace_bytes(static_cast<long long>(B) * H, N);
+  const size_t need = fa::bwd_workspace_bytes(static_cast<long long>(B) * H, N, d);
   if (need > kNoAllocScratchBytes) return FA_ERR_UNSUPPORTED;   // more than the static scratch
   float* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != FA_OK) return st;
