@@ -130,8 +130,11 @@ fa_status fa_trace_read(int kind, double* total_ms, long long* launches);
  * array's device address (cudaGetSymbolAddress) with that device current; make
  * that first call before any stream capture.  All calls share the one array and
  * it keeps the last call's contents: calls that overlap on the GPU (other
- * streams, other host threads) race on it, so serialise them.  Nothing in it
- * needs to start at zero: each call writes every scratch value it reads. */
+ * streams, other host threads) race on it, so serialise them.  Each call
+ * writes every scratch value before reading it, and clears the part that must
+ * start at zero (the fp32 dQ accumulator used for head dim 128) first.
+ * Capacity: 8 bytes per row for head dims 32 and 64 (B*H*ceil(N/128)*128 up to
+ * 2,097,152 rows), 520 bytes per row for head dim 128 (up to 32,263 rows). */
 fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
                          const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
                          int H, int N, int d, int causal, float scale, fa_dtype dtype,
