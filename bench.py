@@ -48,10 +48,8 @@ DEFAULT_WORKLOAD = "n8k_causal_d128_bf16"
 KERNEL_SOURCES = {
     "fwd_kernel": "exact_io_aware_22_gb300/csrc/fa_fwd.cu",
     "bwd_pre_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
-    "bwd_dkdv_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
-    "bwd_dq_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
-    "bwd_fused_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd128.cu",
-    "bwd_dq_convert_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd128.cu",
+    "bwd_dkdv_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd128.cu",
+    "bwd_dq_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd128.cu",
 }
 
 
@@ -300,16 +298,12 @@ def run_ours(args, rank, world, local_rank):
     elem = 2
     n_bytes = B * H * N * d * elem
     Np = (N + 127) // 128 * 128
-    acc_bytes = B * H * Np * d * 4 if d == 128 else 0     # fp32 dQ accumulator (head dim 128)
     alg = {
         "fwd_kernel": ("tensor", fwd_f),
-        "bwd_fused_kernel": ("tensor", bwd_f),           # all five backward products
         "bwd_dkdv_kernel": ("tensor", 0.8 * bwd_f),     # S, dP recompute, dV, dK: 4 of 5 products
-        "bwd_dq_kernel": ("tensor", 0.2 * bwd_f),       # dQ: 1 of 5 products
-        # reads O, dO, L; writes D, L*log2e and (head dim 128) zeroes the accumulator
-        "bwd_pre_kernel": ("hbm", 2 * n_bytes + 4 * B * H * N + 2 * 4 * B * H * Np + acc_bytes),
-        # reads the fp32 accumulator rows < N, writes dQ
-        "bwd_dq_convert_kernel": ("hbm", B * H * N * d * 4 + n_bytes),
+        "bwd_dq_kernel": ("tensor", 0.2 * bwd_f),       # dQ: 1 of 5 products (S, dP recomputed)
+        # reads O, dO, L; writes D and L*log2e
+        "bwd_pre_kernel": ("hbm", 2 * n_bytes + 4 * B * H * N + 2 * 4 * B * H * Np),
     }
     top = max(traced, key=lambda kk: traced[kk][0])
     bound, work = alg[top]

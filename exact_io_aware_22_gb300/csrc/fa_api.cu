@@ -138,9 +138,8 @@ bool g_trace_on = false;
 int g_trace_n = 0;
 int g_trace_open = -1;   // record whose stop event is pending
 
-const char* const kTraceNames[fa::TR_NKINDS] = {"fwd_kernel",      "bwd_pre_kernel",
-                                                "bwd_dkdv_kernel", "bwd_dq_kernel",
-                                                "bwd_fused_kernel", "bwd_dq_convert_kernel"};
+const char* const kTraceNames[fa::TR_NKINDS] = {"fwd_kernel", "bwd_pre_kernel", "bwd_dkdv_kernel",
+                                                "bwd_dq_kernel"};
 
 }  // namespace
 
@@ -235,7 +234,8 @@ fa_status fa_device_status(void* stream) {
   const uint32_t zero = 0;
   e = cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e);
-  return (v & fa::FA_DEV_TIMEOUT) ? FA_ERR_TIMEOUT : FA_OK;
+  if (v & fa::FA_DEV_TIMEOUT) return FA_ERR_TIMEOUT;
+  return (v & fa::FA_DEV_SMEM_ALIGN) ? FA_ERR_UNSUPPORTED : FA_OK;
 }
 
 fa_status fa_selftest_timeout(unsigned long long limit_ns, void* stream) {
@@ -326,19 +326,11 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
     if (e != cudaSuccess) return cuda_fail(e);
     owned = true;
   }
+  a.Q = Q;
   a.O = O;
   a.dO = dO;
   a.L = L;
   a.Dvec = static_cast<float*>(ws);
-  if (d == 128) {
-    const long long Np = (static_cast<long long>(N) + 127) / 128 * 128;
-    a.dQacc = a.Dvec + 2 * BH * Np;
-    if ((st = make_map(&a.tmQ64, Q, d, N, BH, bf16, 64)) != FA_OK ||
-        (st = make_map(&a.tmdO64, dO, d, N, BH, bf16, 64)) != FA_OK) {
-      if (owned) cudaFreeAsync(ws, s);
-      return st;
-    }
-  }
   a.dQ = dQ;
   a.dK = dK;
   a.dV = dV;

@@ -72,8 +72,7 @@ __global__ void __launch_bounds__(256) pre_kernel(const void* __restrict__ O,
                                                   const void* __restrict__ dO,
                                                   const float* __restrict__ L,
                                                   float* __restrict__ Dp, float* __restrict__ Lp,
-                                                  float* __restrict__ dQacc, int N, int Np,
-                                                  long long rows_p) {
+                                                  int N, int Np, long long rows_p) {
   constexpr int TPR = D / 8;   // threads per row, 16 bytes each
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long rp = gt / TPR;
@@ -98,11 +97,6 @@ __global__ void __launch_bounds__(256) pre_kernel(const void* __restrict__ O,
   }
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (dQacc != nullptr && rp < rows_p) {   // the dQ accumulator starts at zero on every call
-    float4* z = reinterpret_cast<float4*>(dQacc + rp * D + part * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   if (rp < rows_p && part == 0) {
     Dp[rp] = src >= 0 ? acc : 0.f;
     Lp[rp] = src >= 0 ? L[src] * LOG2E : INFINITY;
@@ -544,12 +538,12 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     trace_begin(TR_BWD_PRE, st);
     pre_kernel<D, BF16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        a.O, a.dO, a.L, a.Dvec, Lp, D == 128 ? a.dQacc : nullptr, a.N, Np, rows_p);
+        a.O, a.dO, a.L, a.Dvec, Lp, a.N, Np, rows_p);
     trace_end(TR_BWD_PRE, st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if constexpr (D == 128) return launch_bwd128_fused(a, BF16, CAUSAL, st);
+  if constexpr (D == 128) return launch_bwd128(a, BF16, CAUSAL, st);
   {
     auto kern = dkdv_kernel<D, BF16, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -581,10 +575,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-size_t bwd_workspace_bytes(long long BH, int N, int d) {
+size_t bwd_workspace_bytes(long long BH, int N, int /*d*/) {
   const long long Np = static_cast<long long>((N + BM - 1) / BM) * BM;
-  const long long acc = d == 128 ? BH * Np * 128 : 0;
-  return static_cast<size_t>(2 * BH * Np + acc) * sizeof(float);
+  return static_cast<size_t>(2 * BH * Np) * sizeof(float);
 }
 
 cudaError_t launch_bwd(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {

@@ -1,35 +1,45 @@
-// fa_bwd128.cu -- fused attention backward for head dim 128 on sm_103a.
+// fa_bwd128.cu -- attention backward for head dim 128 on sm_103a.
 //
 // Method: "flash-attn-triton" docs page, section "Scope" (backward kernels for
 // dQ, dK, dV that rebuild P from the saved L; causal mask only on diagonal
-// tiles; ragged N) and "Source" (delta pre-pass, then dK/dV and dQ).  Gradients
-// follow the chain rule of the forward:
+// tiles; ragged N) and "Source" (delta pre-pass, then dK/dV, then dQ).
+// Gradients follow the chain rule of the forward:
 //   P = exp(S - L),  dV = P^T dO,  dP = dO V^T,  D = rowsum(dO o O),
 //   dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
 //
-// One CTA per 128-key block (K, V stay in shared memory); the loop runs over
-// 64-query tiles (causal: from the diagonal down).  Per tile, five tcgen05
-// products, accumulators in TMEM (512 columns):
-//   [  0,128) dV += P^T dO        A = P^T from TMEM (double-buffered), B = dO
-//   [128,256) dK += dS^T Q        A = dS^T swizzled in smem (double-buffered)
-//   [256,320) S^T  = K Q^T        fp32, 128 keys x 64 queries
-//   [320,384) dP^T = V dO^T
-//   [384,448) dQ^T = K^T dS^T     fp32, 128 (head dim) x 64 queries
-//   [448,512) P^T, two buffers of 32 columns (64 packed 16-bit queries)
-// Roles (512 threads, one CTA per SM):
-//   warp 0       TMA producer: K, V once; Q, dO tiles plus their L, D into a ring.
-//   warp 1       TMEM allocator; lane 0 issues every MMA and commit.
-//   warps 4-11   two compute warpgroups, one thread per key row, 32 query
-//                columns each: rebuild P^T and dS^T from S^T, dP^T, L, D.
-//   warps 12-15  dQ warpgroup, one thread per head-dim row of dQ^T: takes the
-//                tile out of TMEM and adds it into the fp32 dQ accumulator with
-//                fp32 reductions at L2 (each warp instruction covers 32
-//                consecutive head-dim floats of one query row).  Going straight
-//                from registers keeps the tile out of shared memory, whose
-//                bandwidth the N = 64 MMAs already saturate.
-// The compute warps release S^T / dP^T as soon as they hold them in registers,
-// so the next tile's S^T, dP^T MMAs overlap this tile's softmax-like work, and
-// this tile's dV, dK, dQ^T MMAs overlap the next tile's.
+// Two kernels after the pre-pass, both with every tensor product a tcgen05 MMA
+// of M = 128, N = 128 (an M = 128 MMA costs about as much at N = 64 as at
+// N = 128 on this part, so narrower tiles waste half the tensor rate):
+//
+//   dkdv_kernel  key-stationary: one CTA per 128-key block, K and V in shared
+//                memory, loop over 128-query tiles (causal: from the diagonal
+//                down).  TMEM: dV | dK | R | X, 128 columns each.  R holds
+//                S^T = K Q^T, then dP^T = V dO^T once the compute warps hold
+//                S^T in registers, then the next tile's S^T once they hold dP^T.
+//                X holds P^T as 16-bit pairs in two 64-column buffers (A operand
+//                of dV += P^T dO); dS^T goes to shared memory (A operand of
+//                dK += dS^T Q).  Pipe order per tile i: dP^T(i), S^T(i+1),
+//                dV(i), dK(i).
+//   dq_kernel    query-stationary: one CTA per 128-query tile, loop over 128-key
+//                blocks (causal: up to the diagonal).  Each compute thread of the
+//                first warpgroup copies its row of Q into TMEM once, so S = Q K^T
+//                takes its A operand from TMEM; shared memory holds dO and a
+//                three-stage K/V ring (one block's loads take longer than its
+//                MMAs; two stages left the tensor pipe waiting).  TMEM:
+//                dQ | S | dP | Z (64) | Q (64).  S and dP have columns of their
+//                own, so the next block's S and dP start as soon as the compute
+//                warps hold this block's; dS = P o (dP - D) goes as 16-bit pairs
+//                into Z and feeds dQ += dS K from TMEM.
+// Recomputing S and dP for dQ costs two extra products, but it needs no
+// cross-CTA reduction: accumulating dQ partials in fp32 at L2 from the
+// key-stationary kernel is bound by L2 reduction throughput on this part
+// (about 3 TB/s, i.e. ~1.4 ms for the 4.4 GB of partials at N = 8192 causal),
+// and the split form is deterministic.
+//
+// Roles in both kernels (384 threads, one CTA per SM):
+//   warp 0       TMA producer.   warp 1  TMEM allocator; lane 0 issues MMAs.
+//   warps 4-11   two compute warpgroups, one thread per TMEM lane (a key row
+//                in dkdv, a query row in dq), 64 columns each.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -40,34 +50,12 @@ namespace fa {
 namespace {
 
 constexpr int HD = 128;          // head dim
-constexpr int BN = 128;          // keys per CTA
-constexpr int BQ = 64;           // queries per iteration
-constexpr int THREADS = 512;
-constexpr int STAGES = 3;
-constexpr float LOG2E = 1.4426950408889634f;
+constexpr int BT = 128;          // rows of every tile (keys or queries)
+constexpr int THREADS = 384;
+constexpr int STAGES = 2;
 
-constexpr int KT_BYTES = BN * HD * 2;           // K or V tile: two 64-column chunks
-constexpr int KT_CHUNK = BN * 128;              // 16 KiB
-constexpr int QT_BYTES = BQ * HD * 2;           // Q or dO tile: two 64-column chunks
-constexpr int QT_CHUNK = BQ * 128;              // 8 KiB
-constexpr int DS_BYTES = BN * BQ * 2;           // dS^T tile: one 128-byte row per key
-constexpr int K_OFF = 0;
-constexpr int V_OFF = KT_BYTES;
-constexpr int Q_OFF = 2 * KT_BYTES;
-constexpr int DO_OFF = Q_OFF + STAGES * QT_BYTES;
-constexpr int DS_OFF = DO_OFF + STAGES * QT_BYTES;
-constexpr int LD_OFF = DS_OFF + 2 * DS_BYTES;   // per stage: 64 L*log2e, then 64 D
-constexpr int BAR_OFF = LD_OFF + STAGES * 512;
-// kv_full, q_full[S], q_empty[S], s_full, sp_free, p_full[2], dq_full, dq_empty, o_full, done.
-// p_full alternates by tile parity: the compute warps may finish tile i+1 before the MMA
-// thread has observed tile i, and one barrier would then have run two phases ahead.
-constexpr int NBARS = 1 + 2 * STAGES + 8;
-constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
-constexpr int SMEM_BYTES = SLOT_OFF + 16 + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
-
-constexpr uint32_t DV_COL = 0, DK_COL = 128, S_COL = 256, DP_COL = 320, DQ_COL = 384,
-                   P_COL = 448;
+constexpr int TILE = BT * HD * 2;               // a 128-row tile: two 64-column chunks
+constexpr int CHUNK = BT * 128;                 // 16 KiB
 
 // 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -78,40 +66,90 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
+
+// X^T = A B^T over the head dim into TMEM columns d_col: A and B are 128-row
+// K-major tiles (two 64-column chunks each).
+__device__ __forceinline__ void issue_ab_t(uint32_t d_tmem, uint32_t a, uint32_t b, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    const uint32_t o = (kk / 4) * CHUNK + (kk % 4) * 32;
+    umma_ss(d_tmem, umma_sdesc(a + o, 16, 1024, UMMA_SW128), umma_sdesc(b + o, 16, 1024, UMMA_SW128),
+            idesc, kk > 0);
+  }
+}
+
+// Epilogue: 64 fp32 TMEM columns of this thread's lane, times mul, rounded to the
+// 16-bit type and stored as one contiguous 128-byte run (when valid).
+template <bool BF16>
+__device__ __forceinline__ void store_row64(uint32_t taddr, float mul, void* dst, bool valid) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t v[16];
+    tmem_ld16(taddr + 16 * cc, v);
+    tmem_ld_wait_regs(v);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+    if (valid) {
+      uint4* d4 = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dst) + 32 * cc);
+      d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
+}
+
+// ============================================================== dK / dV
+namespace kv {
+constexpr int K_OFF = 0, V_OFF = TILE, Q_OFF = 2 * TILE;
+constexpr int DO_OFF = Q_OFF + STAGES * TILE;
+constexpr int DS_OFF = DO_OFF + STAGES * TILE;  // dS^T: 128 keys x 128 queries, two chunks
+constexpr int LD_OFF = DS_OFF + TILE;           // per stage: 128 L*log2e, then 128 D
+constexpr int BAR_OFF = LD_OFF + STAGES * 1024;
+// kv_full, q_full[S], q_empty[S], s_full, s_free, dp_full, dp_free, p_full[2], ds_free, o_full, done
+constexpr int NBARS = 1 + 2 * STAGES + 9;
+constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
+constexpr int SMEM_BYTES = SLOT_OFF + 16;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
+constexpr uint32_t DV_COL = 0, DK_COL = 128, R_COL = 256, X_COL = 384;
+}  // namespace kv
+
 template <bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
-    bwd128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  float* __restrict__ dQacc, const float* __restrict__ Dp,
-                  const float* __restrict__ Lp, void* __restrict__ dK, void* __restrict__ dV,
-                  int N, int Np, float scale, float c_log2, KernelCtl ctl) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sb = (raw + 1023u) & ~1023u;
-  uint8_t* sg = smem_raw + (sb - raw);
-
+    dkdv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                   const float* __restrict__ Dp, const float* __restrict__ Lp,
+                   void* __restrict__ dK, void* __restrict__ dV, int N, int Np, float scale,
+                   float c_log2, KernelCtl ctl) {
+  using namespace kv;
+  extern __shared__ __align__(1024) uint8_t sg[];
+  const uint32_t sb = smem_u32(sg);
+  if (sb & 1023u) {                                // see FA_DEV_SMEM_ALIGN
+    if (threadIdx.x == 0) atomicOr(ctl.status, FA_DEV_SMEM_ALIGN);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = (N + BN - 1) / BN;
-  const int nq = (N + BQ - 1) / BQ;
+  const int nkb = (N + BT - 1) / BT;
+  const int nq = Np / BT;
   const int bh = blockIdx.x / nkb;
   const int kb = blockIdx.x % nkb;                 // causal: block 0 has the most work, runs first
-  const int q_start = CAUSAL ? kb * (BN / BQ) : 0;
+  const int q_start = CAUSAL ? kb : 0;             // the diagonal query tile
   const int n_iter = nq - q_start;
 
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
   const int B_KV = 0;
   auto B_QF = [&](int s) { return 1 + s; };
   auto B_QE = [&](int s) { return 1 + STAGES + s; };
-  const int B_SF = 1 + 2 * STAGES, B_SPF = B_SF + 1, B_DQF = B_SF + 2, B_DQE = B_SF + 3,
-            B_OF = B_SF + 4, B_DONE = B_SF + 5;
-  auto B_PF = [&](int b) { return B_SF + 6 + b; };
+  const int B_SF = 1 + 2 * STAGES, B_SFREE = B_SF + 1, B_DPF = B_SF + 2, B_DPFREE = B_SF + 3;
+  auto B_PF = [&](int b) { return B_SF + 4 + b; };   // per P^T buffer: two phases never overlap
+  const int B_DSFREE = B_SF + 6, B_OF = B_SF + 7, B_DONE = B_SF + 8;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBARS; ++i) mbar_init(bar(i), 1);
-    mbar_init(bar(B_SPF), 256);
+    mbar_init(bar(B_SFREE), 256);
+    mbar_init(bar(B_DPFREE), 256);
     mbar_init(bar(B_PF(0)), 256);
     mbar_init(bar(B_PF(1)), 256);
-    mbar_init(bar(B_DQE), 128);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -125,36 +163,29 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (n_iter > 0) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(B_KV), 2 * KT_BYTES);
-        for (int c = 0; c < 2; ++c) {
-          tma_load_3d(sb + K_OFF + c * KT_CHUNK, &tmK, bar(B_KV), c * 64, kb * BN, bh);
-          tma_load_3d(sb + V_OFF + c * KT_CHUNK, &tmV, bar(B_KV), c * 64, kb * BN, bh);
-        }
+    if (lane == 0 && n_iter > 0) {
+      mbar_arrive_expect_tx(bar(B_KV), 2 * TILE);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_3d(sb + K_OFF + c * CHUNK, &tmK, bar(B_KV), c * 64, kb * BT, bh);
+        tma_load_3d(sb + V_OFF + c * CHUNK, &tmV, bar(B_KV), c * 64, kb * BT, bh);
       }
       bool ok = true;
       int it = 0;
-      if (lane == 0) {
-        for (; it < n_iter; ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!(ok = mbar_wait(bar(B_QE(s)), ph ^ 1, ctl))) break;
-          const int qrow = (q_start + it) * BQ;
-          mbar_arrive_expect_tx(bar(B_QF(s)), 2 * QT_BYTES + 512);
-          for (int c = 0; c < 2; ++c) {
-            tma_load_3d(sb + Q_OFF + s * QT_BYTES + c * QT_CHUNK, &tmQ, bar(B_QF(s)), c * 64, qrow,
-                        bh);
-            tma_load_3d(sb + DO_OFF + s * QT_BYTES + c * QT_CHUNK, &tmdO, bar(B_QF(s)), c * 64,
-                        qrow, bh);
-          }
-          // L*log2e and D of the 64 queries (padded per-row arrays, 256-byte aligned rows)
-          const size_t row = static_cast<size_t>(bh) * Np + qrow;
-          bulk_load(sb + LD_OFF + s * 512, Lp + row, 256, bar(B_QF(s)));
-          bulk_load(sb + LD_OFF + s * 512 + 256, Dp + row, 256, bar(B_QF(s)));
+      for (; it < n_iter; ++it) {
+        const int s = it % STAGES;
+        if (!(ok = mbar_wait(bar(B_QE(s)), ((it / STAGES) & 1) ^ 1, ctl))) break;
+        const int qrow = (q_start + it) * BT;
+        mbar_arrive_expect_tx(bar(B_QF(s)), 2 * TILE + 1024);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_3d(sb + Q_OFF + s * TILE + c * CHUNK, &tmQ, bar(B_QF(s)), c * 64, qrow, bh);
+          tma_load_3d(sb + DO_OFF + s * TILE + c * CHUNK, &tmdO, bar(B_QF(s)), c * 64, qrow, bh);
         }
+        // L*log2e and D of the 128 queries (padded per-row arrays, 512-byte aligned rows)
+        const size_t row = static_cast<size_t>(bh) * Np + qrow;
+        bulk_load(sb + LD_OFF + s * 1024, Lp + row, 512, bar(B_QF(s)));
+        bulk_load(sb + LD_OFF + s * 1024 + 512, Dp + row, 512, bar(B_QF(s)));
       }
-      if (!ok && lane == 0) {
+      if (!ok) {
         mbar_wait(bar(B_KV), 0, ctl);
         for (int jj = max(0, it - STAGES); jj < it; ++jj)
           mbar_wait(bar(B_QF(jj % STAGES)), (jj / STAGES) & 1, ctl);
@@ -164,64 +195,46 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_iter > 0) {
-      constexpr uint32_t idS = umma_idesc_f16(BN, BQ, BF16, false, false);   // S^T, dP^T
-      constexpr uint32_t idG = umma_idesc_f16(BN, HD, BF16, false, true);    // dV, dK
-      constexpr uint32_t idQ = umma_idesc_f16(HD, BQ, BF16, true, true);     // dQ^T
-      auto issue_sdp = [&](int it) {
-        const int s = it % STAGES;
-        const uint32_t qa = sb + Q_OFF + s * QT_BYTES, da = sb + DO_OFF + s * QT_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t ok_ = (kk / 4) * KT_CHUNK + (kk % 4) * 32;
-          const uint32_t oq = (kk / 4) * QT_CHUNK + (kk % 4) * 32;
-          umma_ss(tmem + S_COL, umma_sdesc(sb + K_OFF + ok_, 16, 1024, UMMA_SW128),
-                  umma_sdesc(qa + oq, 16, 1024, UMMA_SW128), idS, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t ok_ = (kk / 4) * KT_CHUNK + (kk % 4) * 32;
-          const uint32_t oq = (kk / 4) * QT_CHUNK + (kk % 4) * 32;
-          umma_ss(tmem + DP_COL, umma_sdesc(sb + V_OFF + ok_, 16, 1024, UMMA_SW128),
-                  umma_sdesc(da + oq, 16, 1024, UMMA_SW128), idS, kk > 0);
-        }
-      };
+      constexpr uint32_t idS = umma_idesc_f16(BT, BT, BF16, false, false);   // S^T, dP^T
+      constexpr uint32_t idG = umma_idesc_f16(BT, HD, BF16, false, true);    // dV, dK
       bool ok = mbar_wait(bar(B_KV), 0, ctl) && mbar_wait(bar(B_QF(0)), 0, ctl);
       if (ok) {
         tc_fence_after();
-        issue_sdp(0);
+        issue_ab_t(tmem + R_COL, sb + K_OFF, sb + Q_OFF, idS);
         umma_commit(bar(B_SF));
       }
       for (int it = 0; ok && it < n_iter; ++it) {
         const int s = it % STAGES, b = it & 1;
-        const uint32_t qa = sb + Q_OFF + s * QT_BYTES, da = sb + DO_OFF + s * QT_BYTES;
-        const uint32_t dsa = sb + DS_OFF + b * DS_BYTES;
+        const uint32_t qa = sb + Q_OFF + s * TILE, da = sb + DO_OFF + s * TILE;
+        // dP^T into R once the compute warps hold S^T
+        if (!(ok = mbar_wait(bar(B_SFREE), it & 1, ctl))) break;
+        tc_fence_after();
+        issue_ab_t(tmem + R_COL, sb + V_OFF, da, idS);
+        umma_commit(bar(B_DPF));
+        // the next S^T into R once they hold dP^T
+        if (!(ok = mbar_wait(bar(B_DPFREE), it & 1, ctl))) break;
         if (it + 1 < n_iter) {
-          // S^T, dP^T of the next tile once the compute warps hold this tile's in registers
-          if (!(ok = mbar_wait(bar(B_SPF), it & 1, ctl))) break;
-          if (!(ok = mbar_wait(bar(B_QF((it + 1) % STAGES)), ((it + 1) / STAGES) & 1, ctl))) break;
+          const int s1 = (it + 1) % STAGES;
+          if (!(ok = mbar_wait(bar(B_QF(s1)), ((it + 1) / STAGES) & 1, ctl))) break;
           tc_fence_after();
-          issue_sdp(it + 1);
+          issue_ab_t(tmem + R_COL, sb + K_OFF, sb + Q_OFF + s1 * TILE, idS);
           umma_commit(bar(B_SF));
         }
+        // P^T(i) is in X buffer b and dS^T(i) in shared memory
         if (!(ok = mbar_wait(bar(B_PF(b)), (it >> 1) & 1, ctl))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)       // dV += P^T dO
-          umma_ts(tmem + DV_COL, tmem + P_COL + 32 * b + 8 * kk,
-                  umma_sdesc(da + kk * 2048, QT_CHUNK, 1024, UMMA_SW128), idG,
+        for (int kk = 0; kk < BT / 16; ++kk)       // dV += P^T dO
+          umma_ts(tmem + DV_COL, tmem + X_COL + 64 * b + (kk / 4) * 32 + (kk % 4) * 8,
+                  umma_sdesc(da + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
                   (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)       // dK += dS^T Q
-          umma_ss(tmem + DK_COL, umma_sdesc(dsa + kk * 32, 16, 1024, UMMA_SW128),
-                  umma_sdesc(qa + kk * 2048, QT_CHUNK, 1024, UMMA_SW128), idG,
+        for (int kk = 0; kk < BT / 16; ++kk)       // dK += dS^T Q
+          umma_ss(tmem + DK_COL,
+                  umma_sdesc(sb + DS_OFF + (kk / 4) * CHUNK + (kk % 4) * 32, 16, 1024, UMMA_SW128),
+                  umma_sdesc(qa + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
                   (it > 0 || kk > 0) ? 1u : 0u);
-        if (it > 0 && !(ok = mbar_wait(bar(B_DQE), (it - 1) & 1, ctl))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)       // dQ^T = K^T dS^T
-          umma_ss(tmem + DQ_COL, umma_sdesc(sb + K_OFF + kk * 2048, KT_CHUNK, 1024, UMMA_SW128),
-                  umma_sdesc(dsa + kk * 2048, KT_CHUNK, 1024, UMMA_SW128), idQ, kk > 0);
-        umma_commit(bar(B_DQF));
+        umma_commit(bar(B_DSFREE));
         umma_commit(bar(B_QE(s)));
       }
       if (ok) umma_commit(bar(B_OF));
@@ -229,57 +242,85 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(bar(B_DONE), 0, ctl);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ compute
-    const int h = (warp - 4) >> 2;                 // query columns [32h, 32h + 32)
+    const int h = (warp - 4) >> 2;                 // query columns [64h, 64h + 64)
     const int kr = (warp & 3) * 32 + lane;         // key row (= TMEM lane)
-    const int gkey = kb * BN + kr;
+    const int gkey = kb * BT + kr;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tR = tmem + lane_off + R_COL + 64 * h;
+    uint8_t* ds_row = sg + DS_OFF + h * CHUNK + kr * 128;
+    const float2 c2 = make_float2(c_log2, c_log2);
     bool ok = n_iter > 0;
     for (int it = 0; ok && it < n_iter; ++it) {
       const int s = it % STAGES, b = it & 1;
-      const int q0 = (q_start + it) * BQ + 32 * h;  // first query of this thread's columns
+      const int q0 = (q_start + it) * BT + 64 * h;  // first query of this thread's columns
+      const bool diag = CAUSAL && it == 0;
       if (!(ok = mbar_wait(bar(B_SF), it & 1, ctl))) break;
       tc_fence_after();
-      uint32_t sr[32], dp[32];
-      tmem_ld32(tmem + lane_off + S_COL + 32 * h, sr);
-      tmem_ld32(tmem + lane_off + DP_COL + 32 * h, dp);
-      tmem_ld_wait_regs(sr);
-      tmem_ld_wait_regs(dp);
+      uint32_t x[64];
+      tmem_ld32(tR, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(tR + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
       tc_fence_before();
-      mbar_arrive(bar(B_SPF));
+      mbar_arrive(bar(B_SFREE));                   // R may now receive dP^T
       if (!(ok = mbar_wait(bar(B_QF(s)), (it / STAGES) & 1, ctl))) break;
-      const float4* L4 = reinterpret_cast<const float4*>(sg + LD_OFF + s * 512 + 32 * h * 4);
-      const float4* D4 = reinterpret_cast<const float4*>(sg + LD_OFF + s * 512 + 256 + 32 * h * 4);
-      const bool diag = CAUSAL && it < BN / BQ;
-      uint32_t pw[16];
-      uint8_t* ds_row = sg + DS_OFF + b * DS_BYTES + kr * 128;
+      const float* Ls = reinterpret_cast<const float*>(sg + LD_OFF + s * 1024) + 64 * h;
+      const float* Ds = Ls + 128;
+      // P^T = exp2(S^T c - L log2e); on the diagonal tile, zero where the query precedes
+      // the key
+      float p[64];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {                // 8 queries = one 16-byte chunk of dS^T
-        const float4 la = L4[2 * u], lb = L4[2 * u + 1];
-        const float4 da = D4[2 * u], db = D4[2 * u + 1];
-        const float lq[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(Ls + 4 * c4);
+        const float2 t0 = fma2(make_float2(__uint_as_float(x[4 * c4]), __uint_as_float(x[4 * c4 + 1])),
+                               c2, make_float2(-l4.x, -l4.y));
+        const float2 t1 = fma2(make_float2(__uint_as_float(x[4 * c4 + 2]), __uint_as_float(x[4 * c4 + 3])),
+                               c2, make_float2(-l4.z, -l4.w));
+        p[4 * c4] = ex2(t0.x);
+        p[4 * c4 + 1] = ex2(t0.y);
+        p[4 * c4 + 2] = ex2(t1.x);
+        p[4 * c4 + 3] = ex2(t1.y);
+      }
+      if (diag) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (q0 + c < gkey) p[c] = 0.f;
+      }
+      if (!(ok = mbar_wait(bar(B_DPF), it & 1, ctl))) break;
+      tc_fence_after();
+      tmem_ld32(tR, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(tR + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tc_fence_before();
+      mbar_arrive(bar(B_DPFREE));                  // R may now receive the next S^T
+      // the dK MMAs of the previous tile have finished reading dS^T
+      if (it > 0 && !(ok = mbar_wait(bar(B_DSFREE), (it - 1) & 1, ctl))) break;
+      // dS^T = P^T o (dP^T - D) to shared memory (128-byte swizzle: chunk u of row kr at
+      // u ^ (kr & 7)); P^T as 16-bit pairs into X buffer b (its last reader, dV two tiles
+      // back, finished before the dK MMAs waited on above)
+      uint32_t pw[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 da = *reinterpret_cast<const float4*>(Ds + 8 * u);
+        const float4 db = *reinterpret_cast<const float4*>(Ds + 8 * u + 4);
         const float dq[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-        float p[8], ds[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = 8 * u + e;
-          float pv = ex2(fmaf(__uint_as_float(sr[c]), c_log2, -lq[e]));
-          if (diag && q0 + c < gkey) pv = 0.f;
-          p[e] = pv;
-          ds[e] = pv * (__uint_as_float(dp[c]) - dq[e]);
-        }
         uint32_t dw[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          pw[4 * u + e] = pack2<BF16>(p[2 * e], p[2 * e + 1]);
-          dw[e] = pack2<BF16>(ds[2 * e], ds[2 * e + 1]);
+          const int c = 8 * u + 2 * e;
+          const float2 ds = mul2(make_float2(p[c], p[c + 1]),
+                                 add2(make_float2(__uint_as_float(x[c]), __uint_as_float(x[c + 1])),
+                                      make_float2(-dq[2 * e], -dq[2 * e + 1])));
+          dw[e] = pack2<BF16>(ds.x, ds.y);
+          pw[4 * u + e] = pack2<BF16>(p[c], p[c + 1]);
         }
-        const int chunk = 4 * h + u;               // 128-byte swizzle: chunk ^ (row & 7)
-        *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (kr & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(ds_row + ((u ^ (kr & 7)) << 4)) =
             make_uint4(dw[0], dw[1], dw[2], dw[3]);
       }
-      tmem_st16(tmem + lane_off + P_COL + 32 * b + 16 * h, pw);
+      tmem_st32(tmem + lane_off + X_COL + 64 * b + 32 * h, pw);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -290,49 +331,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       const bool valid = gkey < N;
       const size_t roff = (static_cast<size_t>(bh) * N + gkey) * HD + 64 * h;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = (which == 0 ? DV_COL : DK_COL) + 64 * h;
-        const float mul = which == 0 ? 1.f : scale;
-        T* dst = reinterpret_cast<T*>(which == 0 ? dV : dK) + roff;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_off + col + 16 * cc, v);
-          tmem_ld_wait_regs(v);
-          uint32_t w[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            w[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * cc);
-            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          }
-        }
-      }
-    }
-  } else if (warp >= 12) {
-    // ------------------------------------------------------------ dQ accumulation
-    const int dr = (warp & 3) * 32 + lane;         // head-dim row of dQ^T (= TMEM lane)
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float* acc = dQacc + static_cast<size_t>(bh) * Np * HD + dr;
-    bool ok = n_iter > 0;
-    for (int it = 0; ok && it < n_iter; ++it) {
-      if (!(ok = mbar_wait(bar(B_DQF), it & 1, ctl))) break;
-      tc_fence_after();
-      uint32_t v0[32], v1[32];
-      tmem_ld32(tmem + lane_off + DQ_COL, v0);
-      tmem_ld32(tmem + lane_off + DQ_COL + 32, v1);
-      tmem_ld_wait_regs(v0);
-      tmem_ld_wait_regs(v1);
-      tc_fence_before();
-      mbar_arrive(bar(B_DQE));
-      float* row = acc + static_cast<size_t>((q_start + it) * BQ) * HD;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) atomicAdd(row + c * HD, __uint_as_float(v0[c]));
-#pragma unroll
-      for (int c = 0; c < 32; ++c) atomicAdd(row + (32 + c) * HD, __uint_as_float(v1[c]));
+      store_row64<BF16>(tmem + lane_off + DV_COL + 64 * h, 1.f, reinterpret_cast<T*>(dV) + roff,
+                        valid);
+      store_row64<BF16>(tmem + lane_off + DK_COL + 64 * h, scale, reinterpret_cast<T*>(dK) + roff,
+                        valid);
     }
   }
   tc_fence_before();
@@ -343,54 +345,279 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// dQ = scale * dQacc, rounded to the 16-bit type (rows < N only).
-template <bool BF16>
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
-                                                         void* __restrict__ dQ, int N, int Np,
-                                                         long long n8, float scale) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const long long row = i / (HD / 8);
-  const int part = static_cast<int>(i % (HD / 8));
-  const long long bh = row / N;
-  const int r = static_cast<int>(row % N);
-  const float4* src = reinterpret_cast<const float4*>(acc + ((bh * Np + r) * HD + part * 8));
-  const float4 a = src[0], b = src[1];
-  uint4 w;
-  w.x = pack2<BF16>(a.x * scale, a.y * scale);
-  w.y = pack2<BF16>(a.z * scale, a.w * scale);
-  w.z = pack2<BF16>(b.x * scale, b.y * scale);
-  w.w = pack2<BF16>(b.z * scale, b.w * scale);
-  reinterpret_cast<uint4*>(dQ)[i] = w;
+// ============================================================== dQ
+namespace qd {
+constexpr int KV_STAGES = 3;
+constexpr int DO_OFF = 0;
+constexpr int K_OFF = TILE;
+constexpr int V_OFF = K_OFF + KV_STAGES * TILE;
+constexpr int BAR_OFF = V_OFF + KV_STAGES * TILE;
+// do_full, kv_full[S], kv_empty[S], q_ready, s_full, s_free, dp_full, dp_free, ds_full, z_free,
+// o_full, done
+constexpr int NBARS = 1 + 2 * KV_STAGES + 9;
+constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
+constexpr int SMEM_BYTES = SLOT_OFF + 16;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
+// dQ accumulator | S | dP | Z (dS, 16-bit pairs) | Q (16-bit pairs)
+constexpr uint32_t DQ_COL = 0, S_COL = 128, DP_COL = 256, Z_COL = 384, QT_COL = 448;
+}  // namespace qd
+
+template <bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(THREADS, 1)
+    dq128_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmdO, const void* __restrict__ Q,
+                 const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dQ,
+                 int N, int Np, float scale, float c_log2, KernelCtl ctl) {
+  using namespace qd;
+  extern __shared__ __align__(1024) uint8_t sg[];
+  const uint32_t sb = smem_u32(sg);
+  if (sb & 1023u) {                                // see FA_DEV_SMEM_ALIGN
+    if (threadIdx.x == 0) atomicOr(ctl.status, FA_DEV_SMEM_ALIGN);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nqb = Np / BT;
+  const int nkb = (N + BT - 1) / BT;
+  const int bh = blockIdx.x / nqb;
+  const int qb = nqb - 1 - (blockIdx.x % nqb);     // causal: longest query tiles first
+  const int n_iter = CAUSAL ? min(qb + 1, nkb) : nkb;
+
+  auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
+  const int B_DOF = 0;
+  auto B_KF = [&](int s) { return 1 + s; };
+  auto B_KE = [&](int s) { return 1 + KV_STAGES + s; };
+  const int B_QR = 1 + 2 * KV_STAGES, B_SF = B_QR + 1, B_SFREE = B_QR + 2, B_DPF = B_QR + 3,
+            B_DPFREE = B_QR + 4, B_DSF = B_QR + 5, B_ZFREE = B_QR + 6, B_OF = B_QR + 7,
+            B_DONE = B_QR + 8;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NBARS; ++i) mbar_init(bar(i), 1);
+    mbar_init(bar(B_QR), 128);
+    mbar_init(bar(B_SFREE), 256);
+    mbar_init(bar(B_DPFREE), 256);
+    mbar_init(bar(B_DSF), 256);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + SLOT_OFF, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sg + SLOT_OFF);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (dO once, K/V ring)
+    if (lane == 0 && n_iter > 0) {
+      mbar_arrive_expect_tx(bar(B_DOF), TILE);
+      for (int c = 0; c < 2; ++c)
+        tma_load_3d(sb + DO_OFF + c * CHUNK, &tmdO, bar(B_DOF), c * 64, qb * BT, bh);
+      bool ok = true;
+      int j = 0;
+      for (; j < n_iter; ++j) {
+        const int s = j % KV_STAGES;
+        if (!(ok = mbar_wait(bar(B_KE(s)), ((j / KV_STAGES) & 1) ^ 1, ctl))) break;
+        mbar_arrive_expect_tx(bar(B_KF(s)), 2 * TILE);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_3d(sb + K_OFF + s * TILE + c * CHUNK, &tmK, bar(B_KF(s)), c * 64, j * BT, bh);
+          tma_load_3d(sb + V_OFF + s * TILE + c * CHUNK, &tmV, bar(B_KF(s)), c * 64, j * BT, bh);
+        }
+      }
+      if (!ok) {
+        mbar_wait(bar(B_DOF), 0, ctl);
+        for (int jj = max(0, j - KV_STAGES); jj < j; ++jj)
+          mbar_wait(bar(B_KF(jj % KV_STAGES)), (jj / KV_STAGES) & 1, ctl);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_iter > 0) {
+      constexpr uint32_t idS = umma_idesc_f16(BT, BT, BF16, false, false);   // S, dP
+      constexpr uint32_t idQ = umma_idesc_f16(BT, HD, BF16, false, true);    // dQ
+      auto issue_s = [&](int st) {                   // S = Q K^T, Q from TMEM
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_ts(tmem + S_COL, tmem + QT_COL + kk * 8,
+                  umma_sdesc(sb + K_OFF + st * TILE + (kk / 4) * CHUNK + (kk % 4) * 32, 16, 1024,
+                             UMMA_SW128),
+                  idS, kk > 0);
+      };
+      auto issue_dp = [&](int st) {                  // dP = dO V^T
+        issue_ab_t(tmem + DP_COL, sb + DO_OFF, sb + V_OFF + st * TILE, idS);
+      };
+      bool ok = mbar_wait(bar(B_QR), 0, ctl) && mbar_wait(bar(B_DOF), 0, ctl) &&
+                mbar_wait(bar(B_KF(0)), 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        umma_commit(bar(B_SF));
+        issue_dp(0);
+        umma_commit(bar(B_DPF));
+      }
+      for (int j = 0; ok && j < n_iter; ++j) {
+        const int s = j % KV_STAGES;
+        if (j + 1 < n_iter) {
+          // the next block's S and dP as soon as the compute warps hold this block's
+          const int s1 = (j + 1) % KV_STAGES;
+          if (!(ok = mbar_wait(bar(B_KF(s1)), ((j + 1) / KV_STAGES) & 1, ctl))) break;
+          if (!(ok = mbar_wait(bar(B_SFREE), j & 1, ctl))) break;
+          tc_fence_after();
+          issue_s(s1);
+          umma_commit(bar(B_SF));
+          if (!(ok = mbar_wait(bar(B_DPFREE), j & 1, ctl))) break;
+          tc_fence_after();
+          issue_dp(s1);
+          umma_commit(bar(B_DPF));
+        }
+        // dQ += dS K: dS from Z, K as an MN-major B
+        if (!(ok = mbar_wait(bar(B_DSF), j & 1, ctl))) break;
+        tc_fence_after();
+        const uint32_t ka = sb + K_OFF + s * TILE;
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)
+          umma_ts(tmem + DQ_COL, tmem + Z_COL + (kk / 4) * 32 + (kk % 4) * 8,
+                  umma_sdesc(ka + kk * 2048, CHUNK, 1024, UMMA_SW128), idQ,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_ZFREE));
+        umma_commit(bar(B_KE(s)));
+      }
+      if (ok) umma_commit(bar(B_OF));
+      umma_commit(bar(B_DONE));
+      mbar_wait(bar(B_DONE), 0, ctl);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ compute
+    const int h = (warp - 4) >> 2;                 // key columns [64h, 64h + 64)
+    const int r = (warp & 3) * 32 + lane;          // query row (= TMEM lane)
+    const int grow = qb * BT + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    if (h == 0) {
+      // this row of Q into TMEM as 16-bit pairs (A operand of S = Q K^T); rows past N are zero
+      const uint4* src = reinterpret_cast<const uint4*>(Q) + (static_cast<size_t>(bh) * N + grow) * (HD / 8);
+      uint32_t w[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = grow < N ? __ldg(src + 8 * half + i) : make_uint4(0, 0, 0, 0);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + QT_COL + 32 * half, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_QR));
+    }
+    const float lr = Lp[static_cast<size_t>(bh) * Np + grow];   // +inf past N
+    const float dr = Dp[static_cast<size_t>(bh) * Np + grow];
+    const float lsub = lr == INFINITY ? 0.f : lr;   // padded rows: finite, never stored
+    const float2 c2 = make_float2(c_log2, c_log2), nl2 = make_float2(-lsub, -lsub);
+    const float2 nd2 = make_float2(-dr, -dr);
+    bool ok = n_iter > 0;
+    for (int j = 0; ok && j < n_iter; ++j) {
+      const int k0 = j * BT + 64 * h;
+      if (!(ok = mbar_wait(bar(B_SF), j & 1, ctl))) break;
+      tc_fence_after();
+      uint32_t x[64];
+      tmem_ld32(tmem + lane_off + S_COL + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(tmem + lane_off + S_COL + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tc_fence_before();
+      mbar_arrive(bar(B_SFREE));                   // S may now receive the next block
+      // P = exp2(S c - L log2e); on the diagonal block, zero where the key follows the query
+      float p[64];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float2 t = fma2(make_float2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])),
+                              c2, nl2);
+        p[2 * i] = ex2(t.x);
+        p[2 * i + 1] = ex2(t.y);
+      }
+      if (CAUSAL && j == qb) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (k0 + c > grow) p[c] = 0.f;
+      }
+      if (!(ok = mbar_wait(bar(B_DPF), j & 1, ctl))) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + DP_COL + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(tmem + lane_off + DP_COL + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tc_fence_before();
+      mbar_arrive(bar(B_DPFREE));                  // dP may now receive the next block
+      // dS = P o (dP - D) as 16-bit pairs into Z once the previous block's dQ MMAs read it
+      uint32_t w[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float2 ds = mul2(make_float2(p[2 * i], p[2 * i + 1]),
+                               add2(make_float2(__uint_as_float(x[2 * i]),
+                                                __uint_as_float(x[2 * i + 1])),
+                                    nd2));
+        w[i] = pack2<BF16>(ds.x, ds.y);
+      }
+      if (j > 0 && !(ok = mbar_wait(bar(B_ZFREE), (j - 1) & 1, ctl))) break;
+      tc_fence_after();
+      tmem_st32(tmem + lane_off + Z_COL + 32 * h, w);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_DSF));
+    }
+    if (ok && mbar_wait(bar(B_OF), 0, ctl)) {
+      tc_fence_after();
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      T* dst = reinterpret_cast<T*>(dQ) + (static_cast<size_t>(bh) * N + grow) * HD + 64 * h;
+      store_row64<BF16>(tmem + lane_off + DQ_COL + 64 * h, scale, dst, grow < N);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 template <bool BF16, bool CAUSAL>
 cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
   const int Np = (a.N + 127) / 128 * 128;
   const float* Lp = a.Dvec + static_cast<size_t>(a.BH) * Np;
-  auto kern = bwd128_kernel<BF16, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  const int nkb = (a.N + BN - 1) / BN;
-  const long long grid = static_cast<long long>(nkb) * a.BH;
-  trace_begin(TR_BWD_FUSED, st);
-  kern<<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, st>>>(
-      a.tmQ64, a.tmK, a.tmV, a.tmdO64, a.dQacc, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.scale,
-      a.c_log2, a.ctl);
-  trace_end(TR_BWD_FUSED, st);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const long long n8 = static_cast<long long>(a.BH) * a.N * (HD / 8);
-  trace_begin(TR_BWD_DQCVT, st);
-  dq_convert_kernel<BF16><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, st>>>(
-      a.dQacc, a.dQ, a.N, Np, n8, a.scale);
-  trace_end(TR_BWD_DQCVT, st);
-  return cudaGetLastError();
+  const long long nblk = static_cast<long long>(Np / BT) * a.BH;
+  {
+    auto kern = dkdv128_kernel<BF16, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kv::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    trace_begin(TR_BWD_DKDV, st);
+    kern<<<static_cast<unsigned>(nblk), THREADS, kv::SMEM_BYTES, st>>>(
+        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.scale, a.c_log2, a.ctl);
+    trace_end(TR_BWD_DKDV, st);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kern = dq128_kernel<BF16, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         qd::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    trace_begin(TR_BWD_DQ, st);
+    kern<<<static_cast<unsigned>(nblk), THREADS, qd::SMEM_BYTES, st>>>(
+        a.tmK, a.tmV, a.tmdO, a.Q, a.Dvec, Lp, a.dQ, a.N, Np, a.scale, a.c_log2, a.ctl);
+    trace_end(TR_BWD_DQ, st);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd128_fused(const BwdArgs& a, bool bf16, bool causal, cudaStream_t st) {
+cudaError_t launch_bwd128(const BwdArgs& a, bool bf16, bool causal, cudaStream_t st) {
   if (bf16) return causal ? launch_t<true, true>(a, st) : launch_t<true, false>(a, st);
   return causal ? launch_t<false, true>(a, st) : launch_t<false, false>(a, st);
 }

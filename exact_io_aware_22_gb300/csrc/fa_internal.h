@@ -17,9 +17,7 @@ enum TraceKind {
   TR_BWD_PRE = 1,
   TR_BWD_DKDV = 2,
   TR_BWD_DQ = 3,
-  TR_BWD_FUSED = 4,
-  TR_BWD_DQCVT = 5,
-  TR_NKINDS = 6
+  TR_NKINDS = 4
 };
 // Record an event before / after one kernel launch on `st` (no-op unless tracing).
 void trace_begin(int kind, cudaStream_t st);
@@ -45,8 +43,7 @@ cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, bool causal, cudaStre
 
 struct BwdArgs {
   CUtensorMap tmQ, tmK, tmV, tmO, tmdO;
-  CUtensorMap tmQ64, tmdO64;   // head dim 128: Q and dO in 64-row tiles
-  float* dQacc;                // head dim 128: workspace part holding the accumulator
+  const void* Q;
   const void* O;
   const void* dO;
   const float* L;
@@ -59,8 +56,8 @@ struct BwdArgs {
   KernelCtl ctl;
 };
 cudaError_t launch_bwd(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
-cudaError_t launch_bwd128_fused(const BwdArgs& a, bool bf16, bool causal, cudaStream_t st);
-// Workspace: D and L*log2(e) per padded row, plus (head dim 128) the fp32 dQ accumulator.
+cudaError_t launch_bwd128(const BwdArgs& a, bool bf16, bool causal, cudaStream_t st);
+// Workspace: D and L*log2(e) per padded row.
 size_t bwd_workspace_bytes(long long BH, int N, int d);
 
 }  // namespace fa

@@ -14,7 +14,11 @@ namespace fa {
 // Every spin-wait in the kernels is bounded.  A wait that runs out records
 // FA_DEV_TIMEOUT in the status word that the host reads back, and the kernel
 // unwinds instead of hanging.
-enum : uint32_t { FA_DEV_OK = 0u, FA_DEV_TIMEOUT = 1u };
+// A kernel that needs every byte of the 227 KiB of shared memory cannot also
+// reserve slack to realign it; it checks that the dynamic shared memory starts
+// on a 1024-byte boundary (the 128-byte swizzle atom needs it), and if not,
+// records FA_DEV_SMEM_ALIGN and returns before touching anything.
+enum : uint32_t { FA_DEV_OK = 0u, FA_DEV_TIMEOUT = 1u, FA_DEV_SMEM_ALIGN = 2u };
 
 struct KernelCtl {
   uint32_t* status;         // device status word (sticky OR of FA_DEV_* bits)
@@ -248,6 +252,34 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed fp32 pairs (Blackwell f32x2 arithmetic: two lanes per instruction,
+// each rounded exactly like the scalar operation).
+__device__ __forceinline__ uint64_t f2_bits(float2 v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 bits_f2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
 }
 
 template <bool BF16>

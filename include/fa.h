@@ -87,7 +87,9 @@ int fa_last_cuda_error(void);
 
 /* Synchronises `stream`, then reads and clears the current device's status
  * word: FA_ERR_TIMEOUT if any kernel of this library gave up a bounded wait
- * since the last read, FA_OK otherwise (FA_ERR_CUDA if the read failed). */
+ * since the last read; FA_ERR_UNSUPPORTED if a kernel found its dynamic shared
+ * memory not aligned to 1024 bytes and skipped its work (not expected on
+ * sm_103a); FA_OK otherwise (FA_ERR_CUDA if the read failed). */
 fa_status fa_device_status(void* stream);
 
 /* Bound, in nanoseconds, on any single wait inside the kernels (default 2 s).
@@ -130,11 +132,9 @@ fa_status fa_trace_read(int kind, double* total_ms, long long* launches);
  * array's device address (cudaGetSymbolAddress) with that device current; make
  * that first call before any stream capture.  All calls share the one array and
  * it keeps the last call's contents: calls that overlap on the GPU (other
- * streams, other host threads) race on it, so serialise them.  Each call
- * writes every scratch value before reading it, and clears the part that must
- * start at zero (the fp32 dQ accumulator used for head dim 128) first.
- * Capacity: 8 bytes per row for head dims 32 and 64 (B*H*ceil(N/128)*128 up to
- * 2,097,152 rows), 520 bytes per row for head dim 128 (up to 32,263 rows). */
+ * streams, other host threads) race on it, so serialise them.  Nothing in it
+ * needs to start at zero: each call writes every scratch value before reading
+ * it.  Capacity: 8 bytes per row, B*H*ceil(N/128)*128 up to 2,097,152 rows. */
 fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
                          const void* dO, const float* L, void* dQ, void* dK, void* dV, int B,
                          int H, int N, int d, int causal, float scale, fa_dtype dtype,

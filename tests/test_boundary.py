@@ -97,12 +97,11 @@ def test_bwd_rejects(lib, kw, code):
 
 def test_workspace_size(lib):
     f = lib.fa_bwd_workspace_size
-    # D and L*log2(e), fp32, padded to 128-row blocks; head dim 128 adds the fp32 dQ
-    # accumulator (one 128-float row per padded row)
+    # D and L*log2(e), fp32, padded to 128-row blocks
     assert f(1, 1, 128, 64, 0) == 2 * 128 * 4
     assert f(4, 8, 1000, 32, 1) == 2 * 32 * 1024 * 4
-    assert f(1, 32, 8192, 128, 1) == 2 * 32 * 8192 * 4 + 32 * 8192 * 128 * 4
-    assert f(2, 3, 1000, 128, 0) == 2 * 6 * 1024 * 4 + 6 * 1024 * 128 * 4
+    assert f(1, 32, 8192, 128, 1) == 2 * 32 * 8192 * 4
+    assert f(2, 3, 1000, 128, 0) == 2 * 6 * 1024 * 4
     assert f(1, 1, 1, 32, 1) == 2 * 128 * 4
     assert f(1, 1, 128, 48, 0) == 0 and f(0, 1, 128, 64, 0) == 0
 
