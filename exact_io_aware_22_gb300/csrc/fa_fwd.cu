@@ -258,27 +258,38 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < BN; ++c)
           if (kbase + c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(sr[0]);
+      // row maximum: four independent chains of 3-input max
+      float mc[4];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      for (int q = 0; q < 4; ++q) {
+        mc[q] = __uint_as_float(sr[32 * q]);
+#pragma unroll
+        for (int c = 1; c + 1 < 32; c += 2)
+          mc[q] = fmax3(mc[q], __uint_as_float(sr[32 * q + c]), __uint_as_float(sr[32 * q + c + 1]));
+        mc[q] = fmaxf(mc[q], __uint_as_float(sr[32 * q + 31]));
+      }
+      const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
       const float m_tile = mx * c_log2;
       const bool grow_m = m_tile > m_run + RESCALE_LOG2;
       const float m_use = grow_m ? m_tile : m_run;
       const float alpha = grow_m ? ex2(m_run - m_use) : 1.f;
       const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
-      float rs = 0.f;
+      const float2 c2 = make_float2(c_log2, c_log2), nm2 = make_float2(-m_sub, -m_sub);
+      float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[32 * h + 2 * i]), c_log2, -m_sub));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[32 * h + 2 * i + 1]), c_log2, -m_sub));
-          rs += p0 + p1;
-          pk[i] = pack2<BF16>(p0, p1);
+          const int c = 32 * h + 2 * i;
+          const float2 t = fma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nm2);
+          const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+          rs2[i & 1] = add2(rs2[i & 1], pp);
+          pk[i] = pack2<BF16>(pp.x, pp.y);
         }
         tmem_st16(tS + 16 * h, pk);
       }
+      const float rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
       l_run = l_run * alpha + rs;
       if (j > 0 && __any_sync(0xffffffffu, grow_m)) {
         // O holds sum over tiles < j; PV(j-1) has completed because S(j) was
@@ -288,8 +299,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint32_t o[32];
           tmem_ld32(tO + 32 * cc, o);
           tmem_ld_wait_regs(o);
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < 16; ++i) {
+            const float2 v = mul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
+            o[2 * i] = __float_as_uint(v.x);
+            o[2 * i + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(tO + 32 * cc, o);
         }
       }
