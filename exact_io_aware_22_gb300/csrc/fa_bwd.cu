@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = n_iter > 0;
     for (int it = 0; ok && it < n_iter; ++it) {
       const int qb = i0 + it;
-      if (!(ok = mbar_wait(bar(B_SF), it & 1, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(B_SF), it & 1, ctl))) break;
       tc_fence_after();
       uint32_t s[64], dp[64];
       tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B_PF));
     }
-    if (ok && mbar_wait(bar(B_OF), 0, ctl)) {
+    if (ok && mbar_wait_warp(bar(B_OF), 0, ctl)) {
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       const bool valid = gkey < N;
@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float lsub = lr == INFINITY ? 0.f : lr;
     bool ok = n_iter > 0;
     for (int it = 0; ok && it < n_iter; ++it) {
-      if (!(ok = mbar_wait(bar(B_SF), it & 1, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(B_SF), it & 1, ctl))) break;
       tc_fence_after();
       uint32_t s[64], dp[64];
       tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B_PF));
     }
-    if (ok && mbar_wait(bar(B_OF), 0, ctl)) {
+    if (ok && mbar_wait_warp(bar(B_OF), 0, ctl)) {
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       constexpr int HALF = D / 2;

@@ -13,13 +13,14 @@
 //
 //   dkdv_kernel  key-stationary: one CTA per 128-key block, K and V in shared
 //                memory, loop over 128-query tiles (causal: from the diagonal
-//                down).  TMEM: dV | dK | R | X, 128 columns each.  R holds
-//                S^T = K Q^T, then dP^T = V dO^T once the compute warps hold
-//                S^T in registers, then the next tile's S^T once they hold dP^T.
-//                X holds P^T as 16-bit pairs in two 64-column buffers (A operand
-//                of dV += P^T dO); dS^T goes to shared memory (A operand of
-//                dK += dS^T Q).  Pipe order per tile i: dP^T(i), S^T(i+1),
-//                dV(i), dK(i).
+//                down).  TMEM: dV | dK | S^T | dP^T, 128 columns each.  Each
+//                compute thread writes P^T as 16-bit pairs back over the dP^T
+//                columns it has read (A operand of dV += P^T dO); dS^T goes to
+//                shared memory (A operand of dK += dS^T Q).  The next S^T is
+//                issued as soon as the compute warps hold this one, so it runs
+//                during the P^T work; the next dP^T follows the dV MMAs that
+//                read P^T, and its completion also frees dS^T.  Pipe order per
+//                tile i: S^T(i+1), dV(i), dK(i), dP^T(i+1).
 //   dq_kernel    query-stationary: one CTA per 128-query tile, loop over 128-key
 //                blocks (causal: up to the diagonal).  Each compute thread of the
 //                first warpgroup copies its row of Q into TMEM once, so S = Q K^T
@@ -106,12 +107,13 @@ constexpr int DO_OFF = Q_OFF + STAGES * TILE;
 constexpr int DS_OFF = DO_OFF + STAGES * TILE;  // dS^T: 128 keys x 128 queries, two chunks
 constexpr int LD_OFF = DS_OFF + TILE;           // per stage: 128 L*log2e, then 128 D
 constexpr int BAR_OFF = LD_OFF + STAGES * 1024;
-// kv_full, q_full[S], q_empty[S], s_full, s_free, dp_full, dp_free, p_full[2], ds_free, o_full, done
-constexpr int NBARS = 1 + 2 * STAGES + 9;
+// kv_full, q_full[S], q_empty[S], s_full, s_free, dp_full, p_full, o_full, done
+constexpr int NBARS = 1 + 2 * STAGES + 6;
 constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
 constexpr int SMEM_BYTES = SLOT_OFF + 16;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
-constexpr uint32_t DV_COL = 0, DK_COL = 128, R_COL = 256, X_COL = 384;
+// dV | dK | S^T | dP^T (then P^T as 16-bit pairs over the columns each thread has read)
+constexpr uint32_t DV_COL = 0, DK_COL = 128, S_COL = 256, DP_COL = 384;
 }  // namespace kv
 
 template <bool BF16, bool CAUSAL>
@@ -140,16 +142,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int B_KV = 0;
   auto B_QF = [&](int s) { return 1 + s; };
   auto B_QE = [&](int s) { return 1 + STAGES + s; };
-  const int B_SF = 1 + 2 * STAGES, B_SFREE = B_SF + 1, B_DPF = B_SF + 2, B_DPFREE = B_SF + 3;
-  auto B_PF = [&](int b) { return B_SF + 4 + b; };   // per P^T buffer: two phases never overlap
-  const int B_DSFREE = B_SF + 6, B_OF = B_SF + 7, B_DONE = B_SF + 8;
+  const int B_SF = 1 + 2 * STAGES, B_SFREE = B_SF + 1, B_DPF = B_SF + 2, B_PF = B_SF + 3,
+            B_OF = B_SF + 4, B_DONE = B_SF + 5;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBARS; ++i) mbar_init(bar(i), 1);
     mbar_init(bar(B_SFREE), 256);
-    mbar_init(bar(B_DPFREE), 256);
-    mbar_init(bar(B_PF(0)), 256);
-    mbar_init(bar(B_PF(1)), 256);
+    mbar_init(bar(B_PF), 256);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -200,32 +199,30 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = mbar_wait(bar(B_KV), 0, ctl) && mbar_wait(bar(B_QF(0)), 0, ctl);
       if (ok) {
         tc_fence_after();
-        issue_ab_t(tmem + R_COL, sb + K_OFF, sb + Q_OFF, idS);
+        issue_ab_t(tmem + S_COL, sb + K_OFF, sb + Q_OFF, idS);
         umma_commit(bar(B_SF));
+        issue_ab_t(tmem + DP_COL, sb + V_OFF, sb + DO_OFF, idS);
+        umma_commit(bar(B_DPF));
       }
       for (int it = 0; ok && it < n_iter; ++it) {
-        const int s = it % STAGES, b = it & 1;
+        const int s = it % STAGES;
+        const int s1 = (it + 1) % STAGES;
+        const bool next = it + 1 < n_iter;
         const uint32_t qa = sb + Q_OFF + s * TILE, da = sb + DO_OFF + s * TILE;
-        // dP^T into R once the compute warps hold S^T
-        if (!(ok = mbar_wait(bar(B_SFREE), it & 1, ctl))) break;
-        tc_fence_after();
-        issue_ab_t(tmem + R_COL, sb + V_OFF, da, idS);
-        umma_commit(bar(B_DPF));
-        // the next S^T into R once they hold dP^T
-        if (!(ok = mbar_wait(bar(B_DPFREE), it & 1, ctl))) break;
-        if (it + 1 < n_iter) {
-          const int s1 = (it + 1) % STAGES;
+        if (next) {
+          // the next S^T as soon as the compute warps hold this one
           if (!(ok = mbar_wait(bar(B_QF(s1)), ((it + 1) / STAGES) & 1, ctl))) break;
+          if (!(ok = mbar_wait(bar(B_SFREE), it & 1, ctl))) break;
           tc_fence_after();
-          issue_ab_t(tmem + R_COL, sb + K_OFF, sb + Q_OFF + s1 * TILE, idS);
+          issue_ab_t(tmem + S_COL, sb + K_OFF, sb + Q_OFF + s1 * TILE, idS);
           umma_commit(bar(B_SF));
         }
-        // P^T(i) is in X buffer b and dS^T(i) in shared memory
-        if (!(ok = mbar_wait(bar(B_PF(b)), (it >> 1) & 1, ctl))) break;
+        // P^T (over dP^T's columns) and dS^T (shared memory) are ready
+        if (!(ok = mbar_wait(bar(B_PF), it & 1, ctl))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)       // dV += P^T dO
-          umma_ts(tmem + DV_COL, tmem + X_COL + 64 * b + (kk / 4) * 32 + (kk % 4) * 8,
+          umma_ts(tmem + DV_COL, tmem + DP_COL + (kk / 4) * 64 + (kk % 4) * 8,
                   umma_sdesc(da + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
                   (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
@@ -234,8 +231,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                   umma_sdesc(sb + DS_OFF + (kk / 4) * CHUNK + (kk % 4) * 32, 16, 1024, UMMA_SW128),
                   umma_sdesc(qa + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
                   (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_DSFREE));
         umma_commit(bar(B_QE(s)));
+        if (next) {
+          // the next dP^T over the P^T columns: issued after the dV MMAs that read them.
+          // Its completion also tells the compute warps that dK has read dS^T.
+          issue_ab_t(tmem + DP_COL, sb + V_OFF, sb + DO_OFF + s1 * TILE, idS);
+          umma_commit(bar(B_DPF));
+        }
       }
       if (ok) umma_commit(bar(B_OF));
       umma_commit(bar(B_DONE));
@@ -248,24 +250,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int kr = (warp & 3) * 32 + lane;         // key row (= TMEM lane)
     const int gkey = kb * BT + kr;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tR = tmem + lane_off + R_COL + 64 * h;
+    const uint32_t tS = tmem + lane_off + S_COL + 64 * h;
+    const uint32_t tP = tmem + lane_off + DP_COL + 64 * h;
     uint8_t* ds_row = sg + DS_OFF + h * CHUNK + kr * 128;
     const float2 c2 = make_float2(c_log2, c_log2);
     bool ok = n_iter > 0;
     for (int it = 0; ok && it < n_iter; ++it) {
-      const int s = it % STAGES, b = it & 1;
+      const int s = it % STAGES;
       const int q0 = (q_start + it) * BT + 64 * h;  // first query of this thread's columns
-      const bool diag = CAUSAL && it == 0;
-      if (!(ok = mbar_wait(bar(B_SF), it & 1, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(B_SF), it & 1, ctl))) break;
       tc_fence_after();
       uint32_t x[64];
-      tmem_ld32(tR, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-      tmem_ld32(tR + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
       tc_fence_before();
-      mbar_arrive(bar(B_SFREE));                   // R may now receive dP^T
-      if (!(ok = mbar_wait(bar(B_QF(s)), (it / STAGES) & 1, ctl))) break;
+      mbar_arrive(bar(B_SFREE));                   // S^T may now receive the next tile
+      if (!(ok = mbar_wait_warp(bar(B_QF(s)), (it / STAGES) & 1, ctl))) break;
       const float* Ls = reinterpret_cast<const float*>(sg + LD_OFF + s * 1024) + 64 * h;
       const float* Ds = Ls + 128;
       // P^T = exp2(S^T c - L log2e); on the diagonal tile, zero where the query precedes
@@ -283,25 +285,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         p[4 * c4 + 2] = ex2(t1.x);
         p[4 * c4 + 3] = ex2(t1.y);
       }
-      if (diag) {
+      if (CAUSAL && it == 0) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (q0 + c < gkey) p[c] = 0.f;
       }
-      if (!(ok = mbar_wait(bar(B_DPF), it & 1, ctl))) break;
+      // dP^T of this tile; it also means the dK MMAs of the previous tile are done with
+      // dS^T in shared memory
+      if (!(ok = mbar_wait_warp(bar(B_DPF), it & 1, ctl))) break;
       tc_fence_after();
-      tmem_ld32(tR, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-      tmem_ld32(tR + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_ld32(tP, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-      tc_fence_before();
-      mbar_arrive(bar(B_DPFREE));                  // R may now receive the next S^T
-      // the dK MMAs of the previous tile have finished reading dS^T
-      if (it > 0 && !(ok = mbar_wait(bar(B_DSFREE), (it - 1) & 1, ctl))) break;
       // dS^T = P^T o (dP^T - D) to shared memory (128-byte swizzle: chunk u of row kr at
-      // u ^ (kr & 7)); P^T as 16-bit pairs into X buffer b (its last reader, dV two tiles
-      // back, finished before the dK MMAs waited on above)
-      uint32_t pw[32];
+      // u ^ (kr & 7))
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const float4 da = *reinterpret_cast<const float4*>(Ds + 8 * u);
@@ -315,18 +313,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                                  add2(make_float2(__uint_as_float(x[c]), __uint_as_float(x[c + 1])),
                                       make_float2(-dq[2 * e], -dq[2 * e + 1])));
           dw[e] = pack2<BF16>(ds.x, ds.y);
-          pw[4 * u + e] = pack2<BF16>(p[c], p[c + 1]);
         }
         *reinterpret_cast<uint4*>(ds_row + ((u ^ (kr & 7)) << 4)) =
             make_uint4(dw[0], dw[1], dw[2], dw[3]);
       }
-      tmem_st32(tmem + lane_off + X_COL + 64 * b + 32 * h, pw);
+      {
+        // P^T as 16-bit pairs over the dP^T columns just read (A operand of dV)
+        uint32_t pw[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pw[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
+        tmem_st32(tP, pw);
+      }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(B_PF(b)));
+      mbar_arrive(bar(B_PF));
     }
-    if (ok && mbar_wait(bar(B_OF), 0, ctl)) {
+    if (ok && mbar_wait_warp(bar(B_OF), 0, ctl)) {
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       const bool valid = gkey < N;
@@ -522,7 +525,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = n_iter > 0;
     for (int j = 0; ok && j < n_iter; ++j) {
       const int k0 = j * BT + 64 * h;
-      if (!(ok = mbar_wait(bar(B_SF), j & 1, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(B_SF), j & 1, ctl))) break;
       tc_fence_after();
       uint32_t x[64];
       tmem_ld32(tmem + lane_off + S_COL + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
@@ -545,7 +548,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < 64; ++c)
           if (k0 + c > grow) p[c] = 0.f;
       }
-      if (!(ok = mbar_wait(bar(B_DPF), j & 1, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(B_DPF), j & 1, ctl))) break;
       tc_fence_after();
       tmem_ld32(tmem + lane_off + DP_COL + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
       tmem_ld32(tmem + lane_off + DP_COL + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
@@ -563,14 +566,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                                     nd2));
         w[i] = pack2<BF16>(ds.x, ds.y);
       }
-      if (j > 0 && !(ok = mbar_wait(bar(B_ZFREE), (j - 1) & 1, ctl))) break;
+      if (j > 0 && !(ok = mbar_wait_warp(bar(B_ZFREE), (j - 1) & 1, ctl))) break;
       tc_fence_after();
       tmem_st32(tmem + lane_off + Z_COL + 32 * h, w);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_DSF));
     }
-    if (ok && mbar_wait(bar(B_OF), 0, ctl)) {
+    if (ok && mbar_wait_warp(bar(B_OF), 0, ctl)) {
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       T* dst = reinterpret_cast<T*>(dQ) + (static_cast<size_t>(bh) * N + grow) * HD + 64 * h;

@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      if (!(ok = mbar_wait(bar(B_SF(t)), j & 1, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(B_SF(t)), j & 1, ctl))) break;
       tc_fence_after();
       uint32_t sr[BN];
       tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B_PF(t)));
     }
-    if (ok && nt > 0 && mbar_wait(bar(B_OF(t)), 0, ctl)) {
+    if (ok && nt > 0 && mbar_wait_warp(bar(B_OF(t)), 0, ctl)) {
       tc_fence_after();
       const float inv_l = 1.f / l_run;
       const bool valid = grow < N;

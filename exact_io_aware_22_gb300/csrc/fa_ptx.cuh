@@ -76,6 +76,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const K
   }
 }
 
+// mbar_wait for code in which every lane of the warp waits and then issues
+// warp-wide (.sync.aligned) instructions: the result is the same on all lanes, so
+// a lane whose bound ran out never leaves its warp-mates in an aligned
+// instruction without it.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const KernelCtl& ctl) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl));
+}
+
 // Named barrier among a subset of warps (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
