@@ -20,7 +20,9 @@
 //                issued as soon as the compute warps hold this one, so it runs
 //                during the P^T work; the next dP^T follows the dV MMAs that
 //                read P^T, and its completion also frees dS^T.  Pipe order per
-//                tile i: S^T(i+1), dV(i), dK(i), dP^T(i+1).
+//                tile i: S^T(i+1), dK(i), dV(i), dP^T(i+1).  Q and dO sit in
+//                separate two-stage rings, so the next-but-one Q tile starts
+//                loading as soon as dK(i) has read this one.
 //   dq_kernel    query-stationary: one CTA per 128-query tile, loop over 128-key
 //                blocks (causal: up to the diagonal).  Each compute thread of the
 //                first warpgroup copies its row of Q into TMEM once, so S = Q K^T
@@ -107,8 +109,9 @@ constexpr int DO_OFF = Q_OFF + STAGES * TILE;
 constexpr int DS_OFF = DO_OFF + STAGES * TILE;  // dS^T: 128 keys x 128 queries, two chunks
 constexpr int LD_OFF = DS_OFF + TILE;           // per stage: 128 L*log2e, then 128 D
 constexpr int BAR_OFF = LD_OFF + STAGES * 1024;
-// kv_full, q_full[S], q_empty[S], s_full, s_free, dp_full, p_full, o_full, done
-constexpr int NBARS = 1 + 2 * STAGES + 6;
+// kv_full, q_full[S], q_empty[S], do_full[S], do_empty[S], s_full, s_free, dp_full, p_full,
+// out_full, done
+constexpr int NBARS = 1 + 4 * STAGES + 6;
 constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
 constexpr int SMEM_BYTES = SLOT_OFF + 16;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
@@ -142,7 +145,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int B_KV = 0;
   auto B_QF = [&](int s) { return 1 + s; };
   auto B_QE = [&](int s) { return 1 + STAGES + s; };
-  const int B_SF = 1 + 2 * STAGES, B_SFREE = B_SF + 1, B_DPF = B_SF + 2, B_PF = B_SF + 3,
+  auto B_GF = [&](int s) { return 1 + 2 * STAGES + s; };   // dO and D of a stage
+  auto B_GE = [&](int s) { return 1 + 3 * STAGES + s; };
+  const int B_SF = 1 + 4 * STAGES, B_SFREE = B_SF + 1, B_DPF = B_SF + 2, B_PF = B_SF + 3,
             B_OF = B_SF + 4, B_DONE = B_SF + 5;
 
   if (threadIdx.x == 0) {
@@ -169,25 +174,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_3d(sb + V_OFF + c * CHUNK, &tmV, bar(B_KV), c * 64, kb * BT, bh);
       }
       bool ok = true;
-      int it = 0;
-      for (; it < n_iter; ++it) {
+      // Q with L*log2e, and dO with D, of each query tile in separate stages: the next
+      // S^T needs only Q, whose stage the dK MMAs free before the dV MMAs free dO's.
+      // (L and D: padded per-row arrays, 512-byte aligned per tile.)
+      int nq_issued = 0, ng_issued = 0;
+      for (; ok && ng_issued < n_iter;) {
+        const int it = ng_issued;
         const int s = it % STAGES;
-        if (!(ok = mbar_wait(bar(B_QE(s)), ((it / STAGES) & 1) ^ 1, ctl))) break;
         const int qrow = (q_start + it) * BT;
-        mbar_arrive_expect_tx(bar(B_QF(s)), 2 * TILE + 1024);
-        for (int c = 0; c < 2; ++c) {
-          tma_load_3d(sb + Q_OFF + s * TILE + c * CHUNK, &tmQ, bar(B_QF(s)), c * 64, qrow, bh);
-          tma_load_3d(sb + DO_OFF + s * TILE + c * CHUNK, &tmdO, bar(B_QF(s)), c * 64, qrow, bh);
-        }
-        // L*log2e and D of the 128 queries (padded per-row arrays, 512-byte aligned rows)
         const size_t row = static_cast<size_t>(bh) * Np + qrow;
+        if (!(ok = mbar_wait(bar(B_QE(s)), ((it / STAGES) & 1) ^ 1, ctl))) break;
+        mbar_arrive_expect_tx(bar(B_QF(s)), TILE + 512);
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sb + Q_OFF + s * TILE + c * CHUNK, &tmQ, bar(B_QF(s)), c * 64, qrow, bh);
         bulk_load(sb + LD_OFF + s * 1024, Lp + row, 512, bar(B_QF(s)));
-        bulk_load(sb + LD_OFF + s * 1024 + 512, Dp + row, 512, bar(B_QF(s)));
+        ++nq_issued;
+        if (!(ok = mbar_wait(bar(B_GE(s)), ((it / STAGES) & 1) ^ 1, ctl))) break;
+        mbar_arrive_expect_tx(bar(B_GF(s)), TILE + 512);
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sb + DO_OFF + s * TILE + c * CHUNK, &tmdO, bar(B_GF(s)), c * 64, qrow, bh);
+        bulk_load(sb + LD_OFF + s * 1024 + 512, Dp + row, 512, bar(B_GF(s)));
+        ++ng_issued;
       }
       if (!ok) {
         mbar_wait(bar(B_KV), 0, ctl);
-        for (int jj = max(0, it - STAGES); jj < it; ++jj)
+        for (int jj = max(0, nq_issued - STAGES); jj < nq_issued; ++jj)
           mbar_wait(bar(B_QF(jj % STAGES)), (jj / STAGES) & 1, ctl);
+        for (int jj = max(0, ng_issued - STAGES); jj < ng_issued; ++jj)
+          mbar_wait(bar(B_GF(jj % STAGES)), (jj / STAGES) & 1, ctl);
       }
     }
     __syncwarp();
@@ -201,8 +215,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         issue_ab_t(tmem + S_COL, sb + K_OFF, sb + Q_OFF, idS);
         umma_commit(bar(B_SF));
-        issue_ab_t(tmem + DP_COL, sb + V_OFF, sb + DO_OFF, idS);
-        umma_commit(bar(B_DPF));
+        if ((ok = mbar_wait(bar(B_GF(0)), 0, ctl))) {
+          tc_fence_after();
+          issue_ab_t(tmem + DP_COL, sb + V_OFF, sb + DO_OFF, idS);
+          umma_commit(bar(B_DPF));
+        }
       }
       for (int it = 0; ok && it < n_iter; ++it) {
         const int s = it % STAGES;
@@ -221,20 +238,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!(ok = mbar_wait(bar(B_PF), it & 1, ctl))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)       // dV += P^T dO
-          umma_ts(tmem + DV_COL, tmem + DP_COL + (kk / 4) * 64 + (kk % 4) * 8,
-                  umma_sdesc(da + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
-                  (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)       // dK += dS^T Q
           umma_ss(tmem + DK_COL,
                   umma_sdesc(sb + DS_OFF + (kk / 4) * CHUNK + (kk % 4) * 32, 16, 1024, UMMA_SW128),
                   umma_sdesc(qa + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
                   (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(B_QE(s)));
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)       // dV += P^T dO
+          umma_ts(tmem + DV_COL, tmem + DP_COL + (kk / 4) * 64 + (kk % 4) * 8,
+                  umma_sdesc(da + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_GE(s)));
         if (next) {
           // the next dP^T over the P^T columns: issued after the dV MMAs that read them.
           // Its completion also tells the compute warps that dK has read dS^T.
+          if (!(ok = mbar_wait(bar(B_GF(s1)), ((it + 1) / STAGES) & 1, ctl))) break;
+          tc_fence_after();
           issue_ab_t(tmem + DP_COL, sb + V_OFF, sb + DO_OFF + s1 * TILE, idS);
           umma_commit(bar(B_DPF));
         }
@@ -293,6 +313,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // dP^T of this tile; it also means the dK MMAs of the previous tile are done with
       // dS^T in shared memory
       if (!(ok = mbar_wait_warp(bar(B_DPF), it & 1, ctl))) break;
+      // D came with dO, which the dP^T MMAs just waited on
+      if (!(ok = mbar_wait_warp(bar(B_GF(s)), (it / STAGES) & 1, ctl))) break;
       tc_fence_after();
       tmem_ld32(tP, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
       tmem_ld32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
