@@ -13,16 +13,15 @@
 //
 //   dkdv_kernel  key-stationary: one CTA per 128-key block, K and V in shared
 //                memory, loop over 128-query tiles (causal: from the diagonal
-//                down).  TMEM: dV | dK | S^T | dP^T, 128 columns each.  Each
-//                compute thread writes P^T as 16-bit pairs back over the dP^T
-//                columns it has read (A operand of dV += P^T dO); dS^T goes to
-//                shared memory (A operand of dK += dS^T Q).  The next S^T is
-//                issued as soon as the compute warps hold this one, so it runs
-//                during the P^T work; the next dP^T follows the dV MMAs that
-//                read P^T, and its completion also frees dS^T.  Pipe order per
-//                tile i: S^T(i+1), dK(i), dV(i), dP^T(i+1).  Q and dO sit in
-//                separate two-stage rings, so the next-but-one Q tile starts
-//                loading as soon as dK(i) has read this one.
+//                down).  TMEM: dV | dK | S^T | dP^T, 128 columns each.  Once a
+//                compute thread holds its 64 dP^T values it writes P^T and then
+//                dS^T as 16-bit pairs over those columns, 32 each: the A
+//                operands of dV += P^T dO and dK += dS^T Q, so no score tile
+//                passes through shared memory, which holds a three-stage Q ring
+//                and a two-stage dO ring instead.  The next S^T is issued as soon
+//                as the compute warps hold this one; dV starts once P^T is
+//                stored, before dS^T is.  Pipe order per tile i: S^T(i+1), dV(i),
+//                dK(i), dP^T(i+1).
 //   dq_kernel    query-stationary: one CTA per 128-query tile, loop over 128-key
 //                blocks (causal: up to the diagonal).  Each compute thread of the
 //                first warpgroup copies its row of Q into TMEM once, so S = Q K^T
@@ -104,18 +103,20 @@ __device__ __forceinline__ void store_row64(uint32_t taddr, float mul, void* dst
 
 // ============================================================== dK / dV
 namespace kv {
+constexpr int Q_STAGES = 3, DO_STAGES = 2;
 constexpr int K_OFF = 0, V_OFF = TILE, Q_OFF = 2 * TILE;
-constexpr int DO_OFF = Q_OFF + STAGES * TILE;
-constexpr int DS_OFF = DO_OFF + STAGES * TILE;  // dS^T: 128 keys x 128 queries, two chunks
-constexpr int LD_OFF = DS_OFF + TILE;           // per stage: 128 L*log2e, then 128 D
-constexpr int BAR_OFF = LD_OFF + STAGES * 1024;
-// kv_full, q_full[S], q_empty[S], do_full[S], do_empty[S], s_full, s_free, dp_full, p_full,
-// out_full, done
-constexpr int NBARS = 1 + 4 * STAGES + 6;
+constexpr int DO_OFF = Q_OFF + Q_STAGES * TILE;
+constexpr int L_OFF = DO_OFF + DO_STAGES * TILE;   // per Q stage: 128 L*log2e
+constexpr int D_OFF = L_OFF + Q_STAGES * 512;      // per dO stage: 128 D
+constexpr int BAR_OFF = D_OFF + DO_STAGES * 512;
+// kv_full, q_full[3], q_empty[3], do_full[2], do_empty[2], s_full, s_free, dp_full, p_ready,
+// ds_ready, out_full, done
+constexpr int NBARS = 1 + 2 * Q_STAGES + 2 * DO_STAGES + 7;
 constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
 constexpr int SMEM_BYTES = SLOT_OFF + 16;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
-// dV | dK | S^T | dP^T (then P^T as 16-bit pairs over the columns each thread has read)
+// dV | dK | S^T | dP^T.  Once a compute thread holds its 64 dP^T values it writes
+// P^T (16-bit pairs) over the first 32 of those columns and dS^T over the last 32.
 constexpr uint32_t DV_COL = 0, DK_COL = 128, S_COL = 256, DP_COL = 384;
 }  // namespace kv
 
@@ -144,16 +145,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
   const int B_KV = 0;
   auto B_QF = [&](int s) { return 1 + s; };
-  auto B_QE = [&](int s) { return 1 + STAGES + s; };
-  auto B_GF = [&](int s) { return 1 + 2 * STAGES + s; };   // dO and D of a stage
-  auto B_GE = [&](int s) { return 1 + 3 * STAGES + s; };
-  const int B_SF = 1 + 4 * STAGES, B_SFREE = B_SF + 1, B_DPF = B_SF + 2, B_PF = B_SF + 3,
-            B_OF = B_SF + 4, B_DONE = B_SF + 5;
+  auto B_QE = [&](int s) { return 1 + Q_STAGES + s; };
+  auto B_GF = [&](int g) { return 1 + 2 * Q_STAGES + g; };   // dO and D of a stage
+  auto B_GE = [&](int g) { return 1 + 2 * Q_STAGES + DO_STAGES + g; };
+  const int B_SF = 1 + 2 * Q_STAGES + 2 * DO_STAGES, B_SFREE = B_SF + 1, B_DPF = B_SF + 2,
+            B_PR = B_SF + 3, B_DR = B_SF + 4, B_OF = B_SF + 5, B_DONE = B_SF + 6;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBARS; ++i) mbar_init(bar(i), 1);
     mbar_init(bar(B_SFREE), 256);
-    mbar_init(bar(B_PF), 256);
+    mbar_init(bar(B_PR), 256);
+    mbar_init(bar(B_DR), 256);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -173,35 +175,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_3d(sb + K_OFF + c * CHUNK, &tmK, bar(B_KV), c * 64, kb * BT, bh);
         tma_load_3d(sb + V_OFF + c * CHUNK, &tmV, bar(B_KV), c * 64, kb * BT, bh);
       }
+      // Q with L*log2e in a three-stage ring, dO with D in a two-stage ring (L and D:
+      // padded per-row arrays, 512-byte aligned per tile).  Both stages of a tile are
+      // freed by its dK MMAs, the last reader of either.
       bool ok = true;
-      // Q with L*log2e, and dO with D, of each query tile in separate stages: the next
-      // S^T needs only Q, whose stage the dK MMAs free before the dV MMAs free dO's.
-      // (L and D: padded per-row arrays, 512-byte aligned per tile.)
       int nq_issued = 0, ng_issued = 0;
-      for (; ok && ng_issued < n_iter;) {
-        const int it = ng_issued;
-        const int s = it % STAGES;
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int s = it % Q_STAGES, g = it % DO_STAGES;
         const int qrow = (q_start + it) * BT;
         const size_t row = static_cast<size_t>(bh) * Np + qrow;
-        if (!(ok = mbar_wait(bar(B_QE(s)), ((it / STAGES) & 1) ^ 1, ctl))) break;
+        if (!(ok = mbar_wait(bar(B_QE(s)), ((it / Q_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_QF(s)), TILE + 512);
         for (int c = 0; c < 2; ++c)
           tma_load_3d(sb + Q_OFF + s * TILE + c * CHUNK, &tmQ, bar(B_QF(s)), c * 64, qrow, bh);
-        bulk_load(sb + LD_OFF + s * 1024, Lp + row, 512, bar(B_QF(s)));
+        bulk_load(sb + L_OFF + s * 512, Lp + row, 512, bar(B_QF(s)));
         ++nq_issued;
-        if (!(ok = mbar_wait(bar(B_GE(s)), ((it / STAGES) & 1) ^ 1, ctl))) break;
-        mbar_arrive_expect_tx(bar(B_GF(s)), TILE + 512);
+        if (!(ok = mbar_wait(bar(B_GE(g)), ((it / DO_STAGES) & 1) ^ 1, ctl))) break;
+        mbar_arrive_expect_tx(bar(B_GF(g)), TILE + 512);
         for (int c = 0; c < 2; ++c)
-          tma_load_3d(sb + DO_OFF + s * TILE + c * CHUNK, &tmdO, bar(B_GF(s)), c * 64, qrow, bh);
-        bulk_load(sb + LD_OFF + s * 1024 + 512, Dp + row, 512, bar(B_GF(s)));
+          tma_load_3d(sb + DO_OFF + g * TILE + c * CHUNK, &tmdO, bar(B_GF(g)), c * 64, qrow, bh);
+        bulk_load(sb + D_OFF + g * 512, Dp + row, 512, bar(B_GF(g)));
         ++ng_issued;
       }
       if (!ok) {
         mbar_wait(bar(B_KV), 0, ctl);
-        for (int jj = max(0, nq_issued - STAGES); jj < nq_issued; ++jj)
-          mbar_wait(bar(B_QF(jj % STAGES)), (jj / STAGES) & 1, ctl);
-        for (int jj = max(0, ng_issued - STAGES); jj < ng_issued; ++jj)
-          mbar_wait(bar(B_GF(jj % STAGES)), (jj / STAGES) & 1, ctl);
+        for (int jj = max(0, nq_issued - Q_STAGES); jj < nq_issued; ++jj)
+          mbar_wait(bar(B_QF(jj % Q_STAGES)), (jj / Q_STAGES) & 1, ctl);
+        for (int jj = max(0, ng_issued - DO_STAGES); jj < ng_issued; ++jj)
+          mbar_wait(bar(B_GF(jj % DO_STAGES)), (jj / DO_STAGES) & 1, ctl);
       }
     }
     __syncwarp();
@@ -222,40 +223,43 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       for (int it = 0; ok && it < n_iter; ++it) {
-        const int s = it % STAGES;
-        const int s1 = (it + 1) % STAGES;
+        const int s = it % Q_STAGES, g = it % DO_STAGES;
         const bool next = it + 1 < n_iter;
-        const uint32_t qa = sb + Q_OFF + s * TILE, da = sb + DO_OFF + s * TILE;
         if (next) {
           // the next S^T as soon as the compute warps hold this one
-          if (!(ok = mbar_wait(bar(B_QF(s1)), ((it + 1) / STAGES) & 1, ctl))) break;
+          const int s1 = (it + 1) % Q_STAGES;
+          if (!(ok = mbar_wait(bar(B_QF(s1)), ((it + 1) / Q_STAGES) & 1, ctl))) break;
           if (!(ok = mbar_wait(bar(B_SFREE), it & 1, ctl))) break;
           tc_fence_after();
           issue_ab_t(tmem + S_COL, sb + K_OFF, sb + Q_OFF + s1 * TILE, idS);
           umma_commit(bar(B_SF));
         }
-        // P^T (over dP^T's columns) and dS^T (shared memory) are ready
-        if (!(ok = mbar_wait(bar(B_PF), it & 1, ctl))) break;
+        // dV += P^T dO, P^T from the first half of each warpgroup's dP^T columns
+        if (!(ok = mbar_wait(bar(B_PR), it & 1, ctl))) break;
         tc_fence_after();
+        const uint32_t da = sb + DO_OFF + g * TILE;
 #pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)       // dK += dS^T Q
-          umma_ss(tmem + DK_COL,
-                  umma_sdesc(sb + DS_OFF + (kk / 4) * CHUNK + (kk % 4) * 32, 16, 1024, UMMA_SW128),
-                  umma_sdesc(qa + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
-                  (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_QE(s)));
-#pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)       // dV += P^T dO
+        for (int kk = 0; kk < BT / 16; ++kk)
           umma_ts(tmem + DV_COL, tmem + DP_COL + (kk / 4) * 64 + (kk % 4) * 8,
                   umma_sdesc(da + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
                   (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_GE(s)));
+        // dK += dS^T Q, dS^T from the second half
+        if (!(ok = mbar_wait(bar(B_DR), it & 1, ctl))) break;
+        tc_fence_after();
+        const uint32_t qa = sb + Q_OFF + s * TILE;
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)
+          umma_ts(tmem + DK_COL, tmem + DP_COL + (kk / 4) * 64 + 32 + (kk % 4) * 8,
+                  umma_sdesc(qa + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_QE(s)));
+        umma_commit(bar(B_GE(g)));
         if (next) {
-          // the next dP^T over the P^T columns: issued after the dV MMAs that read them.
-          // Its completion also tells the compute warps that dK has read dS^T.
-          if (!(ok = mbar_wait(bar(B_GF(s1)), ((it + 1) / STAGES) & 1, ctl))) break;
+          // the next dP^T over P^T and dS^T: issued after the MMAs that read them
+          const int g1 = (it + 1) % DO_STAGES;
+          if (!(ok = mbar_wait(bar(B_GF(g1)), ((it + 1) / DO_STAGES) & 1, ctl))) break;
           tc_fence_after();
-          issue_ab_t(tmem + DP_COL, sb + V_OFF, sb + DO_OFF + s1 * TILE, idS);
+          issue_ab_t(tmem + DP_COL, sb + V_OFF, sb + DO_OFF + g1 * TILE, idS);
           umma_commit(bar(B_DPF));
         }
       }
@@ -272,11 +276,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + S_COL + 64 * h;
     const uint32_t tP = tmem + lane_off + DP_COL + 64 * h;
-    uint8_t* ds_row = sg + DS_OFF + h * CHUNK + kr * 128;
     const float2 c2 = make_float2(c_log2, c_log2);
     bool ok = n_iter > 0;
     for (int it = 0; ok && it < n_iter; ++it) {
-      const int s = it % STAGES;
+      const int s = it % Q_STAGES, g = it % DO_STAGES;
       const int q0 = (q_start + it) * BT + 64 * h;  // first query of this thread's columns
       if (!(ok = mbar_wait_warp(bar(B_SF), it & 1, ctl))) break;
       tc_fence_after();
@@ -287,9 +290,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
       tc_fence_before();
       mbar_arrive(bar(B_SFREE));                   // S^T may now receive the next tile
-      if (!(ok = mbar_wait_warp(bar(B_QF(s)), (it / STAGES) & 1, ctl))) break;
-      const float* Ls = reinterpret_cast<const float*>(sg + LD_OFF + s * 1024) + 64 * h;
-      const float* Ds = Ls + 128;
+      if (!(ok = mbar_wait_warp(bar(B_QF(s)), (it / Q_STAGES) & 1, ctl))) break;
+      const float* Ls = reinterpret_cast<const float*>(sg + L_OFF + s * 512) + 64 * h;
       // P^T = exp2(S^T c - L log2e); on the diagonal tile, zero where the query precedes
       // the key
       float p[64];
@@ -310,46 +312,49 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < 64; ++c)
           if (q0 + c < gkey) p[c] = 0.f;
       }
-      // dP^T of this tile; it also means the dK MMAs of the previous tile are done with
-      // dS^T in shared memory
+      // dP^T of this tile (its MMAs follow the previous tile's dV and dK in the pipe)
       if (!(ok = mbar_wait_warp(bar(B_DPF), it & 1, ctl))) break;
-      // D came with dO, which the dP^T MMAs just waited on
-      if (!(ok = mbar_wait_warp(bar(B_GF(s)), (it / STAGES) & 1, ctl))) break;
       tc_fence_after();
       tmem_ld32(tP, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
       tmem_ld32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-      // dS^T = P^T o (dP^T - D) to shared memory (128-byte swizzle: chunk u of row kr at
-      // u ^ (kr & 7))
+      // P^T as 16-bit pairs over the first 32 of those columns
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float4 da = *reinterpret_cast<const float4*>(Ds + 8 * u);
-        const float4 db = *reinterpret_cast<const float4*>(Ds + 8 * u + 4);
-        const float dq[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-        uint32_t dw[4];
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pw[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 8 * u + 2 * e;
-          const float2 ds = mul2(make_float2(p[c], p[c + 1]),
-                                 add2(make_float2(__uint_as_float(x[c]), __uint_as_float(x[c + 1])),
-                                      make_float2(-dq[2 * e], -dq[2 * e + 1])));
-          dw[e] = pack2<BF16>(ds.x, ds.y);
-        }
-        *reinterpret_cast<uint4*>(ds_row + ((u ^ (kr & 7)) << 4)) =
-            make_uint4(dw[0], dw[1], dw[2], dw[3]);
-      }
-      {
-        // P^T as 16-bit pairs over the dP^T columns just read (A operand of dV)
-        uint32_t pw[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pw[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
-        tmem_st32(tP, pw);
+        for (int i = 0; i < 16; ++i) pw[i] = pack2<BF16>(p[32 * hh + 2 * i], p[32 * hh + 2 * i + 1]);
+        tmem_st16(tP + 16 * hh, pw);
       }
       tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(B_PF));
+      mbar_arrive(bar(B_PR));
+      // dS^T = P^T o (dP^T - D) as 16-bit pairs over the last 32 (D came with dO, which
+      // the dP^T MMAs waited on)
+      if (!(ok = mbar_wait_warp(bar(B_GF(g)), (it / DO_STAGES) & 1, ctl))) break;
+      const float* Ds = reinterpret_cast<const float*>(sg + D_OFF + g * 512) + 64 * h;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t dw[16];
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(Ds + 32 * hh + 4 * i4);
+          const int c = 32 * hh + 4 * i4;
+          const float2 ds0 = mul2(make_float2(p[c], p[c + 1]),
+                                  add2(make_float2(__uint_as_float(x[c]), __uint_as_float(x[c + 1])),
+                                       make_float2(-d4.x, -d4.y)));
+          const float2 ds1 = mul2(make_float2(p[c + 2], p[c + 3]),
+                                  add2(make_float2(__uint_as_float(x[c + 2]), __uint_as_float(x[c + 3])),
+                                       make_float2(-d4.z, -d4.w)));
+          dw[2 * i4] = pack2<BF16>(ds0.x, ds0.y);
+          dw[2 * i4 + 1] = pack2<BF16>(ds1.x, ds1.y);
+        }
+        tmem_st16(tP + 32 + 16 * hh, dw);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_DR));
     }
     if (ok && mbar_wait_warp(bar(B_OF), 0, ctl)) {
       tc_fence_after();
