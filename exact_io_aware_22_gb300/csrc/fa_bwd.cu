@@ -136,8 +136,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + BN - 1) / BN;
   const int nqb = Np / BM;
-  const int bh = blockIdx.x / nkb;
-  const int kb = blockIdx.x % nkb;          // key block
+  const BlockPos bp = block_pos(nkb);
+  const int bh = bp.bh;
+  const int kb = bp.rank;                   // key block (causal: block 0 has the most work)
   const int i0 = CAUSAL ? kb : 0;           // BM == BN: the diagonal query block
   const int n_iter = nqb - i0;
 
@@ -366,8 +367,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = Np / BM;
   const int nkb = (N + BN - 1) / BN;
-  const int bh = blockIdx.x / nqb;
-  const int qb = nqb - 1 - (blockIdx.x % nqb);     // longest causal blocks first
+  const BlockPos bp = block_pos(nqb);
+  const int bh = bp.bh;
+  const int qb = nqb - 1 - bp.rank;                // causal: the last query blocks have the most work
   const int n_iter = CAUSAL ? min(qb + 1, nkb) : nkb;
 
   auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };

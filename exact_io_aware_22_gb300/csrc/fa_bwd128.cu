@@ -137,8 +137,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + BT - 1) / BT;
   const int nq = Np / BT;
-  const int bh = blockIdx.x / nkb;
-  const int kb = blockIdx.x % nkb;                 // causal: block 0 has the most work, runs first
+  const BlockPos bp = block_pos(nkb);
+  const int bh = bp.bh;
+  const int kb = bp.rank;                          // causal: block 0 has the most work
   const int q_start = CAUSAL ? kb : 0;             // the diagonal query tile
   const int n_iter = nq - q_start;
 
@@ -408,8 +409,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = Np / BT;
   const int nkb = (N + BT - 1) / BT;
-  const int bh = blockIdx.x / nqb;
-  const int qb = nqb - 1 - (blockIdx.x % nqb);     // causal: longest query tiles first
+  const BlockPos bp = block_pos(nqb);
+  const int bh = bp.bh;
+  const int qb = nqb - 1 - bp.rank;                // causal: the last query tiles have the most work
   const int n_iter = CAUSAL ? min(qb + 1, nkb) : nkb;
 
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };

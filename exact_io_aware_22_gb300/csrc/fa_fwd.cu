@@ -78,8 +78,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sg = smem_raw + (sb - raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / n_qblk;
-  const int qblk = n_qblk - 1 - (blockIdx.x % n_qblk);   // longest causal blocks first
+  const BlockPos bp = block_pos(n_qblk);
+  const int bh = bp.bh;
+  const int qblk = n_qblk - 1 - bp.rank;        // causal: the last query tiles have the most work
   const int row0 = qblk * (NT * BM);
   const int nkv = (N + BN - 1) / BN;
   int n_t[NT];

@@ -255,6 +255,26 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool bf16, b
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- block order
+// Which (batch*head, tile rank) a CTA of a grid of nblk tiles per head takes.
+// Heads go in groups of 8; inside a group every head's rank-0 tile comes first,
+// then every head's rank-1 tile, and so on.  Rank 0 is the tile with the most
+// work under the causal mask, so the grid runs close to longest-first (the short
+// tiles fill the tail), while the CTAs running at one time stream the K/V or
+// Q/dO of at most a few heads, which stay in L2.
+struct BlockPos {
+  int bh, rank;
+};
+__device__ __forceinline__ BlockPos block_pos(int nblk) {
+  constexpr int G = 8;
+  const int bid = static_cast<int>(blockIdx.x);
+  const int BH = static_cast<int>(gridDim.x) / nblk;
+  const int g0 = bid / (G * nblk) * G;
+  const int gsz = min(G, BH - g0);
+  const int w = bid - g0 * nblk;
+  return {g0 + w % gsz, w / gsz};
+}
+
 // ---------------------------------------------------------------- numerics
 __device__ __forceinline__ float ex2(float x) {
   float y;
