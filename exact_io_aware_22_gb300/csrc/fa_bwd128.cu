@@ -69,14 +69,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// X^T = A B^T over the head dim into TMEM columns d_col: A and B are 128-row
-// K-major tiles (two 64-column chunks each).
-__device__ __forceinline__ void issue_ab_t(uint32_t d_tmem, uint32_t a, uint32_t b, uint32_t idesc) {
+// X^T = A B^T over the head dim into TMEM columns d_tmem: A and B are 128-row
+// K-major tiles (two 64-column chunks each), given by their descriptor low words
+// (sdesc_lo with LBO 16).
+__device__ __forceinline__ void issue_ab_t_w(uint32_t d_tmem, uint32_t alo, uint32_t blo,
+                                             uint32_t idesc) {
+  constexpr uint32_t hi = sdesc_hi(1024, UMMA_SW128);
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t o = (kk / 4) * CHUNK + (kk % 4) * 32;
-    umma_ss(d_tmem, umma_sdesc(a + o, 16, 1024, UMMA_SW128), umma_sdesc(b + o, 16, 1024, UMMA_SW128),
-            idesc, kk > 0);
+    const uint32_t o = ((kk / 4) * CHUNK + (kk % 4) * 32) >> 4;
+    umma_ss_w(d_tmem, alo + o, blo + o, hi, idesc, kk > 0);
   }
 }
 
@@ -212,14 +214,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && n_iter > 0) {
       constexpr uint32_t idS = umma_idesc_f16(BT, BT, BF16, false, false);   // S^T, dP^T
       constexpr uint32_t idG = umma_idesc_f16(BT, HD, BF16, false, true);    // dV, dK
+      // descriptor low words: K, V and stage 0 of the Q and dO rings, K-major (LBO 16,
+      // for S^T and dP^T) and MN-major (LBO = one 64-column chunk, for dK and dV); a
+      // stage is TILE bytes on
+      constexpr uint32_t HI = sdesc_hi(1024, UMMA_SW128), STAGE_W = TILE >> 4;
+      const uint32_t k_lo = sdesc_lo(sb + K_OFF, 16), v_lo = sdesc_lo(sb + V_OFF, 16);
+      const uint32_t q_lo = sdesc_lo(sb + Q_OFF, 16), qm_lo = sdesc_lo(sb + Q_OFF, CHUNK);
+      const uint32_t o_lo = sdesc_lo(sb + DO_OFF, 16), om_lo = sdesc_lo(sb + DO_OFF, CHUNK);
       bool ok = mbar_wait(bar(B_KV), 0, ctl) && mbar_wait(bar(B_QF(0)), 0, ctl);
       if (ok) {
         tc_fence_after();
-        issue_ab_t(tmem + S_COL, sb + K_OFF, sb + Q_OFF, idS);
+        issue_ab_t_w(tmem + S_COL, k_lo, q_lo, idS);
         umma_commit(bar(B_SF));
         if ((ok = mbar_wait(bar(B_GF(0)), 0, ctl))) {
           tc_fence_after();
-          issue_ab_t(tmem + DP_COL, sb + V_OFF, sb + DO_OFF, idS);
+          issue_ab_t_w(tmem + DP_COL, v_lo, o_lo, idS);
           umma_commit(bar(B_DPF));
         }
       }
@@ -232,27 +241,25 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!(ok = mbar_wait(bar(B_QF(s1)), ((it + 1) / Q_STAGES) & 1, ctl))) break;
           if (!(ok = mbar_wait(bar(B_SFREE), it & 1, ctl))) break;
           tc_fence_after();
-          issue_ab_t(tmem + S_COL, sb + K_OFF, sb + Q_OFF + s1 * TILE, idS);
+          issue_ab_t_w(tmem + S_COL, k_lo, q_lo + s1 * STAGE_W, idS);
           umma_commit(bar(B_SF));
         }
         // dV += P^T dO, P^T from the first half of each warpgroup's dP^T columns
         if (!(ok = mbar_wait(bar(B_PR), it & 1, ctl))) break;
         tc_fence_after();
-        const uint32_t da = sb + DO_OFF + g * TILE;
+        const uint32_t dv_b = om_lo + g * STAGE_W, acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
-          umma_ts(tmem + DV_COL, tmem + DP_COL + (kk / 4) * 64 + (kk % 4) * 8,
-                  umma_sdesc(da + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
-                  (it > 0 || kk > 0) ? 1u : 0u);
+          umma_ts_w(tmem + DV_COL, tmem + DP_COL + (kk / 4) * 64 + (kk % 4) * 8,
+                    dv_b + kk * (2048 >> 4), HI, idG, kk > 0 ? 1u : acc0);
         // dK += dS^T Q, dS^T from the second half
         if (!(ok = mbar_wait(bar(B_DR), it & 1, ctl))) break;
         tc_fence_after();
-        const uint32_t qa = sb + Q_OFF + s * TILE;
+        const uint32_t dk_b = qm_lo + s * STAGE_W;
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
-          umma_ts(tmem + DK_COL, tmem + DP_COL + (kk / 4) * 64 + 32 + (kk % 4) * 8,
-                  umma_sdesc(qa + kk * 2048, CHUNK, 1024, UMMA_SW128), idG,
-                  (it > 0 || kk > 0) ? 1u : 0u);
+          umma_ts_w(tmem + DK_COL, tmem + DP_COL + (kk / 4) * 64 + 32 + (kk % 4) * 8,
+                    dk_b + kk * (2048 >> 4), HI, idG, kk > 0 ? 1u : acc0);
         umma_commit(bar(B_QE(s)));
         umma_commit(bar(B_GE(g)));
         if (next) {
@@ -260,7 +267,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int g1 = (it + 1) % DO_STAGES;
           if (!(ok = mbar_wait(bar(B_GF(g1)), ((it + 1) / DO_STAGES) & 1, ctl))) break;
           tc_fence_after();
-          issue_ab_t(tmem + DP_COL, sb + V_OFF, sb + DO_OFF + g1 * TILE, idS);
+          issue_ab_t_w(tmem + DP_COL, v_lo, o_lo + g1 * STAGE_W, idS);
           umma_commit(bar(B_DPF));
         }
       }
@@ -316,11 +323,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       // dP^T of this tile (its MMAs follow the previous tile's dV and dK in the pipe)
       if (!(ok = mbar_wait_warp(bar(B_DPF), it & 1, ctl))) break;
       tc_fence_after();
-      tmem_ld32(tP, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-      tmem_ld32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-      // P^T as 16-bit pairs over the first 32 of those columns
+      uint32_t xa[16], xb[16], xc[16];
+      tmem_ld16(tP, xa);
+      tmem_ld16(tP + 16, xb);
+      tmem_ld16(tP + 32, xc);
+      tmem_ld_wait_regs(xa);
+      tmem_ld_wait_regs(xb);
+      tmem_ld_wait_regs(xc);
+      // P^T as 16-bit pairs over columns [0, 32)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pw[16];
@@ -331,27 +341,49 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_PR));
-      // dS^T = P^T o (dP^T - D) as 16-bit pairs over the last 32 (D came with dO, which
-      // the dP^T MMAs waited on)
+      // dS^T = P^T o (dP^T - D) as 16-bit pairs: queries [0, 32) over columns [32, 48),
+      // then queries [32, 64) over [48, 64) (D came with dO, which the dP^T MMAs
+      // waited on)
       if (!(ok = mbar_wait_warp(bar(B_GF(g)), (it / DO_STAGES) & 1, ctl))) break;
       const float* Ds = reinterpret_cast<const float*>(sg + D_OFF + g * 512) + 64 * h;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      {
         uint32_t dw[16];
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(Ds + 32 * hh + 4 * i4);
-          const int c = 32 * hh + 4 * i4;
+          const float4 d4 = *reinterpret_cast<const float4*>(Ds + 4 * i4);
+          const int c = 4 * i4, o = (i4 & 3) * 4;
+          const uint32_t* xx = i4 < 4 ? xa : xb;
           const float2 ds0 = mul2(make_float2(p[c], p[c + 1]),
-                                  add2(make_float2(__uint_as_float(x[c]), __uint_as_float(x[c + 1])),
+                                  add2(make_float2(__uint_as_float(xx[o]), __uint_as_float(xx[o + 1])),
                                        make_float2(-d4.x, -d4.y)));
           const float2 ds1 = mul2(make_float2(p[c + 2], p[c + 3]),
-                                  add2(make_float2(__uint_as_float(x[c + 2]), __uint_as_float(x[c + 3])),
+                                  add2(make_float2(__uint_as_float(xx[o + 2]), __uint_as_float(xx[o + 3])),
                                        make_float2(-d4.z, -d4.w)));
           dw[2 * i4] = pack2<BF16>(ds0.x, ds0.y);
           dw[2 * i4 + 1] = pack2<BF16>(ds1.x, ds1.y);
         }
-        tmem_st16(tP + 32 + 16 * hh, dw);
+        tmem_st16(tP + 32, dw);
+      }
+      {
+        uint32_t xd[16];
+        tmem_ld16(tP + 48, xd);
+        tmem_ld_wait_regs(xd);
+        uint32_t dw[16];
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(Ds + 32 + 4 * i4);
+          const int c = 32 + 4 * i4, o = (i4 & 3) * 4;
+          const uint32_t* xx = i4 < 4 ? xc : xd;
+          const float2 ds0 = mul2(make_float2(p[c], p[c + 1]),
+                                  add2(make_float2(__uint_as_float(xx[o]), __uint_as_float(xx[o + 1])),
+                                       make_float2(-d4.x, -d4.y)));
+          const float2 ds1 = mul2(make_float2(p[c + 2], p[c + 3]),
+                                  add2(make_float2(__uint_as_float(xx[o + 2]), __uint_as_float(xx[o + 3])),
+                                       make_float2(-d4.z, -d4.w)));
+          dw[2 * i4] = pack2<BF16>(ds0.x, ds0.y);
+          dw[2 * i4 + 1] = pack2<BF16>(ds1.x, ds1.y);
+        }
+        tmem_st16(tP + 48, dw);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -468,16 +500,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && n_iter > 0) {
       constexpr uint32_t idS = umma_idesc_f16(BT, BT, BF16, false, false);   // S, dP
       constexpr uint32_t idQ = umma_idesc_f16(BT, HD, BF16, false, true);    // dQ
+      // descriptor low words of dO and of stage 0 of the K and V rings, K-major (LBO 16)
+      // and, for K as the B operand of dQ, MN-major (LBO = one 64-column chunk)
+      constexpr uint32_t HI = sdesc_hi(1024, UMMA_SW128), STAGE_W = TILE >> 4;
+      const uint32_t k_lo = sdesc_lo(sb + K_OFF, 16), km_lo = sdesc_lo(sb + K_OFF, CHUNK);
+      const uint32_t v_lo = sdesc_lo(sb + V_OFF, 16), o_lo = sdesc_lo(sb + DO_OFF, 16);
       auto issue_s = [&](int st) {                   // S = Q K^T, Q from TMEM
+        const uint32_t b0 = k_lo + st * STAGE_W;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_ts(tmem + S_COL, tmem + QT_COL + kk * 8,
-                  umma_sdesc(sb + K_OFF + st * TILE + (kk / 4) * CHUNK + (kk % 4) * 32, 16, 1024,
-                             UMMA_SW128),
-                  idS, kk > 0);
+          umma_ts_w(tmem + S_COL, tmem + QT_COL + kk * 8,
+                    b0 + (((kk / 4) * CHUNK + (kk % 4) * 32) >> 4), HI, idS, kk > 0);
       };
       auto issue_dp = [&](int st) {                  // dP = dO V^T
-        issue_ab_t(tmem + DP_COL, sb + DO_OFF, sb + V_OFF + st * TILE, idS);
+        issue_ab_t_w(tmem + DP_COL, o_lo, v_lo + st * STAGE_W, idS);
       };
       bool ok = mbar_wait(bar(B_QR), 0, ctl) && mbar_wait(bar(B_DOF), 0, ctl) &&
                 mbar_wait(bar(B_KF(0)), 0, ctl);
@@ -506,12 +542,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         // dQ += dS K: dS from Z, K as an MN-major B
         if (!(ok = mbar_wait(bar(B_DSF), j & 1, ctl))) break;
         tc_fence_after();
-        const uint32_t ka = sb + K_OFF + s * TILE;
+        const uint32_t kb0 = km_lo + s * STAGE_W;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
-          umma_ts(tmem + DQ_COL, tmem + Z_COL + (kk / 4) * 32 + (kk % 4) * 8,
-                  umma_sdesc(ka + kk * 2048, CHUNK, 1024, UMMA_SW128), idQ,
-                  (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts_w(tmem + DQ_COL, tmem + Z_COL + (kk / 4) * 32 + (kk % 4) * 8,
+                    kb0 + kk * (2048 >> 4), HI, idQ, kk > 0 ? 1u : acc0);
         umma_commit(bar(B_ZFREE));
         umma_commit(bar(B_KE(s)));
       }

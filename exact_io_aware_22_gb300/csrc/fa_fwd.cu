@@ -165,23 +165,26 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && n_max > 0) {
       constexpr uint32_t idS = umma_idesc_f16(BM, BN, BF16, false, false);
       constexpr uint32_t idO = umma_idesc_f16(BM, D, BF16, false, true);
+      // descriptor low words of Q tile 0 and of stage 0 of the K and V rings (K-major
+      // with LBO 16; V MN-major with LBO = one swizzle-width chunk); tiles and stages
+      // are TILE_BYTES apart
+      constexpr uint32_t HI = sdesc_hi(8 * C::SW, C::SWZ), STAGE_W = C::TILE_BYTES >> 4;
+      const uint32_t q_lo = sdesc_lo(sb + C::Q_OFF, 16), k_lo = sdesc_lo(sb + C::K_OFF, 16);
+      const uint32_t v_lo = sdesc_lo(sb + C::V_OFF, C::CHUNK_BYTES);
       auto issue_S = [&](int t, int s) {
-        const uint32_t qa = sb + C::Q_OFF + t * C::TILE_BYTES;
-        const uint32_t ka = sb + C::K_OFF + s * C::TILE_BYTES;
+        const uint32_t qa = q_lo + t * STAGE_W, ka = k_lo + s * STAGE_W;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = kmajor_koff<D>(kk);
-          umma_ss(tmem + C::S_COL + t * BN, umma_sdesc(qa + o, 16, 8 * C::SW, C::SWZ),
-                  umma_sdesc(ka + o, 16, 8 * C::SW, C::SWZ), idS, kk > 0);
+          const uint32_t o = kmajor_koff<D>(kk) >> 4;
+          umma_ss_w(tmem + C::S_COL + t * BN, qa + o, ka + o, HI, idS, kk > 0);
         }
       };
       auto issue_PV = [&](int t, int s, bool acc) {
-        const uint32_t va = sb + C::V_OFF + s * C::TILE_BYTES;
+        const uint32_t va = v_lo + s * STAGE_W, acc0 = acc ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          umma_ts(tmem + C::O_COL + t * D, tmem + C::S_COL + t * BN + kk * 8,
-                  umma_sdesc(va + kk * 16 * C::SW, C::CHUNK_BYTES, 8 * C::SW, C::SWZ), idO,
-                  (acc || kk > 0) ? 1u : 0u);
+          umma_ts_w(tmem + C::O_COL + t * D, tmem + C::S_COL + t * BN + kk * 8,
+                    va + ((kk * 16 * C::SW) >> 4), HI, idO, kk > 0 ? 1u : acc0);
         }
       };
       bool ok = mbar_wait(bar(B_QF), 0, ctl) && mbar_wait(bar(B_KF(0)), 0, ctl);

@@ -62,13 +62,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait that may suspend the thread for up to `hint_ns` (it resumes as soon as
+// the phase completes), so a waiting warp takes no issue slots from the warps
+// sharing its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase with the given parity to complete.  Returns false (and
 // records a timeout) if it does not complete within ctl.wait_limit_ns.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const KernelCtl& ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (globaltimer_ns() - t0 > ctl.wait_limit_ns) {
       atomicOr(ctl.status, FA_DEV_TIMEOUT);
       return false;
@@ -140,6 +153,26 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// umma_ss / umma_ts with the shared-memory descriptors given as their words
+// (sdesc_lo / sdesc_hi).
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint32_t alo, uint32_t blo,
+                                          uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\tmov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(alo), "r"(blo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo,
+                                          uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\tmov.b64 b, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(blo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrive (once) on an mbarrier when all previously issued tcgen05 async ops of
@@ -245,6 +278,18 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
+// The same descriptor as two 32-bit words.  The high word (SBO, version,
+// swizzle) is one constant for all operands of a kernel; the low word (start
+// address, LBO) is set up once per buffer, and an offset inside a tile only adds
+// offset/16 to it: shared addresses stay below 2^18, so the 14-bit start-address
+// field never carries into LBO.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo, uint32_t swz) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | ((swz & 7u) << 29);
+}
+
 // Instruction descriptor, kind::f16 with fp32 accumulator: A and B both fp16
 // or both bf16; a_mn / b_mn select MN-major operands; N>>3 at bits 17..22,
 // M>>4 at bits 24..28.
@@ -265,14 +310,16 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool bf16, b
 struct BlockPos {
   int bh, rank;
 };
-__device__ __forceinline__ BlockPos block_pos(int nblk) {
+__device__ __forceinline__ BlockPos block_pos(int nblk, int bid) {
   constexpr int G = 8;
-  const int bid = static_cast<int>(blockIdx.x);
   const int BH = static_cast<int>(gridDim.x) / nblk;
   const int g0 = bid / (G * nblk) * G;
   const int gsz = min(G, BH - g0);
   const int w = bid - g0 * nblk;
   return {g0 + w % gsz, w / gsz};
+}
+__device__ __forceinline__ BlockPos block_pos(int nblk) {
+  return block_pos(nblk, static_cast<int>(blockIdx.x));
 }
 
 // ---------------------------------------------------------------- numerics
