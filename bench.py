@@ -5,7 +5,9 @@ One step = the whole hot path over one batch of synthetic input: the forward
 (O, L) and the backward (D pre-pass, dK/dV, dQ) of attention for the long-
 context workload B=1, H=32, N=8192, d=128, bf16, causal.  Inputs are resident
 in HBM before timing; the four inputs (256 MiB) and the per-kernel working sets
-exceed the 126 MB L2, so no flush is needed between steps.
+exceed the 126 MB L2, so no flush is needed between steps.  Smaller workloads
+(--workload) whose inputs fit in L2 get a buffer of four times the L2 size
+written between steps, outside the timed spans.
 
 Prints one JSON line (rank 0).  FLOPs follow the usual convention: 4*B*H*N^2*d
 forward, 2.5x that backward, halved when causal.
@@ -45,6 +47,7 @@ WORKLOADS = {
     "gpt2m_causal_d64_fp16": (8, 16, 1024, 64, "fp16", True),
 }
 DEFAULT_WORKLOAD = "n8k_causal_d128_bf16"
+L2_BYTES = 129 * 1000 * 1000        # GB300 L2 (126 MiB)
 KERNEL_SOURCES = {
     "fwd_kernel": "exact_io_aware_22_gb300/csrc/fa_fwd.cu",
     "bwd_pre_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
@@ -267,23 +270,43 @@ def run_ours(args, rank, world, local_rank):
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_id = str(local_rank)
+    # Q, K, V, dO larger than L2: nothing survives in L2 from one step to the next.
+    # Otherwise write a buffer larger than L2 between steps and time each step alone.
+    in_bytes = 4 * B * H * N * d * 2
+    flush = None
+    if in_bytes < L2_BYTES:
+        flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    l2_note = (f"inputs larger than L2 ({in_bytes >> 20} MiB of Q,K,V,dO), no flush" if flush is None
+               else f"inputs fit in L2 ({in_bytes >> 20} MiB of Q,K,V,dO): "
+                    f"{flush.numel() * 4 >> 20} MiB written between steps, outside the timed spans")
     sampler = ClockSampler(gpu_id)
     time.sleep(0.2)
     barrier()
     torch.cuda.synchronize()
     fa.trace_enable(True)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
+    if flush is None:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        spans = [(t0, t1)]
+    else:
+        spans = []
+        for _ in range(args.steps):
+            flush.zero_()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            step()
+            t1.record(stream)
+            spans.append((t0, t1))
     torch.cuda.synchronize()
     barrier()
     fa.trace_enable(False)
     clocks = sampler.stop()
     if fa.device_status() != 0:
         raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
-    ms = t0.elapsed_time(t1) / args.steps
+    ms = sum(a.elapsed_time(b) for a, b in spans) / args.steps
     traced = fa.trace_read()
     ms = max_over_ranks(ms, world, dev)
     value = whole_job_tflops(fwd_f + bwd_f, world, ms)
@@ -363,7 +386,7 @@ def run_ours(args, rank, world, local_rank):
                "data": "synthetic",
                "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d,
                           "causal": causal, "parallelism": f"replicas x{world}",
-                          "l2": "inputs larger than L2 (256 MiB of Q,K,V,dO), no flush"},
+                          "l2": l2_note},
                "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                "fwd_tflops": fwd_f / (fwd_ms / 1e3) / 1e12 if fwd_ms else None,
                "bwd_tflops": bwd_f / (bwd_ms / 1e3) / 1e12 if bwd_ms else None,
