@@ -39,13 +39,22 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOP/s (N=8K,d=128,bf16,causal); % of GB300 tensor peak"
 WORKLOADS = {
-    # name: (B, H, N, d, dtype, causal)
+    # name: (B, H, N, d, dtype, causal[, Hkv]); Hkv < H: K/V heads shared by groups of
+    # H/Hkv query heads (grouped-query attention), same FLOPs as H independent heads
     "n8k_causal_d128_bf16": (1, 32, 8192, 128, "bf16", True),
     "n16k_causal_d128_bf16": (1, 32, 16384, 128, "bf16", True),
     "n4k_causal_d128_bf16": (2, 16, 4096, 128, "bf16", True),
     "n4k_full_d128_bf16": (2, 16, 4096, 128, "bf16", False),
     "gpt2m_causal_d64_fp16": (8, 16, 1024, 64, "fp16", True),
+    "gqa8_n8k_causal_d128_bf16": (1, 32, 8192, 128, "bf16", True, 8),
 }
+
+
+def workload(name):
+    """(B, H, Hkv, N, d, dtype, causal) of a named workload."""
+    w = WORKLOADS[name]
+    B, H, N, d, dtype, causal = w[:6]
+    return B, H, (w[6] if len(w) > 6 else H), N, d, dtype, causal
 DEFAULT_WORKLOAD = "n8k_causal_d128_bf16"
 L2_BYTES = 129 * 1000 * 1000        # GB300 L2 (126 MiB)
 KERNEL_SOURCES = {
@@ -172,6 +181,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _head(flat, h, grp):
+    """Query head h (flat b*H+h index) with its K/V head, as (1, 1, N, d) fp64 arrays."""
+    return {n: flat[n][(h // grp if n in ("k", "v") else h):][:1].double().numpy()[None]
+            for n in flat}
+
+
 def cpu_baseline(x, B, H, N, d, causal, scale, budget_s=10.0, max_heads=8):
     """Time the fp64 oracle as it stands on the host cores over whole (batch, head) pairs
     of the workload until ``budget_s`` is spent (at least one pair)."""
@@ -179,9 +194,10 @@ def cpu_baseline(x, B, H, N, d, causal, scale, budget_s=10.0, max_heads=8):
     import oracle
     fwd_f, bwd_f = attn_flops(1, 1, N, d, causal)
     heads, t_total = 0, 0.0
-    flat = {n: x[n].reshape(B * H, N, d) for n in ("q", "k", "v", "do")}
+    flat = {n: x[n].reshape(-1, N, d) for n in ("q", "k", "v", "do")}
+    grp = H * B // flat["k"].shape[0]
     while heads < min(max_heads, B * H) and (heads == 0 or t_total < budget_s):
-        sel = {n: flat[n][heads:heads + 1].double().numpy()[None] for n in flat}
+        sel = _head(flat, heads, grp)
         t0 = time.perf_counter()
         oracle.fwd(sel["q"], sel["k"], sel["v"], causal, scale)
         oracle.bwd(sel["q"], sel["k"], sel["v"], sel["do"], causal, scale)
@@ -198,15 +214,14 @@ def run_reference(args, rank, world):
         return
     import oracle
     from exact_io_aware_22_gb300 import inputs
-    B, H, N, d, dtype, causal = WORKLOADS[args.workload]
+    B, H, Hkv, N, d, dtype, causal = workload(args.workload)
     scale = 1.0 / math.sqrt(d)
-    x = inputs.make_inputs(B, H, N, d, dtype, seed=0)
-    flat = {n: x[n].reshape(B * H, N, d) for n in ("q", "k", "v", "do")}
+    x = inputs.make_inputs(B, H, N, d, dtype, seed=0, Hkv=Hkv)
+    flat = {n: x[n].reshape(-1, N, d) for n in ("q", "k", "v", "do")}
     fwd_f, bwd_f = attn_flops(1, 1, N, d, causal)
 
     def step(i):
-        h = i % (B * H)
-        sel = {n: flat[n][h:h + 1].double().numpy()[None] for n in flat}
+        sel = _head(flat, i % (B * H), H // Hkv)
         oracle.fwd(sel["q"], sel["k"], sel["v"], causal, scale)
         oracle.bwd(sel["q"], sel["k"], sel["v"], sel["do"], causal, scale)
 
@@ -223,8 +238,8 @@ def run_reference(args, rank, world):
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic",
-           "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": causal,
-                      "step_unit": "one (batch, head) pair"},
+           "config": {"workload": args.workload, "B": B, "H": H, "Hkv": Hkv, "N": N, "d": d,
+                      "causal": causal, "step_unit": "one (batch, head) pair"},
            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -241,14 +256,14 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    B, H, N, d, dtype, causal = WORKLOADS[args.workload]
+    B, H, Hkv, N, d, dtype, causal = workload(args.workload)
     scale = 1.0 / math.sqrt(d)
     fwd_f, bwd_f = attn_flops(B, H, N, d, causal)
-    x = inputs.make_inputs(B, H, N, d, dtype, seed=rank)
+    x = inputs.make_inputs(B, H, N, d, dtype, seed=rank, Hkv=Hkv)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.bwd_workspace_size(B, H, N, d, causal), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -272,7 +287,7 @@ def run_ours(args, rank, world, local_rank):
         gpu_id = str(local_rank)
     # Q, K, V, dO larger than L2: nothing survives in L2 from one step to the next.
     # Otherwise write a buffer larger than L2 between steps and time each step alone.
-    in_bytes = 4 * B * H * N * d * 2
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do))
     flush = None
     if in_bytes < L2_BYTES:
         flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -347,7 +362,7 @@ def run_ours(args, rank, world, local_rank):
         hx = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        hg = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
+        hg = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
 
         def e2e_step():
             for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
@@ -372,7 +387,8 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         ems = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
         e2e = {"value": whole_job_tflops(fwd_f + bwd_f, world, ems), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": 4 * n_bytes, "d2h_bytes_per_step": 4 * n_bytes + 4 * B * H * N,
+               "h2d_bytes_per_step": in_bytes,
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv)),
                "ms_per_step": ems, "steps": ke}
 
     cpu = None
@@ -385,7 +401,7 @@ def run_ours(args, rank, world, local_rank):
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
                "data": "synthetic",
                "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d,
-                          "causal": causal, "parallelism": f"replicas x{world}",
+                          "causal": causal, "Hkv": Hkv, "parallelism": f"replicas x{world}",
                           "l2": l2_note},
                "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                "fwd_tflops": fwd_f / (fwd_ms / 1e3) / 1e12 if fwd_ms else None,

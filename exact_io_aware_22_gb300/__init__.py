@@ -60,6 +60,11 @@ def load_library(path: str | None = None):
     lib.fa_bwd_workspace_size.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
     lib.fa_bwd.restype = i
+    lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_gqa.restype = i
+    lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, i,
+                               vp]
+    lib.fa_bwd_gqa.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_cuda_error.restype = i
@@ -112,16 +117,28 @@ def _need_cuda(*ts):
             raise ValueError("all tensors must be contiguous (B, H, N, d)")
 
 
+def _kv_heads(q, k, v) -> int:
+    """Hkv of K and V shaped (B, Hkv, N, d) beside q (B, H, N, d), H a multiple of Hkv."""
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be (B, H, N, d) and k, v one (B, Hkv, N, d) shape")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if (k.shape[0], k.shape[2], k.shape[3]) != (B, N, d) or Hkv < 1 or H % Hkv:
+        raise ValueError("k, v must be (B, Hkv, N, d) with H a multiple of Hkv")
+    return Hkv
+
+
 def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=None):
     """O, L = attention(q, k, v) for (B, H, N, d) fp16/bf16 CUDA tensors.
 
     L is (B, H, N) fp32, the natural-log logsumexp of each row's scaled scores.
+    k and v may have fewer heads, (B, Hkv, N, d) with H a multiple of Hkv: each
+    group of H/Hkv consecutive query heads shares one K/V head (GQA; Hkv = 1 is MQA).
     ``scale`` defaults to 1/sqrt(d).  Runs asynchronously on torch's current stream.
     """
     import torch
     _need_cuda(q, k, v)
-    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must share one (B, H, N, d) shape")
+    Hkv = _kv_heads(q, k, v)
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share one dtype")
     B, H, N, d = q.shape
@@ -136,8 +153,12 @@ def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=
             or lse.dtype != torch.float32:
         raise ValueError("out must match q; lse must be (B, H, N) fp32")
     lib = load_library()
-    _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(causal),
-                      float(scale), _dtype_code(q), _stream()), "fa_fwd")
+    if Hkv == H:
+        _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(causal),
+                          float(scale), _dtype_code(q), _stream()), "fa_fwd")
+    else:
+        _check(lib.fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                              int(causal), float(scale), _dtype_code(q), _stream()), "fa_fwd_gqa")
     return out, lse
 
 
@@ -147,34 +168,46 @@ def bwd_workspace_size(B: int, H: int, N: int, d: int, causal: bool = True) -> i
 
 def bwd(q, k, v, o, lse, do, causal: bool = True, scale: float | None = None,
         dq=None, dk=None, dv=None, workspace=None):
-    """dQ, dK, dV of attention for upstream gradient ``do`` (all (B, H, N, d)).
+    """dQ, dK, dV of attention for upstream gradient ``do``.
 
-    ``o`` and ``lse`` are the forward's outputs.  ``workspace`` (optional) is a CUDA
-    uint8 tensor of at least ``bwd_workspace_size`` bytes; without it the library
-    takes scratch from the stream-ordered allocator.
+    q, o, do, dq are (B, H, N, d); k, v, dk, dv are (B, Hkv, N, d) (Hkv = H unless
+    K/V heads are shared, as in ``fwd``; a shared head's dK and dV sum over its
+    query heads).  ``o`` and ``lse`` are the forward's outputs.  ``workspace``
+    (optional) is a CUDA uint8 tensor of at least ``bwd_workspace_size`` bytes;
+    without it the library takes scratch from the stream-ordered allocator.
     """
     import torch
     _need_cuda(q, k, v, o, lse, do)
+    Hkv = _kv_heads(q, k, v)
     B, H, N, d = q.shape
     for t in (k, v, o, do):
-        if t.shape != q.shape or t.dtype != q.dtype:
-            raise ValueError("q, k, v, o, do must share one shape and dtype")
+        if t.dtype != q.dtype:
+            raise ValueError("q, k, v, o, do must share one dtype")
+    if o.shape != q.shape or do.shape != q.shape:
+        raise ValueError("o and do must match q")
     if lse.shape != (B, H, N) or lse.dtype != torch.float32:
         raise ValueError("lse must be (B, H, N) fp32")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
     _need_cuda(dq, dk, dv)
+    if dq.shape != q.shape or dk.shape != k.shape or dv.shape != v.shape:
+        raise ValueError("dq must match q, dk and dv must match k and v")
     ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
     if workspace is not None:
         _need_cuda(workspace)
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     lib = load_library()
-    _check(lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                      _ptr(dv), ws_ptr, ws_bytes, B, H, N, d, int(causal), float(scale),
-                      _dtype_code(q), _stream()), "fa_bwd")
+    if Hkv == H:
+        _check(lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                          _ptr(dk), _ptr(dv), ws_ptr, ws_bytes, B, H, N, d, int(causal),
+                          float(scale), _dtype_code(q), _stream()), "fa_bwd")
+    else:
+        _check(lib.fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                              _ptr(dk), _ptr(dv), ws_ptr, ws_bytes, B, H, Hkv, N, d, int(causal),
+                              float(scale), _dtype_code(q), _stream()), "fa_bwd_gqa")
     return dq, dk, dv
 
 

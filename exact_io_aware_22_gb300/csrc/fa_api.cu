@@ -249,34 +249,58 @@ fa_status fa_selftest_timeout(unsigned long long limit_ns, void* stream) {
   return fa_device_status(stream);
 }
 
-fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
-                 int N, int d, int causal, float scale, fa_dtype dtype, void* stream) {
+// Hkv K/V heads shared by groups of H/Hkv consecutive query heads (Hkv == H: no sharing).
+static fa_status check_heads(int H, int Hkv) {
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_INVALID_VALUE;
+  return FA_OK;
+}
+
+static fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* L, int B,
+                          int H, int Hkv, int N, int d, int causal, float scale, fa_dtype dtype,
+                          void* stream) {
   fa_status st = check_common(B, H, N, d, causal, scale, static_cast<int>(dtype));
   if (st != FA_OK) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if (!Q || !K || !V || !O || !L) return FA_ERR_INVALID_VALUE;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(L, 4))
     return FA_ERR_MISALIGNED;
-  const long long BH = static_cast<long long>(B) * H;
+  const long long BH = static_cast<long long>(B) * H, BHkv = static_cast<long long>(B) * Hkv;
   const size_t nbytes = static_cast<size_t>(BH) * N * d * 2, lbytes = static_cast<size_t>(BH) * N * 4;
-  for (const void* in : {Q, K, V})
-    if (overlap(in, nbytes, O, nbytes) || overlap(in, nbytes, L, lbytes)) return FA_ERR_INVALID_VALUE;
+  const size_t kvbytes = static_cast<size_t>(BHkv) * N * d * 2;
+  const void* ins[3] = {Q, K, V};
+  const size_t insz[3] = {nbytes, kvbytes, kvbytes};
+  for (int i = 0; i < 3; ++i)
+    if (overlap(ins[i], insz[i], O, nbytes) || overlap(ins[i], insz[i], L, lbytes))
+      return FA_ERR_INVALID_VALUE;
   if (overlap(O, nbytes, L, lbytes)) return FA_ERR_INVALID_VALUE;
 
   const bool bf16 = dtype == FA_BF16;
   fa::FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   if ((st = make_map(&a.tmQ, Q, d, N, BH, bf16)) != FA_OK) return st;
-  if ((st = make_map(&a.tmK, K, d, N, BH, bf16)) != FA_OK) return st;
-  if ((st = make_map(&a.tmV, V, d, N, BH, bf16)) != FA_OK) return st;
+  if ((st = make_map(&a.tmK, K, d, N, BHkv, bf16)) != FA_OK) return st;
+  if ((st = make_map(&a.tmV, V, d, N, BHkv, bf16)) != FA_OK) return st;
   if ((st = ctl_for_launch(&a.ctl)) != FA_OK) return st;
   a.O = O;
   a.L = L;
   a.N = N;
   a.BH = static_cast<int>(BH);
+  a.group = H / Hkv;
   a.c_log2 = scale * 1.4426950408889634f;
   cudaError_t e = fa::launch_fwd(a, d, bf16, causal != 0, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
+}
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                 int N, int d, int causal, float scale, fa_dtype dtype, void* stream) {
+  return fwd_impl(Q, K, V, O, L, B, H, H, N, d, causal, scale, dtype, stream);
+}
+
+fa_status fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                     int Hkv, int N, int d, int causal, float scale, fa_dtype dtype,
+                     void* stream) {
+  return fwd_impl(Q, K, V, O, L, B, H, Hkv, N, d, causal, scale, dtype, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
@@ -284,12 +308,13 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
   return fa::bwd_workspace_bytes(static_cast<long long>(B) * H, N, d);
 }
 
-fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                 const float* L, void* dQ, void* dK, void* dV, void* workspace,
-                 size_t workspace_bytes, int B, int H, int N, int d, int causal, float scale,
-                 fa_dtype dtype, void* stream) {
+static fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
+                          const void* dO, const float* L, void* dQ, void* dK, void* dV,
+                          void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                          int d, int causal, float scale, fa_dtype dtype, void* stream) {
   fa_status st = check_common(B, H, N, d, causal, scale, static_cast<int>(dtype));
   if (st != FA_OK) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if (!Q || !K || !V || !O || !dO || !L || !dQ || !dK || !dV) return FA_ERR_INVALID_VALUE;
   for (const void* p : {Q, K, V, O, dO, static_cast<const void*>(dQ), static_cast<const void*>(dK),
                         static_cast<const void*>(dV)})
@@ -298,23 +323,28 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   const long long BH = static_cast<long long>(B) * H;
   const size_t need = fa::bwd_workspace_bytes(BH, N, d);
   if (workspace && workspace_bytes < need) return FA_ERR_INVALID_VALUE;
+  const long long BHkv = static_cast<long long>(B) * Hkv;
   const size_t nbytes = static_cast<size_t>(BH) * N * d * 2, lbytes = static_cast<size_t>(BH) * N * 4;
+  const size_t kvbytes = static_cast<size_t>(BHkv) * N * d * 2;
   const void* outs[3] = {dQ, dK, dV};
+  const size_t outsz[3] = {nbytes, kvbytes, kvbytes};
+  const void* ins[5] = {Q, K, V, O, dO};
+  const size_t insz[5] = {nbytes, kvbytes, kvbytes, nbytes, nbytes};
   for (int i = 0; i < 3; ++i) {
-    for (const void* in : {Q, K, V, O, dO})
-      if (overlap(in, nbytes, outs[i], nbytes)) return FA_ERR_INVALID_VALUE;
-    if (overlap(L, lbytes, outs[i], nbytes)) return FA_ERR_INVALID_VALUE;
+    for (int j = 0; j < 5; ++j)
+      if (overlap(ins[j], insz[j], outs[i], outsz[i])) return FA_ERR_INVALID_VALUE;
+    if (overlap(L, lbytes, outs[i], outsz[i])) return FA_ERR_INVALID_VALUE;
     for (int j = i + 1; j < 3; ++j)
-      if (overlap(outs[i], nbytes, outs[j], nbytes)) return FA_ERR_INVALID_VALUE;
-    if (workspace && overlap(workspace, need, outs[i], nbytes)) return FA_ERR_INVALID_VALUE;
+      if (overlap(outs[i], outsz[i], outs[j], outsz[j])) return FA_ERR_INVALID_VALUE;
+    if (workspace && overlap(workspace, need, outs[i], outsz[i])) return FA_ERR_INVALID_VALUE;
   }
 
   const bool bf16 = dtype == FA_BF16;
   fa::BwdArgs a;
   std::memset(&a, 0, sizeof(a));
   if ((st = make_map(&a.tmQ, Q, d, N, BH, bf16)) != FA_OK) return st;
-  if ((st = make_map(&a.tmK, K, d, N, BH, bf16)) != FA_OK) return st;
-  if ((st = make_map(&a.tmV, V, d, N, BH, bf16)) != FA_OK) return st;
+  if ((st = make_map(&a.tmK, K, d, N, BHkv, bf16)) != FA_OK) return st;
+  if ((st = make_map(&a.tmV, V, d, N, BHkv, bf16)) != FA_OK) return st;
   if ((st = make_map(&a.tmO, O, d, N, BH, bf16)) != FA_OK) return st;
   if ((st = make_map(&a.tmdO, dO, d, N, BH, bf16)) != FA_OK) return st;
   if ((st = ctl_for_launch(&a.ctl)) != FA_OK) return st;
@@ -336,6 +366,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   a.dV = dV;
   a.N = N;
   a.BH = static_cast<int>(BH);
+  a.group = H / Hkv;
   a.scale = scale;
   a.c_log2 = scale * 1.4426950408889634f;
   cudaError_t e = fa::launch_bwd(a, d, bf16, causal != 0, s);
@@ -345,6 +376,22 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   }
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                 size_t workspace_bytes, int B, int H, int N, int d, int causal, float scale,
+                 fa_dtype dtype, void* stream) {
+  return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, B, H, H, N, d, causal,
+                  scale, dtype, stream);
+}
+
+fa_status fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                     size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int causal,
+                     float scale, fa_dtype dtype, void* stream) {
+  return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, B, H, Hkv, N, d,
+                  causal, scale, dtype, stream);
 }
 
 }  // extern "C"

@@ -125,7 +125,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dK,
-                void* __restrict__ dV, int N, int Np, float scale, float c_log2, KernelCtl ctl) {
+                void* __restrict__ dV, int N, int Np, int group, float scale, float c_log2,
+                KernelCtl ctl) {
   using G = Geo<D>;
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -137,10 +138,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nkb = (N + BN - 1) / BN;
   const int nqb = Np / BM;
   const BlockPos bp = block_pos(nkb);
-  const int bh = bp.bh;
+  const int bkv = bp.bh;                    // K/V head; its query heads are bkv*group + g
   const int kb = bp.rank;                   // key block (causal: block 0 has the most work)
   const int i0 = CAUSAL ? kb : 0;           // BM == BN: the diagonal query block
-  const int n_iter = nqb - i0;
+  const int n_head = nqb - i0;              // query blocks per query head
+  const int n_iter = group * n_head;        // every query head of the group in turn
 
   auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };
   const int B_KV = 0;
@@ -166,17 +168,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && n_iter > 0) {
       bool ok = true;
       mbar_arrive_expect_tx(bar(B_KV), 2 * G::TILE_BYTES);
-      load_tile<D>(sb + C::K_OFF, &tmK, bar(B_KV), kb * BN, bh);
-      load_tile<D>(sb + C::V_OFF, &tmV, bar(B_KV), kb * BN, bh);
+      load_tile<D>(sb + C::K_OFF, &tmK, bar(B_KV), kb * BN, bkv);
+      load_tile<D>(sb + C::V_OFF, &tmV, bar(B_KV), kb * BN, bkv);
       int it = 0;
       for (; it < n_iter; ++it) {
         const int s = it % G::STAGES;
         const uint32_t ph = (it / G::STAGES) & 1;
         if (!(ok = mbar_wait(bar(B_QE(s)), ph ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_QF(s)), 2 * G::TILE_BYTES);
-        const int qrow = (i0 + it) * BM;
-        load_tile<D>(sb + C::Q_OFF + s * G::TILE_BYTES, &tmQ, bar(B_QF(s)), qrow, bh);
-        load_tile<D>(sb + C::DO_OFF + s * G::TILE_BYTES, &tmdO, bar(B_QF(s)), qrow, bh);
+        const int g = it / n_head;
+        const int qrow = (i0 + it - g * n_head) * BM, bhq = bkv * group + g;
+        load_tile<D>(sb + C::Q_OFF + s * G::TILE_BYTES, &tmQ, bar(B_QF(s)), qrow, bhq);
+        load_tile<D>(sb + C::DO_OFF + s * G::TILE_BYTES, &tmdO, bar(B_QF(s)), qrow, bhq);
       }
       if (!ok) {
         mbar_wait(bar(B_KV), 0, ctl);
@@ -242,11 +245,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tS = tmem + lane_off + C::S_COL + h * 64;
     const uint32_t tP = tmem + lane_off + C::DP_COL + h * 64;
     uint8_t* ds_row = sg + C::DS_OFF + h * (128 * 128) + kr * 128;
-    const float* Lb = Lp + static_cast<size_t>(bh) * Np;
-    const float* Db = Dp + static_cast<size_t>(bh) * Np;
     bool ok = n_iter > 0;
     for (int it = 0; ok && it < n_iter; ++it) {
-      const int qb = i0 + it;
+      const int g = it / n_head;
+      const int qb = i0 + it - g * n_head;
+      const float* Lb = Lp + static_cast<size_t>(bkv * group + g) * Np;
+      const float* Db = Dp + static_cast<size_t>(bkv * group + g) * Np;
       if (!(ok = mbar_wait_warp(bar(B_SF), it & 1, ctl))) break;
       tc_fence_after();
       uint32_t s[64], dp[64];
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       const bool valid = gkey < N;
-      const size_t roff = (static_cast<size_t>(bh) * N + gkey) * D;
+      const size_t roff = (static_cast<size_t>(bkv) * N + gkey) * D;
       constexpr int HALF = D / 2;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dQ,
-              int N, int Np, float scale, float c_log2, KernelCtl ctl) {
+              int N, int Np, int group, float scale, float c_log2, KernelCtl ctl) {
   using G = Geo<D>;
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -404,8 +408,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t ph = (it / G::STAGES) & 1;
         if (!(ok = mbar_wait(bar(B_KE(s)), ph ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_KF(s)), 2 * G::TILE_BYTES);
-        load_tile<D>(sb + C::K_OFF + s * G::TILE_BYTES, &tmK, bar(B_KF(s)), it * BN, bh);
-        load_tile<D>(sb + C::V_OFF + s * G::TILE_BYTES, &tmV, bar(B_KF(s)), it * BN, bh);
+        load_tile<D>(sb + C::K_OFF + s * G::TILE_BYTES, &tmK, bar(B_KF(s)), it * BN, bh / group);
+        load_tile<D>(sb + C::V_OFF + s * G::TILE_BYTES, &tmV, bar(B_KF(s)), it * BN, bh / group);
       }
       if (!ok) {
         mbar_wait(bar(B_QF), 0, ctl);
@@ -551,10 +555,11 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DkdvCfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const long long grid = static_cast<long long>(nqb) * a.BH;
+    const long long grid = static_cast<long long>(nqb) * (a.BH / a.group);   // per K/V head
     trace_begin(TR_BWD_DKDV, st);
     kern<<<static_cast<unsigned>(grid), THREADS, DkdvCfg<D>::SMEM_BYTES, st>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.scale, a.c_log2, a.ctl);
+        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.scale, a.c_log2,
+        a.ctl);
     trace_end(TR_BWD_DKDV, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -567,7 +572,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     const long long grid = static_cast<long long>(nqb) * a.BH;
     trace_begin(TR_BWD_DQ, st);
     kern<<<static_cast<unsigned>(grid), THREADS, DqCfg<D>::SMEM_BYTES, st>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dQ, a.N, Np, a.scale, a.c_log2, a.ctl);
+        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.scale, a.c_log2, a.ctl);
     trace_end(TR_BWD_DQ, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -127,8 +127,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     dkdv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                    const float* __restrict__ Dp, const float* __restrict__ Lp,
-                   void* __restrict__ dK, void* __restrict__ dV, int N, int Np, float scale,
-                   float c_log2, KernelCtl ctl) {
+                   void* __restrict__ dK, void* __restrict__ dV, int N, int Np, int group,
+                   float scale, float c_log2, KernelCtl ctl) {
   using namespace kv;
   extern __shared__ __align__(1024) uint8_t sg[];
   const uint32_t sb = smem_u32(sg);
@@ -140,10 +140,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nkb = (N + BT - 1) / BT;
   const int nq = Np / BT;
   const BlockPos bp = block_pos(nkb);
-  const int bh = bp.bh;
+  const int bkv = bp.bh;                           // K/V head; its query heads: bkv*group + g
   const int kb = bp.rank;                          // causal: block 0 has the most work
   const int q_start = CAUSAL ? kb : 0;             // the diagonal query tile
-  const int n_iter = nq - q_start;
+  const int n_head = nq - q_start;                 // query tiles per query head
+  const int n_iter = group * n_head;               // the group's query heads one after another
 
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
   const int B_KV = 0;
@@ -175,8 +176,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(bar(B_KV), 2 * TILE);
       for (int c = 0; c < 2; ++c) {
-        tma_load_3d(sb + K_OFF + c * CHUNK, &tmK, bar(B_KV), c * 64, kb * BT, bh);
-        tma_load_3d(sb + V_OFF + c * CHUNK, &tmV, bar(B_KV), c * 64, kb * BT, bh);
+        tma_load_3d(sb + K_OFF + c * CHUNK, &tmK, bar(B_KV), c * 64, kb * BT, bkv);
+        tma_load_3d(sb + V_OFF + c * CHUNK, &tmV, bar(B_KV), c * 64, kb * BT, bkv);
       }
       // Q with L*log2e in a three-stage ring, dO with D in a two-stage ring (L and D:
       // padded per-row arrays, 512-byte aligned per tile).  Both stages of a tile are
@@ -185,18 +186,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       int nq_issued = 0, ng_issued = 0;
       for (int it = 0; ok && it < n_iter; ++it) {
         const int s = it % Q_STAGES, g = it % DO_STAGES;
-        const int qrow = (q_start + it) * BT;
-        const size_t row = static_cast<size_t>(bh) * Np + qrow;
+        const int gh = it / n_head;                // which query head of the group
+        const int qrow = (q_start + it - gh * n_head) * BT, bhq = bkv * group + gh;
+        const size_t row = static_cast<size_t>(bhq) * Np + qrow;
         if (!(ok = mbar_wait(bar(B_QE(s)), ((it / Q_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_QF(s)), TILE + 512);
         for (int c = 0; c < 2; ++c)
-          tma_load_3d(sb + Q_OFF + s * TILE + c * CHUNK, &tmQ, bar(B_QF(s)), c * 64, qrow, bh);
+          tma_load_3d(sb + Q_OFF + s * TILE + c * CHUNK, &tmQ, bar(B_QF(s)), c * 64, qrow, bhq);
         bulk_load(sb + L_OFF + s * 512, Lp + row, 512, bar(B_QF(s)));
         ++nq_issued;
         if (!(ok = mbar_wait(bar(B_GE(g)), ((it / DO_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_GF(g)), TILE + 512);
         for (int c = 0; c < 2; ++c)
-          tma_load_3d(sb + DO_OFF + g * TILE + c * CHUNK, &tmdO, bar(B_GF(g)), c * 64, qrow, bh);
+          tma_load_3d(sb + DO_OFF + g * TILE + c * CHUNK, &tmdO, bar(B_GF(g)), c * 64, qrow,
+                      bhq);
         bulk_load(sb + D_OFF + g * 512, Dp + row, 512, bar(B_GF(g)));
         ++ng_issued;
       }
@@ -286,9 +289,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tP = tmem + lane_off + DP_COL + 64 * h;
     const float2 c2 = make_float2(c_log2, c_log2);
     bool ok = n_iter > 0;
-    for (int it = 0; ok && it < n_iter; ++it) {
+    for (int it = 0, itl = 0; ok && it < n_iter; ++it, itl = itl + 1 == n_head ? 0 : itl + 1) {
       const int s = it % Q_STAGES, g = it % DO_STAGES;
-      const int q0 = (q_start + it) * BT + 64 * h;  // first query of this thread's columns
       if (!(ok = mbar_wait_warp(bar(B_SF), it & 1, ctl))) break;
       tc_fence_after();
       uint32_t x[64];
@@ -315,10 +317,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         p[4 * c4 + 2] = ex2(t1.x);
         p[4 * c4 + 3] = ex2(t1.y);
       }
-      if (CAUSAL && it == 0) {
+      if (CAUSAL && itl == 0) {
+        // the diagonal tile (query tile kb of each head): zero where the query (column
+        // 64h + c) precedes the key (row kr)
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (q0 + c < gkey) p[c] = 0.f;
+          if (64 * h + c < kr) p[c] = 0.f;
       }
       // dP^T of this tile (its MMAs follow the previous tile's dV and dK in the pipe)
       if (!(ok = mbar_wait_warp(bar(B_DPF), it & 1, ctl))) break;
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       const bool valid = gkey < N;
-      const size_t roff = (static_cast<size_t>(bh) * N + gkey) * HD + 64 * h;
+      const size_t roff = (static_cast<size_t>(bkv) * N + gkey) * HD + 64 * h;
       store_row64<BF16>(tmem + lane_off + DV_COL + 64 * h, 1.f, reinterpret_cast<T*>(dV) + roff,
                         valid);
       store_row64<BF16>(tmem + lane_off + DK_COL + 64 * h, scale, reinterpret_cast<T*>(dK) + roff,
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     dq128_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmdO, const void* __restrict__ Q,
                  const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dQ,
-                 int N, int Np, float scale, float c_log2, KernelCtl ctl) {
+                 int N, int Np, int group, float scale, float c_log2, KernelCtl ctl) {
   using namespace qd;
   extern __shared__ __align__(1024) uint8_t sg[];
   const uint32_t sb = smem_u32(sg);
@@ -444,6 +448,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const BlockPos bp = block_pos(nqb);
   const int bh = bp.bh;
   const int qb = nqb - 1 - bp.rank;                // causal: the last query tiles have the most work
+  const int bkv = bh / group;                      // the K/V head of this query head
   const int n_iter = CAUSAL ? min(qb + 1, nkb) : nkb;
 
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
@@ -484,8 +489,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!(ok = mbar_wait(bar(B_KE(s)), ((j / KV_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_KF(s)), 2 * TILE);
         for (int c = 0; c < 2; ++c) {
-          tma_load_3d(sb + K_OFF + s * TILE + c * CHUNK, &tmK, bar(B_KF(s)), c * 64, j * BT, bh);
-          tma_load_3d(sb + V_OFF + s * TILE + c * CHUNK, &tmV, bar(B_KF(s)), c * 64, j * BT, bh);
+          tma_load_3d(sb + K_OFF + s * TILE + c * CHUNK, &tmK, bar(B_KF(s)), c * 64, j * BT, bkv);
+          tma_load_3d(sb + V_OFF + s * TILE + c * CHUNK, &tmV, bar(B_KF(s)), c * 64, j * BT, bkv);
         }
       }
       if (!ok) {
@@ -657,15 +662,17 @@ template <bool BF16, bool CAUSAL>
 cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
   const int Np = (a.N + 127) / 128 * 128;
   const float* Lp = a.Dvec + static_cast<size_t>(a.BH) * Np;
-  const long long nblk = static_cast<long long>(Np / BT) * a.BH;
+  const long long nblk = static_cast<long long>(Np / BT) * a.BH;           // dQ: per query head
+  const long long nblk_kv = static_cast<long long>(Np / BT) * (a.BH / a.group);   // per K/V head
   {
     auto kern = dkdv128_kernel<BF16, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kv::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DKDV, st);
-    kern<<<static_cast<unsigned>(nblk), THREADS, kv::SMEM_BYTES, st>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.scale, a.c_log2, a.ctl);
+    kern<<<static_cast<unsigned>(nblk_kv), THREADS, kv::SMEM_BYTES, st>>>(
+        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.scale, a.c_log2,
+        a.ctl);
     trace_end(TR_BWD_DKDV, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -677,7 +684,7 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DQ, st);
     kern<<<static_cast<unsigned>(nblk), THREADS, qd::SMEM_BYTES, st>>>(
-        a.tmK, a.tmV, a.tmdO, a.Q, a.Dvec, Lp, a.dQ, a.N, Np, a.scale, a.c_log2, a.ctl);
+        a.tmK, a.tmV, a.tmdO, a.Q, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.scale, a.c_log2, a.ctl);
     trace_end(TR_BWD_DQ, st);
     return cudaGetLastError();
   }

@@ -70,7 +70,8 @@ template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, void* __restrict__ Out,
-               float* __restrict__ Lout, int N, int n_qblk, float c_log2, KernelCtl ctl) {
+               float* __restrict__ Lout, int N, int n_qblk, int group, float c_log2,
+               KernelCtl ctl) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const BlockPos bp = block_pos(n_qblk);
   const int bh = bp.bh;
   const int qblk = n_qblk - 1 - bp.rank;        // causal: the last query tiles have the most work
+  const int bkv = bh / group;                   // the K/V head of this query head (b-major heads)
   const int row0 = qblk * (NT * BM);
   const int nkv = (N + BN - 1) / BN;
   int n_t[NT];
@@ -140,12 +142,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(bar(B_KF(s)), C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(sb + C::K_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmK, bar(B_KF(s)),
-                      c * C::ATOM, j * BN, bh);
+                      c * C::ATOM, j * BN, bkv);
         if (!(ok = mbar_wait(bar(B_VE(s)), ph ^ 1, ctl))) { ++j; break; }
         mbar_arrive_expect_tx(bar(B_VF(s)), C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(sb + C::V_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV, bar(B_VF(s)),
-                      c * C::ATOM, j * BN, bh);
+                      c * C::ATOM, j * BN, bkv);
       }
       if (!ok) {
         // drain: wait (bounded) for every copy this thread issued, so no bulk
@@ -366,7 +368,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   trace_begin(TR_FWD, st);
   kern<<<static_cast<unsigned>(grid), THREADS, C::SMEM_BYTES, st>>>(
-      a.tmQ, a.tmK, a.tmV, a.O, a.L, a.N, n_qblk, a.c_log2, a.ctl);
+      a.tmQ, a.tmK, a.tmV, a.O, a.L, a.N, n_qblk, a.group, a.c_log2, a.ctl);
   trace_end(TR_FWD, st);
   return cudaGetLastError();
 }

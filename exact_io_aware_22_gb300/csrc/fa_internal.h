@@ -32,10 +32,11 @@ struct FwdTileInfo {
 FwdTileInfo fwd_tile_info(int d);
 
 struct FwdArgs {
-  CUtensorMap tmQ, tmK, tmV;   // 3-D maps (d, N, B*H) of the 16-bit inputs
+  CUtensorMap tmQ, tmK, tmV;   // 3-D maps (d, N, B*H) of Q; (d, N, B*Hkv) of K and V
   void* O;
   float* L;
   int N, BH;
+  int group;                   // query heads per K/V head (H / Hkv; 1 without sharing)
   float c_log2;                // scale * log2(e)
   KernelCtl ctl;
 };
@@ -51,7 +52,8 @@ struct BwdArgs {
   void* dQ;
   void* dK;
   void* dV;
-  int N, BH;
+  int N, BH;                   // BH = B*H query heads
+  int group;                   // query heads per K/V head; B*H/group K/V heads
   float scale, c_log2;
   KernelCtl ctl;
 };

@@ -7,7 +7,8 @@ Recipe: one CPU ``torch.Generator`` seeded per workload; draws in the fixed
 order Q, K, V, dO, each i.i.d. N(0, 1) in fp32 of shape (B, H, N, d); Q and K
 are then multiplied by ``qk_std`` (4 for the large-row-maximum stress case);
 finally every tensor is rounded to the 16-bit dtype.  The oracle consumes the
-rounded values upcast exactly to fp64.
+rounded values upcast exactly to fp64.  With ``Hkv`` (grouped-query attention)
+K and V are drawn with Hkv heads instead of H, in the same order.
 """
 from __future__ import annotations
 
@@ -17,14 +18,16 @@ DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
 
 
 def make_inputs(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int = 0,
-                qk_std: float = 1.0):
-    """Return dict(q, k, v, do) of CPU tensors (B, H, N, d) in ``dtype``."""
+                qk_std: float = 1.0, Hkv: int | None = None):
+    """Return dict(q, k, v, do) of CPU tensors in ``dtype``: q and do (B, H, N, d),
+    k and v (B, Hkv, N, d) (Hkv defaults to H)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
     shape = (B, H, N, d)
+    kv_shape = (B, H if Hkv is None else Hkv, N, d)
     q = torch.randn(shape, generator=g, dtype=torch.float32)
-    k = torch.randn(shape, generator=g, dtype=torch.float32)
-    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(kv_shape, generator=g, dtype=torch.float32)
+    v = torch.randn(kv_shape, generator=g, dtype=torch.float32)
     do = torch.randn(shape, generator=g, dtype=torch.float32)
     if qk_std != 1.0:
         q = q * qk_std

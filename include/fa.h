@@ -78,6 +78,27 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  size_t workspace_bytes, int B, int H, int N, int d, int causal, float scale,
                  fa_dtype dtype, void* stream);
 
+/* Grouped-query and multi-query attention (GQA / MQA).  The docs page lists
+ * "MQA/GQA" among the features its kernels do not have yet ("Scope"); the note
+ * credits FlashAttention-2 with adding them ("Versions and Evolution").  K and V
+ * have Hkv heads instead of H: query head h of batch b attends with K/V head
+ * h / (H/Hkv) of batch b (consecutive query heads share one K/V head; Hkv == 1 is
+ * MQA, Hkv == H is fa_fwd / fa_bwd).  Each query head computes exactly what
+ * fa_fwd computes with that K/V head; in the backward, dK and dV of a shared head
+ * are the sums over its H/Hkv query heads.
+ *   Layout   Q, O, dO, dQ: (B, H, N, d); K, V, dK, dV: (B, Hkv, N, d); L: (B, H, N).
+ *   Errors   as fa_fwd / fa_bwd, plus FA_ERR_INVALID_VALUE when Hkv < 1, Hkv > H
+ *            or H is not a multiple of Hkv.
+ *   Workspace of fa_bwd_gqa: fa_bwd_workspace_size(B, H, N, d, causal) bytes (it
+ *            depends on the query heads only), or NULL as for fa_bwd. */
+fa_status fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                     int Hkv, int N, int d, int causal, float scale, fa_dtype dtype,
+                     void* stream);
+fa_status fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                     size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int causal,
+                     float scale, fa_dtype dtype, void* stream);
+
 /* Static description of a status code. */
 const char* fa_status_string(fa_status s);
 

@@ -11,6 +11,12 @@ Contents
     (batch, head).  Definitions follow the "flash-attn-triton" docs page,
     section "The argument" (S = QK^T/sqrt(d), row softmax, P V), with causal
     masking lower-triangular (FlashAttention note, "Key Mechanisms").
+  * ``fwd_gqa``/``bwd_gqa``: grouped-query / multi-query attention (the docs
+    page lists MQA/GQA as "not yet", "Scope"; FlashAttention-2 added them, note
+    "Versions and Evolution"): K and V have Hkv heads, each shared by H/Hkv
+    consecutive query heads.  Defined as the plain attention of every query head
+    with its group's K/V head; the gradient of a shared head is the sum over the
+    query heads that read it (chain rule).
   * ``fwd_online``/``row_partial``/``merge``: the separate naive online-softmax
     oracle of the docs page's Fig. 3 and the two-partial merge of the tutorial
     page ("Softmax in pieces").
@@ -94,6 +100,29 @@ class Oracle:
                             B, H, N, d, int(causal), float(scale))
         return dq, dk, dv, D
 
+    @staticmethod
+    def _group(q, k) -> int:
+        H, Hkv = q.shape[1], k.shape[1]
+        if Hkv < 1 or H % Hkv:
+            raise ValueError("H must be a multiple of the K/V head count")
+        return H // Hkv
+
+    def fwd_gqa(self, q, k, v, causal: bool, scale: float):
+        """O, L with K, V of shape (B, Hkv, N, d): query head h uses K/V head h // (H/Hkv)."""
+        g = self._group(q, k)
+        return self.fwd(q, np.repeat(_f64(k), g, axis=1), np.repeat(_f64(v), g, axis=1), causal,
+                        scale)
+
+    def bwd_gqa(self, q, k, v, do, causal: bool, scale: float):
+        """dQ (B, H, N, d); dK, dV (B, Hkv, N, d), each the sum over the group's query
+        heads of the per-head gradient; D = rowsum(dO o O)."""
+        g = self._group(q, k)
+        B, Hkv, N, d = k.shape
+        dq, dk, dv, D = self.bwd(q, np.repeat(_f64(k), g, axis=1), np.repeat(_f64(v), g, axis=1),
+                                 do, causal, scale)
+        return (dq, dk.reshape(B, Hkv, g, N, d).sum(axis=2), dv.reshape(B, Hkv, g, N, d).sum(axis=2),
+                D)
+
     def fwd_online(self, q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):
         """O, L by the per-tile online update (docs page Fig. 3), key tiles of ``tile``."""
         q, k, v = _f64(q), _f64(k), _f64(v)
@@ -149,6 +178,14 @@ def fwd(q, k, v, causal: bool, scale: float):
 
 def bwd(q, k, v, do, causal: bool, scale: float):
     return get().bwd(q, k, v, do, causal, scale)
+
+
+def fwd_gqa(q, k, v, causal: bool, scale: float):
+    return get().fwd_gqa(q, k, v, causal, scale)
+
+
+def bwd_gqa(q, k, v, do, causal: bool, scale: float):
+    return get().bwd_gqa(q, k, v, do, causal, scale)
 
 
 def fwd_online(q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):

@@ -242,6 +242,53 @@ def pin_torch_sdpa(orc, shapes=((1, 1, 128, 64, False), (2, 3, 100, 32, True),
         _close(dv, tv.grad.numpy(), 1e-10, f"dV vs SDPA {B, H, N, d, causal}")
 
 
+def pin_gqa(orc, shapes=((1, 4, 2, 37, 8, False), (2, 6, 2, 45, 16, True),
+                         (1, 4, 1, 33, 8, True), (1, 3, 3, 20, 8, True))):
+    """Grouped-query / multi-query attention.  Library special case: torch's
+    scaled_dot_product_attention with enable_gqa (query head h reads K/V head
+    h // (H/Hkv)) in fp64 with autograd.  Then central finite differences of
+    sum(O o dO) on tiny shapes, where a shared K/V head's gradient must be the sum
+    over its query heads."""
+    import torch
+    rng = np.random.default_rng(10)
+    for B, H, Hkv, N, d, causal in shapes:
+        scale = 1.0 / math.sqrt(d)
+        q, do = _rand(rng, B, H, N, d), _rand(rng, B, H, N, d)
+        k, v = _rand(rng, B, Hkv, N, d), _rand(rng, B, Hkv, N, d)
+        tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal,
+                                                              scale=scale, enable_gqa=True)
+        to.backward(torch.tensor(do, dtype=torch.float64))
+        o, _ = orc.fwd_gqa(q, k, v, causal, scale)
+        dq, dk, dv, _ = orc.bwd_gqa(q, k, v, do, causal, scale)
+        tag = f"{B, H, Hkv, N, d, causal}"
+        _close(o, to.detach().numpy(), 1e-10, f"GQA O vs SDPA {tag}")
+        _close(dq, tq.grad.numpy(), 1e-10, f"GQA dQ vs SDPA {tag}")
+        _close(dk, tk.grad.numpy(), 1e-10, f"GQA dK vs SDPA {tag}")
+        _close(dv, tv.grad.numpy(), 1e-10, f"GQA dV vs SDPA {tag}")
+    h = 1e-6
+    for Hkv in (1, 2):
+        for causal in (False, True):
+            q, do = _rand(rng, 1, 4, 3, 2), _rand(rng, 1, 4, 3, 2)
+            k, v = _rand(rng, 1, Hkv, 3, 2), _rand(rng, 1, Hkv, 3, 2)
+            dq, dk, dv, _ = orc.bwd_gqa(q, k, v, do, causal, 0.8)
+
+            def loss(qq, kk, vv):
+                return float(np.sum(orc.fwd_gqa(qq, kk, vv, causal, 0.8)[0] * do))
+            for name, x, g in (("dK", k, dk), ("dV", v, dv), ("dQ", q, dq)):
+                fd = np.zeros_like(x)
+                for idx in np.ndindex(x.shape):
+                    xp, xm = x.copy(), x.copy()
+                    xp[idx] += h
+                    xm[idx] -= h
+                    ap = {"q": q, "k": k, "v": v}
+                    am = dict(ap)
+                    ap[name[1].lower()], am[name[1].lower()] = xp, xm
+                    fd[idx] = (loss(ap["q"], ap["k"], ap["v"]) - loss(am["q"], am["k"], am["v"])) / (2 * h)
+                err = float(np.max(np.abs(fd - g))) / max(float(np.max(np.abs(fd))), 1e-3)
+                assert err < 1e-6, f"GQA finite differences {name} Hkv={Hkv} causal={causal}: {err:.2e}"
+
+
 def pin_page_sizes(iomodel):
     """Sizes the pages print (tests/golden/page_sizes.json) from the byte model."""
     with open(os.path.join(GOLDEN, "page_sizes.json")) as f:
@@ -259,4 +306,4 @@ def pin_page_sizes(iomodel):
 
 ORACLE_PINS = [pin_rows_sum_to_one, pin_constant_keys, pin_causal_first_row,
                pin_online_matches_safe, pin_L_is_logsumexp, pin_merge, pin_finite_differences,
-               pin_gradient_invariants, pin_torch_sdpa]
+               pin_gradient_invariants, pin_torch_sdpa, pin_gqa]

@@ -49,21 +49,37 @@ def _sel(t: torch.Tensor, heads):
     return flat[list(heads)].unsqueeze(0)
 
 
-def compare(B, H, N, d, dtype, causal, qk_std=1.0, heads=None, seed=0, scale=None):
+def compare(B, H, N, d, dtype, causal, qk_std=1.0, heads=None, seed=0, scale=None, Hkv=None):
     """Run the CUDA path on the whole problem and the oracle on ``heads`` (flat b*H+h
-    indices; None = all).  Returns the error report; asserts the tolerances."""
+    indices; None = all).  Returns the error report; asserts the tolerances.
+
+    With ``Hkv`` (K/V heads shared by groups of H/Hkv query heads) ``heads`` lists
+    flat K/V head indices b*Hkv+j, and each is compared with all its query heads."""
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    x = inputs.make_inputs(B, H, N, d, dtype, seed=seed, qk_std=qk_std)
+    x = inputs.make_inputs(B, H, N, d, dtype, seed=seed, qk_std=qk_std, Hkv=Hkv)
     g = gpu_fwd_bwd(x, causal, scale)
-    q, k, v, do = (_sel(x[n].double(), heads).numpy() for n in ("q", "k", "v", "do"))
-    o_ref, l_ref = oracle.fwd(q, k, v, causal, scale)
-    dq_ref, dk_ref, dv_ref, _ = oracle.bwd(q, k, v, do, causal, scale)
+    if Hkv is None:
+        q, k, v, do = (_sel(x[n].double(), heads).numpy() for n in ("q", "k", "v", "do"))
+        o_ref, l_ref = oracle.fwd(q, k, v, causal, scale)
+        dq_ref, dk_ref, dv_ref, _ = oracle.bwd(q, k, v, do, causal, scale)
+        qheads = kvheads = heads
+    else:
+        grp = H // Hkv
+        kvheads = heads
+        qheads = None if heads is None else [j * grp + t for j in heads for t in range(grp)]
+        q, do = (_sel(x[n].double(), qheads).numpy() for n in ("q", "do"))
+        k, v = (_sel(x[n].double(), kvheads).numpy() for n in ("k", "v"))
+        if heads is not None:   # the selected groups as one batch of len(heads) K/V heads
+            q, do = (t.reshape(1, len(heads) * grp, N, d) for t in (q, do))
+        o_ref, l_ref = oracle.fwd_gqa(q, k, v, causal, scale)
+        dq_ref, dk_ref, dv_ref, _ = oracle.bwd_gqa(q, k, v, do, causal, scale)
     rep = {}
     # size of one dS_ij * k_j term: scale * max|dP| * max|k|, with |dP| <= |dO| |v|
     term = scale * float(np.max(np.linalg.norm(do, axis=-1)) * np.max(np.linalg.norm(v, axis=-1))
                          * max(np.max(np.abs(k)), np.max(np.abs(q))))
     for name, ref in (("o", o_ref), ("lse", l_ref), ("dq", dq_ref), ("dk", dk_ref), ("dv", dv_ref)):
-        got = _sel(g[name], heads).double().numpy()
+        got = _sel(g[name], kvheads if name in ("dk", "dv") else qheads).double().numpy()
+        got = got.reshape(ref.shape)
         assert np.isfinite(got).all(), f"{name}: non-finite values"
         err = float(np.max(np.abs(got - ref)))
         if name in ("dq", "dk", "dv"):

@@ -95,6 +95,45 @@ def test_bwd_rejects(lib, kw, code):
     assert bwd(lib, **kw) == code
 
 
+M1 = 0x100000   # fake buffers 1 MiB apart: the 8-head tensors here are 128 KiB
+
+
+def fwd_gqa(lib, Hkv, **kw):
+    a = dict(Q=M1, K=2 * M1, V=3 * M1, O=4 * M1, L=5 * M1, B=1, H=8, N=128, d=64,
+             causal=1, scale=0.125, dtype=1)
+    a.update(kw)
+    return lib.fa_fwd_gqa(*(ctypes.c_void_p(a[k]) for k in ("Q", "K", "V", "O", "L")), a["B"],
+                          a["H"], Hkv, a["N"], a["d"], a["causal"], a["scale"], a["dtype"], None)
+
+
+def bwd_gqa(lib, Hkv, **kw):
+    a = dict(Q=M1, K=2 * M1, V=3 * M1, O=4 * M1, dO=5 * M1, L=6 * M1, dQ=7 * M1,
+             dK=8 * M1, dV=9 * M1, ws=10 * M1, ws_bytes=1 << 20, B=1, H=8, N=128, d=64,
+             causal=1, scale=0.125, dtype=1)
+    a.update(kw)
+    ptrs = [ctypes.c_void_p(a[k]) for k in ("Q", "K", "V", "O", "dO", "L", "dQ", "dK", "dV", "ws")]
+    return lib.fa_bwd_gqa(*ptrs, a["ws_bytes"], a["B"], a["H"], Hkv, a["N"], a["d"], a["causal"],
+                          a["scale"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("Hkv", [0, -1, 9, 3, 5])
+def test_gqa_rejects_head_counts(lib, Hkv):
+    # K/V heads must divide the 8 query heads
+    assert fwd_gqa(lib, Hkv) == INVALID
+    assert bwd_gqa(lib, Hkv) == INVALID
+
+
+def test_gqa_rejects_like_mha(lib):
+    assert fwd_gqa(lib, 2, d=48) == UNSUPPORTED
+    assert fwd_gqa(lib, 2, K=2 * M1 + 8) == MISALIGNED
+    # with 2 K/V heads K spans 2*128*64*2 = 32 KiB: an O that starts 16 KiB in overlaps it,
+    # one that starts 32 KiB in does not reach Q, K or V (its 128 KiB end before 3 * M1)
+    assert fwd_gqa(lib, 2, O=2 * M1 + 16384) == INVALID
+    assert bwd_gqa(lib, 2, dK=2 * M1 + 16384) == INVALID      # dK overlaps K
+    assert bwd_gqa(lib, 2, dK=7 * M1 + 65536) == INVALID      # dK inside dQ (128 KiB)
+    assert bwd_gqa(lib, 4, ws_bytes=16) == INVALID
+
+
 def test_workspace_size(lib):
     f = lib.fa_bwd_workspace_size
     # D and L*log2(e), fp32, padded to 128-row blocks

@@ -99,3 +99,29 @@ def test_errors_raise_before_launch():
     q = torch.zeros(1, 1, 64, 64, dtype=torch.float16, device="cuda")
     with pytest.raises(fa.FAError, match="INVALID"):
         fa.fwd(q, q.clone(), q.clone(), scale=-1.0)
+
+
+def test_gqa_entry_points_with_equal_heads_match_mha():
+    """fa_fwd_gqa / fa_bwd_gqa with Hkv == H compute what fa_fwd / fa_bwd compute, bit
+    for bit (the same kernels run with groups of one)."""
+    import ctypes
+    import exact_io_aware_22_gb300 as fa
+    from exact_io_aware_22_gb300 import inputs
+    B, H, N, d = 2, 4, 383, 128
+    x = inputs.make_inputs(B, H, N, d, "bf16", seed=21)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fwd(q, k, v, causal=True)
+    dq, dk, dv = fa.bwd(q, k, v, o, lse, do, causal=True)
+    lib = fa.load_library()
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+    scale = 1.0 / d ** 0.5
+    assert lib.fa_fwd_gqa(p(q), p(k), p(v), p(o2), p(lse2), B, H, H, N, d, 1, scale, 1, stream) == 0
+    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    assert lib.fa_bwd_gqa(p(q), p(k), p(v), p(o), p(do), p(lse), p(dq2), p(dk2), p(dv2), None, 0,
+                          B, H, H, N, d, 1, scale, 1, stream) == 0
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    for a, b in ((o, o2), (lse, lse2), (dq, dq2), (dk, dk2), (dv, dv2)):
+        assert torch.equal(a, b)

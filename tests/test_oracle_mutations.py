@@ -59,8 +59,43 @@ def test_mutant_is_caught(name, tmp_path):
             except AssertionError as e:
                 failures.append(pin.__name__)
             continue
+        if pin is pins.pin_gqa:
+            try:
+                pin(orc, shapes=((1, 4, 2, 21, 8, True),))
+            except AssertionError:
+                failures.append(pin.__name__)
+            continue
         try:
             pin(orc)
         except AssertionError:
             failures.append(pin.__name__)
     assert failures, f"no pin caught the planted mistake '{name}'"
+
+
+# Planted mistakes in the oracle's grouped-query layer (Python, oracle/__init__.py):
+# each mutant module is the oracle package's source with one textual edit, run on the
+# real compiled core.
+PY_SRC = os.path.join(os.path.dirname(oracle.__file__), "__init__.py")
+GQA_MUTANTS = {
+    "GQA: dK averaged over the group": (
+        "return (dq, dk.reshape(B, Hkv, g, N, d).sum(axis=2),",
+        "return (dq, dk.reshape(B, Hkv, g, N, d).mean(axis=2),"),
+    "GQA: dV from the first query head only": (
+        "dv.reshape(B, Hkv, g, N, d).sum(axis=2),",
+        "dv.reshape(B, Hkv, g, N, d)[:, :, 0],"),
+    "GQA: interleaved head mapping": (
+        "return self.fwd(q, np.repeat(_f64(k), g, axis=1), np.repeat(_f64(v), g, axis=1), causal,",
+        "return self.fwd(q, np.tile(_f64(k), (1, g, 1, 1)), np.tile(_f64(v), (1, g, 1, 1)), causal,"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GQA_MUTANTS))
+def test_gqa_mutant_is_caught(name):
+    before, after = GQA_MUTANTS[name]
+    text = open(PY_SRC).read()
+    assert text.count(before) == 1, f"mutation anchor not unique: {before!r}"
+    ns = {"__name__": "oracle_mutant", "__file__": PY_SRC}
+    exec(compile(text.replace(before, after), "oracle_mutant", "exec"), ns)
+    orc = ns["Oracle"](oracle.build())
+    with pytest.raises(AssertionError):
+        pins.pin_gqa(orc, shapes=((1, 4, 2, 21, 8, True),))

@@ -54,3 +54,26 @@ def test_stress_row_maxima(dtype):
 def test_non_default_scale():
     compare(1, 2, 256, 64, "fp16", True, scale=0.05, seed=5)
     compare(1, 2, 256, 64, "bf16", False, scale=0.4, seed=6)
+
+
+# Grouped-query / multi-query attention: (B, H, Hkv, N, d, dtype, causal)
+GQA_CASES = [
+    (2, 8, 2, 300, 128, "bf16", True),
+    (1, 8, 1, 257, 128, "fp16", False),     # MQA
+    (2, 6, 3, 200, 64, "fp16", True),
+    (1, 4, 2, 129, 32, "bf16", True),
+    (1, 4, 2, 1, 64, "fp16", True),         # one key
+    (1, 16, 4, 2048, 128, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("case", GQA_CASES, ids=[str(c) for c in GQA_CASES])
+def test_gqa(case):
+    B, H, Hkv, N, d, dt, causal = case
+    print(case, compare(B, H, N, d, dt, causal, seed=11, Hkv=Hkv))
+
+
+def test_gqa_full_size_sampled():
+    # 1 x 32 query heads x 8 K/V heads x 8192 x 128, bf16 causal; K/V heads 0 and 7, each
+    # with its four query heads, compared in full
+    print(compare(1, 32, 8192, 128, "bf16", True, heads=(0, 7), Hkv=8))
