@@ -17,6 +17,9 @@ Contents
     consecutive query heads.  Defined as the plain attention of every query head
     with its group's K/V head; the gradient of a shared head is the sum over the
     query heads that read it (chain rule).
+  * ``window`` (fwd, bwd and the GQA pair): a causal sliding window of W keys,
+    query i seeing keys i - W < j <= i (docs page "Scope" lists sliding windows
+    as not yet supported and fixes no convention; this is the plain reading).
   * ``fwd_online``/``row_partial``/``merge``: the separate naive online-softmax
     oracle of the docs page's Fig. 3 and the two-partial merge of the tutorial
     page ("Softmax in pieces").
@@ -67,8 +70,8 @@ class Oracle:
         lib = ctypes.CDLL(so_path)
         dp = ctypes.POINTER(ctypes.c_double)
         i, dbl = ctypes.c_int, ctypes.c_double
-        lib.oracle_fwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dbl]
-        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, dbl]
+        lib.oracle_fwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dbl, i]
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, dbl, i]
         lib.oracle_fwd_online.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dbl, i, i]
         lib.oracle_row_partial.argtypes = [dp, dp, dp, i, i, i, i, i, dbl, i, i, dp, dp]
         lib.oracle_row_partial.restype = dbl
@@ -80,24 +83,33 @@ class Oracle:
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
 
-    def fwd(self, q, k, v, causal: bool, scale: float):
-        """O, L for (B,H,N,d) inputs.  L is the natural-log logsumexp of scaled scores."""
+    @staticmethod
+    def _window(causal: bool, window: int) -> int:
+        if window < 0 or (window > 0 and not causal):
+            raise ValueError("a sliding window is a causal band of window >= 1 keys")
+        return int(window)
+
+    def fwd(self, q, k, v, causal: bool, scale: float, window: int = 0):
+        """O, L for (B,H,N,d) inputs.  L is the natural-log logsumexp of scaled scores.
+        window > 0 (causal only): query i sees keys i - window < j <= i."""
+        window = self._window(causal, window)
         q, k, v = _f64(q), _f64(k), _f64(v)
         B, H, N, d = q.shape
         o = np.empty_like(q)
         lse = np.empty((B, H, N), dtype=np.float64)
         self.lib.oracle_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d, int(causal),
-                            float(scale))
+                            float(scale), window)
         return o, lse
 
-    def bwd(self, q, k, v, do, causal: bool, scale: float):
+    def bwd(self, q, k, v, do, causal: bool, scale: float, window: int = 0):
         """dQ, dK, dV and D = rowsum(dO o O) from the plain definition."""
+        window = self._window(causal, window)
         q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
         B, H, N, d = q.shape
         dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
         D = np.empty((B, H, N), dtype=np.float64)
         self.lib.oracle_bwd(_p(q), _p(k), _p(v), _p(do), _p(dq), _p(dk), _p(dv), _p(D),
-                            B, H, N, d, int(causal), float(scale))
+                            B, H, N, d, int(causal), float(scale), window)
         return dq, dk, dv, D
 
     @staticmethod
@@ -107,19 +119,19 @@ class Oracle:
             raise ValueError("H must be a multiple of the K/V head count")
         return H // Hkv
 
-    def fwd_gqa(self, q, k, v, causal: bool, scale: float):
+    def fwd_gqa(self, q, k, v, causal: bool, scale: float, window: int = 0):
         """O, L with K, V of shape (B, Hkv, N, d): query head h uses K/V head h // (H/Hkv)."""
         g = self._group(q, k)
         return self.fwd(q, np.repeat(_f64(k), g, axis=1), np.repeat(_f64(v), g, axis=1), causal,
-                        scale)
+                        scale, window)
 
-    def bwd_gqa(self, q, k, v, do, causal: bool, scale: float):
+    def bwd_gqa(self, q, k, v, do, causal: bool, scale: float, window: int = 0):
         """dQ (B, H, N, d); dK, dV (B, Hkv, N, d), each the sum over the group's query
         heads of the per-head gradient; D = rowsum(dO o O)."""
         g = self._group(q, k)
         B, Hkv, N, d = k.shape
         dq, dk, dv, D = self.bwd(q, np.repeat(_f64(k), g, axis=1), np.repeat(_f64(v), g, axis=1),
-                                 do, causal, scale)
+                                 do, causal, scale, window)
         return (dq, dk.reshape(B, Hkv, g, N, d).sum(axis=2), dv.reshape(B, Hkv, g, N, d).sum(axis=2),
                 D)
 
@@ -172,20 +184,20 @@ def num_threads() -> int:
     return get().num_threads()
 
 
-def fwd(q, k, v, causal: bool, scale: float):
-    return get().fwd(q, k, v, causal, scale)
+def fwd(q, k, v, causal: bool, scale: float, window: int = 0):
+    return get().fwd(q, k, v, causal, scale, window)
 
 
-def bwd(q, k, v, do, causal: bool, scale: float):
-    return get().bwd(q, k, v, do, causal, scale)
+def bwd(q, k, v, do, causal: bool, scale: float, window: int = 0):
+    return get().bwd(q, k, v, do, causal, scale, window)
 
 
-def fwd_gqa(q, k, v, causal: bool, scale: float):
-    return get().fwd_gqa(q, k, v, causal, scale)
+def fwd_gqa(q, k, v, causal: bool, scale: float, window: int = 0):
+    return get().fwd_gqa(q, k, v, causal, scale, window)
 
 
-def bwd_gqa(q, k, v, do, causal: bool, scale: float):
-    return get().bwd_gqa(q, k, v, do, causal, scale)
+def bwd_gqa(q, k, v, do, causal: bool, scale: float, window: int = 0):
+    return get().bwd_gqa(q, k, v, do, causal, scale, window)
 
 
 def fwd_online(q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):

@@ -17,6 +17,10 @@
  *       m_i  = max_j S_ij,  l_i = sum_j exp(S_ij - m_i)
  *       P_ij = exp(S_ij - m_i) / l_i,  O_i = sum_j P_ij v_j
  *       L_i  = m_i + ln(l_i)        (natural-log logsumexp of scaled scores)
+ *   Sliding window (window W > 0, causal only): key j is allowed for query i
+ *   iff i - W < j <= i, the W most recent keys.  The docs page lists sliding
+ *   windows among the features its kernels do not have yet ("Scope") and
+ *   defines no convention; this causal band is the plain reading.
  *   A row with no allowed key (never produced by square causal masks) gets
  *   O_i = 0 and L_i = -inf: the tutorial page ("Start with a safe softmax")
  *   asks for fully masked rows to be handled but fixes no convention.
@@ -57,6 +61,8 @@ static double dot(const double* a, const double* b, int d)
 }
 
 static int n_allowed(int i, int N, int causal) { return causal ? (i + 1 < N ? i + 1 : N) : N; }
+/* first allowed key of row i under a window of W keys (0: no window) */
+static int win_start(int i, int window) { return (window > 0 && i - window + 1 > 0) ? i - window + 1 : 0; }
 
 int oracle_num_threads(void)
 {
@@ -84,7 +90,7 @@ static double row_scores(const double* qi, const double* k, int nk, int d, doubl
 }
 
 void oracle_fwd(const double* Q, const double* K, const double* V, double* O, double* L,
-                int B, int H, int N, int d, int causal, double scale)
+                int B, int H, int N, int d, int causal, double scale, int window)
 {
     long BH = (long)B * H;
     /* every (batch, head, row) is independent */
@@ -99,15 +105,16 @@ void oracle_fwd(const double* Q, const double* K, const double* V, double* O, do
                 const double* v = V + bh * N * d;
                 double* o = O + bh * N * d;
                 double* lse = L + bh * N;
-                int nk = n_allowed(i, N, causal);
+                int j0 = win_start(i, window);
+                int nk = n_allowed(i, N, causal) - j0;   /* keys j0 .. j0 + nk - 1 */
                 double l;
-                double m = row_scores(q + (long)i * d, k, nk, d, scale, s, &l);
+                double m = row_scores(q + (long)i * d, k + (long)j0 * d, nk, d, scale, s, &l);
                 double* oi = o + (long)i * d;
                 for (int c = 0; c < d; ++c) oi[c] = 0.0;
                 if (nk == 0) { lse[i] = -INFINITY; continue; }
                 for (int j = 0; j < nk; ++j) {
                     double p = exp(s[j] - m) / l;
-                    const double* vj = v + (long)j * d;
+                    const double* vj = v + (long)(j0 + j) * d;
                     for (int c = 0; c < d; ++c) oi[c] += p * vj[c];
                 }
                 lse[i] = m + log(l);
@@ -126,7 +133,7 @@ void oracle_fwd(const double* Q, const double* K, const double* V, double* O, do
  * dK_j = scale sum_i dS_ij q_i and dV_j = sum_i P_ij dO_i. */
 void oracle_bwd(const double* Q, const double* K, const double* V, const double* dO,
                 double* dQ, double* dK, double* dV, double* Dout,
-                int B, int H, int N, int d, int causal, double scale)
+                int B, int H, int N, int d, int causal, double scale, int window)
 {
     long BH = (long)B * H;
     double* Lrow = (double*)malloc(sizeof(double) * (BH * N > 0 ? BH * N : 1));
@@ -141,27 +148,28 @@ void oracle_bwd(const double* Q, const double* K, const double* V, const double*
                 const double* k = K + bh * N * d;
                 const double* v = V + bh * N * d;
                 const double* dout = dO + bh * N * d;
-                int nk = n_allowed(i, N, causal);
+                int j0 = win_start(i, window);
+                int nk = n_allowed(i, N, causal) - j0;   /* keys j0 .. j0 + nk - 1 */
                 const double* qi = q + (long)i * d;
                 const double* doi = dout + (long)i * d;
                 double* dqi = dQ + bh * N * d + (long)i * d;
                 for (int c = 0; c < d; ++c) { dqi[c] = 0.0; oi[c] = 0.0; }
                 if (nk == 0) { Dout[bh * N + i] = 0.0; Lrow[bh * N + i] = -INFINITY; continue; }
                 double l;
-                double m = row_scores(qi, k, nk, d, scale, s, &l);
+                double m = row_scores(qi, k + (long)j0 * d, nk, d, scale, s, &l);
                 Lrow[bh * N + i] = m + log(l);
-                /* s[j] <- P_ij, and O_i = sum_j P_ij v_j */
+                /* s[j] <- P_i,j0+j, and O_i = sum_j P_ij v_j */
                 for (int j = 0; j < nk; ++j) {
                     s[j] = exp(s[j] - m) / l;
-                    const double* vj = v + (long)j * d;
+                    const double* vj = v + (long)(j0 + j) * d;
                     for (int c = 0; c < d; ++c) oi[c] += s[j] * vj[c];
                 }
                 double Di = dot(doi, oi, d);
                 Dout[bh * N + i] = Di;
                 for (int j = 0; j < nk; ++j) {
-                    double dpij = dot(doi, v + (long)j * d, d);
+                    double dpij = dot(doi, v + (long)(j0 + j) * d, d);
                     double dsij = s[j] * (dpij - Di);
-                    const double* kj = k + (long)j * d;
+                    const double* kj = k + (long)(j0 + j) * d;
                     for (int c = 0; c < d; ++c) dqi[c] += scale * dsij * kj[c];
                 }
             }
@@ -182,6 +190,7 @@ void oracle_bwd(const double* Q, const double* K, const double* V, const double*
             double* dvj = dV + bh * N * d + (long)j * d;
             for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
             for (int i = causal ? j : 0; i < N; ++i) {
+                if (window > 0 && i - j >= window) break;   /* key j left row i's window */
                 const double* qi = q + (long)i * d;
                 const double* doi = dout + (long)i * d;
                 double pij = exp(scale * dot(qi, kj, d) - Lrow[bh * N + i]);

@@ -289,6 +289,46 @@ def pin_gqa(orc, shapes=((1, 4, 2, 37, 8, False), (2, 6, 2, 45, 16, True),
                 assert err < 1e-6, f"GQA finite differences {name} Hkv={Hkv} causal={causal}: {err:.2e}"
 
 
+def pin_window(orc, shapes=((1, 2, 70, 16, 5), (2, 1, 130, 8, 17), (1, 2, 64, 8, 64),
+                            (1, 1, 40, 4, 2))):
+    """Causal sliding window of W keys.  W = 1: every row sees only its own key, so
+    O = V, L_i = scale q_i.k_i, dV = dO and dQ = dK = 0.  W >= N: plain causal.
+    Library special case: torch's scaled_dot_product_attention with the band mask
+    j <= i < j + W in fp64, with autograd for the gradients."""
+    import torch
+    rng = np.random.default_rng(11)
+    q, k, v, do = (_rand(rng, 1, 2, 33, 8) for _ in range(4))
+    o, lse = orc.fwd(q, k, v, True, 0.7, window=1)
+    dq, dk, dv, _ = orc.bwd(q, k, v, do, True, 0.7, window=1)
+    _close(o, v, 1e-12, "W=1: O = V")
+    _close(lse, 0.7 * np.sum(q * k, -1), 1e-12, "W=1: L = scale q.k")
+    _close(dv, do, 1e-12, "W=1: dV = dO")
+    _close(dq, np.zeros_like(dq), 1e-12, "W=1: dQ = 0")
+    _close(dk, np.zeros_like(dk), 1e-12, "W=1: dK = 0")
+    for W in (33, 40):
+        ow, lw = orc.fwd(q, k, v, True, 0.7, window=W)
+        oc, lc = orc.fwd(q, k, v, True, 0.7)
+        _close(ow, oc, 1e-13, f"W={W} >= N: O as causal")
+        _close(lw, lc, 1e-13, f"W={W} >= N: L as causal")
+    for B, H, N, d, W in shapes:
+        scale = 1.0 / math.sqrt(d)
+        q, k, v, do = (_rand(rng, B, H, N, d) for _ in range(4))
+        i = np.arange(N)[:, None]
+        j = np.arange(N)[None, :]
+        band = torch.tensor((j <= i) & (i - j < W))
+        tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=band,
+                                                              scale=scale)
+        to.backward(torch.tensor(do, dtype=torch.float64))
+        o, _ = orc.fwd(q, k, v, True, scale, window=W)
+        dq, dk, dv, _ = orc.bwd(q, k, v, do, True, scale, window=W)
+        tag = f"{B, H, N, d} W={W}"
+        _close(o, to.detach().numpy(), 1e-10, f"window O vs SDPA {tag}")
+        _close(dq, tq.grad.numpy(), 1e-10, f"window dQ vs SDPA {tag}")
+        _close(dk, tk.grad.numpy(), 1e-10, f"window dK vs SDPA {tag}")
+        _close(dv, tv.grad.numpy(), 1e-10, f"window dV vs SDPA {tag}")
+
+
 def pin_page_sizes(iomodel):
     """Sizes the pages print (tests/golden/page_sizes.json) from the byte model."""
     with open(os.path.join(GOLDEN, "page_sizes.json")) as f:
@@ -306,4 +346,4 @@ def pin_page_sizes(iomodel):
 
 ORACLE_PINS = [pin_rows_sum_to_one, pin_constant_keys, pin_causal_first_row,
                pin_online_matches_safe, pin_L_is_logsumexp, pin_merge, pin_finite_differences,
-               pin_gradient_invariants, pin_torch_sdpa, pin_gqa]
+               pin_gradient_invariants, pin_torch_sdpa, pin_gqa, pin_window]

@@ -35,10 +35,17 @@ MUTANTS = {
     "online: alpha not applied to l": ("l = l * alpha + psum;", "l = l + psum;"),
     "online: alpha not applied to acc": ("for (int t = 0; t < d; ++t) acc[t] *= alpha;",
                                          "for (int t = 0; t < d; ++t) acc[t] *= 1.0;"),
+    "window starts one key early": (
+        "return (window > 0 && i - window + 1 > 0) ? i - window + 1 : 0;",
+        "return (window > 0 && i - window > 0) ? i - window : 0;"),
+    "window: key pass keeps one query too many": (
+        "if (window > 0 && i - j >= window) break;", "if (window > 0 && i - j > window) break;"),
     "merge: wrong weight": ("*l_out = a1 * l1 + a2 * l2;", "*l_out = a1 * l1 + a1 * l2;"),
     "scores transposed (k_i . q_j)": (
-        "double m = row_scores(q + (long)i * d, k, nk, d, scale, s, &l);\n                double* oi = o",
-        "double m = row_scores(k + (long)i * d, q, nk, d, scale, s, &l);\n                double* oi = o"),
+        "double m = row_scores(q + (long)i * d, k + (long)j0 * d, nk, d, scale, s, &l);\n"
+        "                double* oi = o",
+        "double m = row_scores(k + (long)i * d, q + (long)j0 * d, nk, d, scale, s, &l);\n"
+        "                double* oi = o"),
 }
 
 
