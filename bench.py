@@ -39,22 +39,25 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOP/s (N=8K,d=128,bf16,causal); % of GB300 tensor peak"
 WORKLOADS = {
-    # name: (B, H, N, d, dtype, causal[, Hkv]); Hkv < H: K/V heads shared by groups of
-    # H/Hkv query heads (grouped-query attention), same FLOPs as H independent heads
+    # name: (B, H, N, d, dtype, causal[, Hkv[, window]]); Hkv < H: K/V heads shared by
+    # groups of H/Hkv query heads (grouped-query attention), same FLOPs as H independent
+    # heads; window > 0: causal sliding window of that many keys
     "n8k_causal_d128_bf16": (1, 32, 8192, 128, "bf16", True),
     "n16k_causal_d128_bf16": (1, 32, 16384, 128, "bf16", True),
     "n4k_causal_d128_bf16": (2, 16, 4096, 128, "bf16", True),
     "n4k_full_d128_bf16": (2, 16, 4096, 128, "bf16", False),
     "gpt2m_causal_d64_fp16": (8, 16, 1024, 64, "fp16", True),
     "gqa8_n8k_causal_d128_bf16": (1, 32, 8192, 128, "bf16", True, 8),
+    "swa4k_gqa8_n16k_d128_bf16": (1, 32, 16384, 128, "bf16", True, 8, 4096),
 }
 
 
 def workload(name):
-    """(B, H, Hkv, N, d, dtype, causal) of a named workload."""
+    """(B, H, Hkv, N, d, dtype, causal, window) of a named workload."""
     w = WORKLOADS[name]
     B, H, N, d, dtype, causal = w[:6]
-    return B, H, (w[6] if len(w) > 6 else H), N, d, dtype, causal
+    return (B, H, (w[6] if len(w) > 6 else H), N, d, dtype, causal,
+            (w[7] if len(w) > 7 else 0))
 DEFAULT_WORKLOAD = "n8k_causal_d128_bf16"
 L2_BYTES = 129 * 1000 * 1000        # GB300 L2 (126 MiB)
 KERNEL_SOURCES = {
@@ -65,10 +68,15 @@ KERNEL_SOURCES = {
 }
 
 
-def attn_flops(B, H, N, d, causal):
-    f = 4.0 * B * H * N * N * d
-    if causal:
-        f *= 0.5
+def attn_flops(B, H, N, d, causal, window=0):
+    """(forward, backward) FLOPs: 4*d per (query, allowed key) pair forward, 2.5x that
+    backward.  Causal counts N^2/2 pairs (the usual halving); a sliding window of W < N
+    keys counts its exact pairs, W(W+1)/2 + (N-W)W."""
+    if window and window < N:
+        pairs = window * (window + 1) / 2 + (N - window) * window
+    else:
+        pairs = N * N * (0.5 if causal else 1.0)
+    f = 4.0 * B * H * pairs * d
     return f, 2.5 * f
 
 
@@ -187,20 +195,20 @@ def _head(flat, h, grp):
             for n in flat}
 
 
-def cpu_baseline(x, B, H, N, d, causal, scale, budget_s=10.0, max_heads=8):
+def cpu_baseline(x, B, H, N, d, causal, scale, budget_s=10.0, max_heads=8, window=0):
     """Time the fp64 oracle as it stands on the host cores over whole (batch, head) pairs
     of the workload until ``budget_s`` is spent (at least one pair)."""
     import numpy as np
     import oracle
-    fwd_f, bwd_f = attn_flops(1, 1, N, d, causal)
+    fwd_f, bwd_f = attn_flops(1, 1, N, d, causal, window)
     heads, t_total = 0, 0.0
     flat = {n: x[n].reshape(-1, N, d) for n in ("q", "k", "v", "do")}
     grp = H * B // flat["k"].shape[0]
     while heads < min(max_heads, B * H) and (heads == 0 or t_total < budget_s):
         sel = _head(flat, heads, grp)
         t0 = time.perf_counter()
-        oracle.fwd(sel["q"], sel["k"], sel["v"], causal, scale)
-        oracle.bwd(sel["q"], sel["k"], sel["v"], sel["do"], causal, scale)
+        oracle.fwd(sel["q"], sel["k"], sel["v"], causal, scale, window)
+        oracle.bwd(sel["q"], sel["k"], sel["v"], sel["do"], causal, scale, window)
         t_total += time.perf_counter() - t0
         heads += 1
     value = heads * (fwd_f + bwd_f) / t_total / 1e12
@@ -214,16 +222,16 @@ def run_reference(args, rank, world):
         return
     import oracle
     from exact_io_aware_22_gb300 import inputs
-    B, H, Hkv, N, d, dtype, causal = workload(args.workload)
+    B, H, Hkv, N, d, dtype, causal, window = workload(args.workload)
     scale = 1.0 / math.sqrt(d)
     x = inputs.make_inputs(B, H, N, d, dtype, seed=0, Hkv=Hkv)
     flat = {n: x[n].reshape(-1, N, d) for n in ("q", "k", "v", "do")}
-    fwd_f, bwd_f = attn_flops(1, 1, N, d, causal)
+    fwd_f, bwd_f = attn_flops(1, 1, N, d, causal, window)
 
     def step(i):
         sel = _head(flat, i % (B * H), H // Hkv)
-        oracle.fwd(sel["q"], sel["k"], sel["v"], causal, scale)
-        oracle.bwd(sel["q"], sel["k"], sel["v"], sel["do"], causal, scale)
+        oracle.fwd(sel["q"], sel["k"], sel["v"], causal, scale, window)
+        oracle.bwd(sel["q"], sel["k"], sel["v"], sel["do"], causal, scale, window)
 
     for i in range(args.warmup):
         step(i)
@@ -239,7 +247,7 @@ def run_reference(args, rank, world):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic",
            "config": {"workload": args.workload, "B": B, "H": H, "Hkv": Hkv, "N": N, "d": d,
-                      "causal": causal, "step_unit": "one (batch, head) pair"},
+                      "causal": causal, "window": window, "step_unit": "one (batch, head) pair"},
            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -256,9 +264,9 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    B, H, Hkv, N, d, dtype, causal = workload(args.workload)
+    B, H, Hkv, N, d, dtype, causal, window = workload(args.workload)
     scale = 1.0 / math.sqrt(d)
-    fwd_f, bwd_f = attn_flops(B, H, N, d, causal)
+    fwd_f, bwd_f = attn_flops(B, H, N, d, causal, window)
     x = inputs.make_inputs(B, H, N, d, dtype, seed=rank, Hkv=Hkv)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
@@ -268,8 +276,9 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def step():
-        fa.fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
-        fa.bwd(q, k, v, o, lse, do, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+        fa.fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse, window=window)
+        fa.bwd(q, k, v, o, lse, do, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+               window=window)
 
     def barrier():
         if world > 1:
@@ -393,7 +402,7 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(x, B, H, N, d, causal, scale)
+        cpu = cpu_baseline(x, B, H, N, d, causal, scale, window=window)
 
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -401,7 +410,8 @@ def run_ours(args, rank, world, local_rank):
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
                "data": "synthetic",
                "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d,
-                          "causal": causal, "Hkv": Hkv, "parallelism": f"replicas x{world}",
+                          "causal": causal, "Hkv": Hkv, "window": window,
+                          "parallelism": f"replicas x{world}",
                           "l2": l2_note},
                "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                "fwd_tflops": fwd_f / (fwd_ms / 1e3) / 1e12 if fwd_ms else None,

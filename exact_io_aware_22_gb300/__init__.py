@@ -65,6 +65,11 @@ def load_library(path: str | None = None):
     lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, i,
                                vp]
     lib.fa_bwd_gqa.restype = i
+    lib.fa_fwd_swa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_swa.restype = i
+    lib.fa_bwd_swa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, i,
+                               vp]
+    lib.fa_bwd_swa.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_cuda_error.restype = i
@@ -128,17 +133,27 @@ def _kv_heads(q, k, v) -> int:
     return Hkv
 
 
-def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=None):
+def _window(causal: bool, window: int) -> int:
+    if window < 0 or (window > 0 and not causal):
+        raise ValueError("window > 0 is a causal sliding window (causal=True)")
+    return int(window)
+
+
+def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=None,
+        window: int = 0):
     """O, L = attention(q, k, v) for (B, H, N, d) fp16/bf16 CUDA tensors.
 
     L is (B, H, N) fp32, the natural-log logsumexp of each row's scaled scores.
     k and v may have fewer heads, (B, Hkv, N, d) with H a multiple of Hkv: each
     group of H/Hkv consecutive query heads shares one K/V head (GQA; Hkv = 1 is MQA).
+    ``window`` > 0 (causal only) limits each query to the ``window`` most recent keys,
+    itself included (sliding-window attention).
     ``scale`` defaults to 1/sqrt(d).  Runs asynchronously on torch's current stream.
     """
     import torch
     _need_cuda(q, k, v)
     Hkv = _kv_heads(q, k, v)
+    window = _window(causal, window)
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share one dtype")
     B, H, N, d = q.shape
@@ -153,7 +168,10 @@ def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=
             or lse.dtype != torch.float32:
         raise ValueError("out must match q; lse must be (B, H, N) fp32")
     lib = load_library()
-    if Hkv == H:
+    if window > 0:
+        _check(lib.fa_fwd_swa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                              window, float(scale), _dtype_code(q), _stream()), "fa_fwd_swa")
+    elif Hkv == H:
         _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(causal),
                           float(scale), _dtype_code(q), _stream()), "fa_fwd")
     else:
@@ -167,18 +185,20 @@ def bwd_workspace_size(B: int, H: int, N: int, d: int, causal: bool = True) -> i
 
 
 def bwd(q, k, v, o, lse, do, causal: bool = True, scale: float | None = None,
-        dq=None, dk=None, dv=None, workspace=None):
+        dq=None, dk=None, dv=None, workspace=None, window: int = 0):
     """dQ, dK, dV of attention for upstream gradient ``do``.
 
     q, o, do, dq are (B, H, N, d); k, v, dk, dv are (B, Hkv, N, d) (Hkv = H unless
     K/V heads are shared, as in ``fwd``; a shared head's dK and dV sum over its
-    query heads).  ``o`` and ``lse`` are the forward's outputs.  ``workspace``
-    (optional) is a CUDA uint8 tensor of at least ``bwd_workspace_size`` bytes;
-    without it the library takes scratch from the stream-ordered allocator.
+    query heads; ``window`` as in ``fwd``).  ``o`` and ``lse`` are the forward's
+    outputs.  ``workspace`` (optional) is a CUDA uint8 tensor of at least
+    ``bwd_workspace_size`` bytes; without it the library takes scratch from the
+    stream-ordered allocator.
     """
     import torch
     _need_cuda(q, k, v, o, lse, do)
     Hkv = _kv_heads(q, k, v)
+    window = _window(causal, window)
     B, H, N, d = q.shape
     for t in (k, v, o, do):
         if t.dtype != q.dtype:
@@ -200,7 +220,11 @@ def bwd(q, k, v, o, lse, do, causal: bool = True, scale: float | None = None,
         _need_cuda(workspace)
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     lib = load_library()
-    if Hkv == H:
+    if window > 0:
+        _check(lib.fa_bwd_swa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                              _ptr(dk), _ptr(dv), ws_ptr, ws_bytes, B, H, Hkv, N, d, window,
+                              float(scale), _dtype_code(q), _stream()), "fa_bwd_swa")
+    elif Hkv == H:
         _check(lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                           _ptr(dk), _ptr(dv), ws_ptr, ws_bytes, B, H, N, d, int(causal),
                           float(scale), _dtype_code(q), _stream()), "fa_bwd")

@@ -257,7 +257,7 @@ static fa_status check_heads(int H, int Hkv) {
 
 static fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* L, int B,
                           int H, int Hkv, int N, int d, int causal, float scale, fa_dtype dtype,
-                          void* stream) {
+                          void* stream, int window = 0) {
   fa_status st = check_common(B, H, N, d, causal, scale, static_cast<int>(dtype));
   if (st != FA_OK) return st;
   if ((st = check_heads(H, Hkv)) != FA_OK) return st;
@@ -286,6 +286,7 @@ static fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, 
   a.N = N;
   a.BH = static_cast<int>(BH);
   a.group = H / Hkv;
+  a.window = window < N ? window : 0;           // a window of N or more keys is plain causal
   a.c_log2 = scale * 1.4426950408889634f;
   cudaError_t e = fa::launch_fwd(a, d, bf16, causal != 0, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -303,6 +304,13 @@ fa_status fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float
   return fwd_impl(Q, K, V, O, L, B, H, Hkv, N, d, causal, scale, dtype, stream);
 }
 
+fa_status fa_fwd_swa(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                     int Hkv, int N, int d, int window, float scale, fa_dtype dtype,
+                     void* stream) {
+  if (window < 1) return FA_ERR_INVALID_VALUE;
+  return fwd_impl(Q, K, V, O, L, B, H, Hkv, N, d, 1, scale, dtype, stream, window);
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
   if (check_common(B, H, N, d, causal, 1.0f, FA_FP16) != FA_OK) return 0;
   return fa::bwd_workspace_bytes(static_cast<long long>(B) * H, N, d);
@@ -311,7 +319,8 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
 static fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
                           const void* dO, const float* L, void* dQ, void* dK, void* dV,
                           void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
-                          int d, int causal, float scale, fa_dtype dtype, void* stream) {
+                          int d, int causal, float scale, fa_dtype dtype, void* stream,
+                          int window = 0) {
   fa_status st = check_common(B, H, N, d, causal, scale, static_cast<int>(dtype));
   if (st != FA_OK) return st;
   if ((st = check_heads(H, Hkv)) != FA_OK) return st;
@@ -367,6 +376,7 @@ static fa_status bwd_impl(const void* Q, const void* K, const void* V, const voi
   a.N = N;
   a.BH = static_cast<int>(BH);
   a.group = H / Hkv;
+  a.window = window < N ? window : 0;           // a window of N or more keys is plain causal
   a.scale = scale;
   a.c_log2 = scale * 1.4426950408889634f;
   cudaError_t e = fa::launch_bwd(a, d, bf16, causal != 0, s);
@@ -392,6 +402,15 @@ fa_status fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O,
                      float scale, fa_dtype dtype, void* stream) {
   return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, B, H, Hkv, N, d,
                   causal, scale, dtype, stream);
+}
+
+fa_status fa_bwd_swa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                     size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int window,
+                     float scale, fa_dtype dtype, void* stream) {
+  if (window < 1) return FA_ERR_INVALID_VALUE;
+  return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, B, H, Hkv, N, d, 1,
+                  scale, dtype, stream, window);
 }
 
 }  // extern "C"

@@ -125,8 +125,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dK,
-                void* __restrict__ dV, int N, int Np, int group, float scale, float c_log2,
-                KernelCtl ctl) {
+                void* __restrict__ dV, int N, int Np, int group, int window, float scale,
+                float c_log2, KernelCtl ctl) {
   using G = Geo<D>;
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -141,7 +141,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bkv = bp.bh;                    // K/V head; its query heads are bkv*group + g
   const int kb = bp.rank;                   // key block (causal: block 0 has the most work)
   const int i0 = CAUSAL ? kb : 0;           // BM == BN: the diagonal query block
-  const int n_head = nqb - i0;              // query blocks per query head
+  // query blocks per query head: from the diagonal to the last one that sees a key of
+  // this block (a window of W keys reaches query rows up to the block's last key + W - 1)
+  const int n_head = ((CAUSAL && window > 0) ? min(nqb, (kb * BN + BN - 1 + window - 1) / BM + 1)
+                                             : nqb) - i0;
   const int n_iter = group * n_head;        // every query head of the group in turn
 
   auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };
@@ -266,6 +269,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float4* L4 = reinterpret_cast<const float4*>(Lb + q0);
       const float4* D4 = reinterpret_cast<const float4*>(Db + q0);
       const bool diag = CAUSAL && qb == kb;
+      // window edge: zero where the query is W or more rows past the key
+      const bool wedge = CAUSAL && window > 0 && qb * BM + BM - 1 - kb * BN >= window;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {                       // 8 queries (16 bytes of dS^T) per step
         const float4 la = __ldg(L4 + 2 * u), lb = __ldg(L4 + 2 * u + 1);
@@ -278,6 +283,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int c = 8 * u + e;
           float pv = ex2(fmaf(__uint_as_float(s[c]), c_log2, -lq[e]));
           if (diag && q0 + c < gkey) pv = 0.f;
+          if (wedge && q0 + c - gkey >= window) pv = 0.f;
           p[e] = pv;
           ds[e] = pv * (__uint_as_float(dp[c]) - dq[e]);
         }
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dQ,
-              int N, int Np, int group, float scale, float c_log2, KernelCtl ctl) {
+              int N, int Np, int group, int window, float scale, float c_log2, KernelCtl ctl) {
   using G = Geo<D>;
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -374,7 +380,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const BlockPos bp = block_pos(nqb);
   const int bh = bp.bh;
   const int qb = nqb - 1 - bp.rank;                // causal: the last query blocks have the most work
-  const int n_iter = CAUSAL ? min(qb + 1, nkb) : nkb;
+  // key blocks j_lo .. diagonal (a window of W keys starts at the block holding the
+  // block's first row - W + 1); loop position it is key block j_lo + it
+  const int j_lo = (CAUSAL && window > 0) ? max(0, qb * BM - window + 1) / BN : 0;
+  const int n_iter = (CAUSAL ? min(qb + 1, nkb) : nkb) - j_lo;
 
   auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };
   const int B_QF = 0;
@@ -408,8 +417,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t ph = (it / G::STAGES) & 1;
         if (!(ok = mbar_wait(bar(B_KE(s)), ph ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_KF(s)), 2 * G::TILE_BYTES);
-        load_tile<D>(sb + C::K_OFF + s * G::TILE_BYTES, &tmK, bar(B_KF(s)), it * BN, bh / group);
-        load_tile<D>(sb + C::V_OFF + s * G::TILE_BYTES, &tmV, bar(B_KF(s)), it * BN, bh / group);
+        load_tile<D>(sb + C::K_OFF + s * G::TILE_BYTES, &tmK, bar(B_KF(s)), (j_lo + it) * BN,
+                     bh / group);
+        load_tile<D>(sb + C::V_OFF + s * G::TILE_BYTES, &tmV, bar(B_KF(s)), (j_lo + it) * BN,
+                     bh / group);
       }
       if (!ok) {
         mbar_wait(bar(B_QF), 0, ctl);
@@ -483,8 +494,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
-      const int k0 = it * BN + h * 64;
-      const bool diag = CAUSAL && it == qb;
+      const int k0 = (j_lo + it) * BN + h * 64;
+      const bool diag = CAUSAL && j_lo + it == qb;
+      const bool wedge = CAUSAL && window > 0 && qb * BM + BM - 1 - (j_lo + it) * BN >= window;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         float p0 = ex2(fmaf(__uint_as_float(s[2 * i]), c_log2, -lsub));
@@ -492,6 +504,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (diag) {
           if (k0 + 2 * i > grow) p0 = 0.f;
           if (k0 + 2 * i + 1 > grow) p1 = 0.f;
+        }
+        if (wedge) {
+          if (grow - (k0 + 2 * i) >= window) p0 = 0.f;
+          if (grow - (k0 + 2 * i + 1) >= window) p1 = 0.f;
         }
         const float ds0 = p0 * (__uint_as_float(dp[2 * i]) - dr);
         const float ds1 = p1 * (__uint_as_float(dp[2 * i + 1]) - dr);
@@ -558,8 +574,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     const long long grid = static_cast<long long>(nqb) * (a.BH / a.group);   // per K/V head
     trace_begin(TR_BWD_DKDV, st);
     kern<<<static_cast<unsigned>(grid), THREADS, DkdvCfg<D>::SMEM_BYTES, st>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.scale, a.c_log2,
-        a.ctl);
+        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.window, a.scale,
+        a.c_log2, a.ctl);
     trace_end(TR_BWD_DKDV, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -572,7 +588,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     const long long grid = static_cast<long long>(nqb) * a.BH;
     trace_begin(TR_BWD_DQ, st);
     kern<<<static_cast<unsigned>(grid), THREADS, DqCfg<D>::SMEM_BYTES, st>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.scale, a.c_log2, a.ctl);
+        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.window, a.scale,
+        a.c_log2, a.ctl);
     trace_end(TR_BWD_DQ, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                    const float* __restrict__ Dp, const float* __restrict__ Lp,
                    void* __restrict__ dK, void* __restrict__ dV, int N, int Np, int group,
-                   float scale, float c_log2, KernelCtl ctl) {
+                   int window, float scale, float c_log2, KernelCtl ctl) {
   using namespace kv;
   extern __shared__ __align__(1024) uint8_t sg[];
   const uint32_t sb = smem_u32(sg);
@@ -143,7 +143,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bkv = bp.bh;                           // K/V head; its query heads: bkv*group + g
   const int kb = bp.rank;                          // causal: block 0 has the most work
   const int q_start = CAUSAL ? kb : 0;             // the diagonal query tile
-  const int n_head = nq - q_start;                 // query tiles per query head
+  // query tiles per query head: from the diagonal to the last tile that sees a key of
+  // this block (with a window of W keys, query rows up to the block's last key + W - 1)
+  const int n_head = ((CAUSAL && window > 0) ? min(nq, (kb * BT + BT - 1 + window - 1) / BT + 1)
+                                             : nq) - q_start;
   const int n_iter = group * n_head;               // the group's query heads one after another
 
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
@@ -324,6 +327,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < 64; ++c)
           if (64 * h + c < kr) p[c] = 0.f;
       }
+      if (CAUSAL && window > 0 && (itl + 1) * BT - 1 >= window) {
+        // window edge: zero where the query is W or more rows past the key (query
+        // itl*BT + 64h + c and key kr, both relative to this key block's first row)
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (itl * BT + 64 * h + c - kr >= window) p[c] = 0.f;
+      }
       // dP^T of this tile (its MMAs follow the previous tile's dV and dK in the pipe)
       if (!(ok = mbar_wait_warp(bar(B_DPF), it & 1, ctl))) break;
       tc_fence_after();
@@ -434,7 +444,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     dq128_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmdO, const void* __restrict__ Q,
                  const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dQ,
-                 int N, int Np, int group, float scale, float c_log2, KernelCtl ctl) {
+                 int N, int Np, int group, int window, float scale, float c_log2,
+                 KernelCtl ctl) {
   using namespace qd;
   extern __shared__ __align__(1024) uint8_t sg[];
   const uint32_t sb = smem_u32(sg);
@@ -449,7 +460,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bh = bp.bh;
   const int qb = nqb - 1 - bp.rank;                // causal: the last query tiles have the most work
   const int bkv = bh / group;                      // the K/V head of this query head
-  const int n_iter = CAUSAL ? min(qb + 1, nkb) : nkb;
+  // key blocks j_lo .. diagonal; with a window of W keys, from the block holding the
+  // tile's first row - W + 1
+  const int j_lo = (CAUSAL && window > 0) ? max(0, qb * BT - window + 1) / BT : 0;
+  const int n_iter = (CAUSAL ? min(qb + 1, nkb) : nkb) - j_lo;   // loop position j: block j_lo + j
 
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
   const int B_DOF = 0;
@@ -489,8 +503,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!(ok = mbar_wait(bar(B_KE(s)), ((j / KV_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_KF(s)), 2 * TILE);
         for (int c = 0; c < 2; ++c) {
-          tma_load_3d(sb + K_OFF + s * TILE + c * CHUNK, &tmK, bar(B_KF(s)), c * 64, j * BT, bkv);
-          tma_load_3d(sb + V_OFF + s * TILE + c * CHUNK, &tmV, bar(B_KF(s)), c * 64, j * BT, bkv);
+          tma_load_3d(sb + K_OFF + s * TILE + c * CHUNK, &tmK, bar(B_KF(s)), c * 64,
+                      (j_lo + j) * BT, bkv);
+          tma_load_3d(sb + V_OFF + s * TILE + c * CHUNK, &tmV, bar(B_KF(s)), c * 64,
+                      (j_lo + j) * BT, bkv);
         }
       }
       if (!ok) {
@@ -594,7 +610,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float2 nd2 = make_float2(-dr, -dr);
     bool ok = n_iter > 0;
     for (int j = 0; ok && j < n_iter; ++j) {
-      const int k0 = j * BT + 64 * h;
+      const int k0 = (j_lo + j) * BT + 64 * h;    // first key of this thread's columns
       if (!(ok = mbar_wait_warp(bar(B_SF), j & 1, ctl))) break;
       tc_fence_after();
       uint32_t x[64];
@@ -613,10 +629,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         p[2 * i] = ex2(t.x);
         p[2 * i + 1] = ex2(t.y);
       }
-      if (CAUSAL && j == qb) {
+      if (CAUSAL && j_lo + j == qb) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (k0 + c > grow) p[c] = 0.f;
+      }
+      if (CAUSAL && window > 0 && qb * BT + BT - 1 - (j_lo + j) * BT >= window) {
+        // window edge: zero where the query is W or more rows past the key
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (grow - (k0 + c) >= window) p[c] = 0.f;
       }
       if (!(ok = mbar_wait_warp(bar(B_DPF), j & 1, ctl))) break;
       tc_fence_after();
@@ -671,8 +693,8 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DKDV, st);
     kern<<<static_cast<unsigned>(nblk_kv), THREADS, kv::SMEM_BYTES, st>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.scale, a.c_log2,
-        a.ctl);
+        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.window, a.scale,
+        a.c_log2, a.ctl);
     trace_end(TR_BWD_DKDV, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -684,7 +706,8 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DQ, st);
     kern<<<static_cast<unsigned>(nblk), THREADS, qd::SMEM_BYTES, st>>>(
-        a.tmK, a.tmV, a.tmdO, a.Q, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.scale, a.c_log2, a.ctl);
+        a.tmK, a.tmV, a.tmdO, a.Q, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.window, a.scale,
+        a.c_log2, a.ctl);
     trace_end(TR_BWD_DQ, st);
     return cudaGetLastError();
   }

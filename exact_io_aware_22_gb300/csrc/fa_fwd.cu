@@ -66,12 +66,12 @@ __device__ __forceinline__ uint32_t kmajor_koff(int kk) {
   return (e / C::ATOM) * C::CHUNK_BYTES + (e % C::ATOM) * 2;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, void* __restrict__ Out,
-               float* __restrict__ Lout, int N, int n_qblk, int group, float c_log2,
-               KernelCtl ctl) {
+               float* __restrict__ Lout, int N, int n_qblk, int group, int window,
+               float c_log2, KernelCtl ctl) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -85,15 +85,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bkv = bh / group;                   // the K/V head of this query head (b-major heads)
   const int row0 = qblk * (NT * BM);
   const int nkv = (N + BN - 1) / BN;
-  int n_t[NT];
+  // KV tiles [lo_t[t], n_t[t]) of Q tile t: up to the diagonal when causal; with a
+  // sliding window of W keys, from the tile holding key (first row - W + 1)
+  int n_t[NT], lo_t[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const int r = row0 + t * BM;
     if (r >= N) n_t[t] = 0;
     else if (CAUSAL) n_t[t] = min(nkv, min(r + BM - 1, N - 1) / BN + 1);
     else n_t[t] = nkv;
+    lo_t[t] = WINDOW ? max(0, r - window + 1) / BN : 0;
   }
+  const int j0 = lo_t[0];                       // the stream starts at tile 0's first KV tile
   const int n_max = max(n_t[0], n_t[1]);
+  const int n_stream = n_max - j0;              // KV tiles loaded, j0 .. n_max - 1
 
   auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };
   const int B_QF = 0;
@@ -127,27 +132,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_max > 0) {
+    if (lane == 0 && n_stream > 0) {
       bool ok = true;
       mbar_arrive_expect_tx(bar(B_QF), NT * C::TILE_BYTES);
       for (int t = 0; t < NT; ++t)
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(sb + C::Q_OFF + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, bar(B_QF),
                       c * C::ATOM, row0 + t * BM, bh);
-      int j = 0;
-      for (; j < n_max; ++j) {
+      int j = 0;                                // stream position: KV tile j0 + j
+      for (; j < n_stream; ++j) {
         const int s = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
+        const int krow = (j0 + j) * BN;
         if (!(ok = mbar_wait(bar(B_KE(s)), ph ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_KF(s)), C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(sb + C::K_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmK, bar(B_KF(s)),
-                      c * C::ATOM, j * BN, bkv);
+                      c * C::ATOM, krow, bkv);
         if (!(ok = mbar_wait(bar(B_VE(s)), ph ^ 1, ctl))) { ++j; break; }
         mbar_arrive_expect_tx(bar(B_VF(s)), C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(sb + C::V_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV, bar(B_VF(s)),
-                      c * C::ATOM, j * BN, bkv);
+                      c * C::ATOM, krow, bkv);
       }
       if (!ok) {
         // drain: wait (bounded) for every copy this thread issued, so no bulk
@@ -164,7 +170,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_max > 0) {
+    if (lane == 0 && n_stream > 0) {
       constexpr uint32_t idS = umma_idesc_f16(BM, BN, BF16, false, false);
       constexpr uint32_t idO = umma_idesc_f16(BM, D, BF16, false, true);
       // descriptor low words of Q tile 0 and of stage 0 of the K and V rings (K-major
@@ -193,24 +199,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < NT; ++t)
-          if (n_t[t] > 0) {
+          if (lo_t[t] == j0 && n_t[t] > j0) {
             issue_S(t, 0);
             umma_commit(bar(B_SF(t)));
           }
         umma_commit(bar(B_KE(0)));
       }
-      for (int j = 0; ok && j < n_max; ++j) {
-        const int s = j % C::STAGES;
-        const int s1 = (j + 1) % C::STAGES;
-        const uint32_t ph = (j / C::STAGES) & 1, ph1 = ((j + 1) / C::STAGES) & 1;
+      // stream position jj holds KV tile j = j0 + jj; Q tile t takes part while
+      // lo_t[t] <= j < n_t[t], its own iteration index being j - lo_t[t]
+      for (int jj = 0; ok && jj < n_stream; ++jj) {
+        const int j = j0 + jj;
+        const int s = jj % C::STAGES;
+        const int s1 = (jj + 1) % C::STAGES;
+        const uint32_t ph = (jj / C::STAGES) & 1, ph1 = ((jj + 1) / C::STAGES) & 1;
         if (!(ok = mbar_wait(bar(B_VF(s)), ph, ctl))) break;
         bool k_next = false;
         for (int t = 0; t < NT && ok; ++t) {
-          if (j >= n_t[t]) continue;
-          if (!(ok = mbar_wait(bar(B_PF(t)), j & 1, ctl))) break;
-          tc_fence_after();
-          issue_PV(t, s, j > 0);
-          if (j + 1 < n_t[t]) {
+          const bool in_t = j >= lo_t[t] && j < n_t[t];
+          if (in_t) {
+            if (!(ok = mbar_wait(bar(B_PF(t)), (j - lo_t[t]) & 1, ctl))) break;
+            tc_fence_after();
+            issue_PV(t, s, j > lo_t[t]);
+          }
+          if (j + 1 >= lo_t[t] && j + 1 < n_t[t]) {
             if (!k_next) {
               if (!(ok = mbar_wait(bar(B_KF(s1)), ph1, ctl))) break;
               tc_fence_after();
@@ -218,7 +229,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             issue_S(t, s1);
             umma_commit(bar(B_SF(t)));
-          } else {
+          } else if (in_t) {
             umma_commit(bar(B_OF(t)));
           }
         }
@@ -239,8 +250,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::S_COL + t * BN;
     const uint32_t tO = tmem + lane_off + C::O_COL + t * D;
-    const int nt = n_t[t];
+    const int nt = n_t[t] - lo_t[t];             // this tile's KV tiles, from lo_t[t]
     const int tile_row0 = row0 + t * BM;
+    const int lo_key = WINDOW ? grow - window + 1 : 0;   // first allowed key
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
@@ -255,14 +267,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
       tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-      const int kbase = j * BN;
-      // masks: causal on the diagonal tile only, key padding on the last tile
-      const bool need_mask = (CAUSAL && kbase + BN - 1 > tile_row0) || (kbase + BN > N);
+      const int kbase = (lo_t[t] + j) * BN;
+      // masks: causal on the diagonal tile, key padding on the last tile, and with a
+      // window the tiles reaching left of some row's first allowed key
+      const bool need_mask = (CAUSAL && kbase + BN - 1 > tile_row0) || (kbase + BN > N) ||
+                             (WINDOW && kbase < tile_row0 + BM - window);
       if (need_mask) {
-        const int lim = CAUSAL ? min(grow + 1, N) : N;   // keys < lim are allowed
+        const int lim = CAUSAL ? min(grow + 1, N) : N;   // keys in [lo_key, lim) are allowed
 #pragma unroll
         for (int c = 0; c < BN; ++c)
-          if (kbase + c >= lim) sr[c] = __float_as_uint(-INFINITY);
+          if (kbase + c >= lim || (WINDOW && kbase + c < lo_key)) sr[c] = __float_as_uint(-INFINITY);
       }
       // row maximum: four independent chains of 3-input max
       float mc[4];
@@ -356,10 +370,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool WINDOW>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = fwd_kernel<D, BF16, CAUSAL>;
+  auto kern = fwd_kernel<D, BF16, CAUSAL, WINDOW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -368,7 +382,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   trace_begin(TR_FWD, st);
   kern<<<static_cast<unsigned>(grid), THREADS, C::SMEM_BYTES, st>>>(
-      a.tmQ, a.tmK, a.tmV, a.O, a.L, a.N, n_qblk, a.group, a.c_log2, a.ctl);
+      a.tmQ, a.tmK, a.tmV, a.O, a.L, a.N, n_qblk, a.group, a.window, a.c_log2, a.ctl);
   trace_end(TR_FWD, st);
   return cudaGetLastError();
 }
@@ -384,14 +398,21 @@ FwdTileInfo fwd_tile_info(int d) {
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
-#define FA_FWD_CASE(DD, BB, CC) \
-  if (d == DD && bf16 == BB && causal == CC) return launch_fwd_t<DD, BB, CC>(a, st);
-  FA_FWD_CASE(32, false, false) FA_FWD_CASE(32, false, true)
-  FA_FWD_CASE(32, true, false) FA_FWD_CASE(32, true, true)
-  FA_FWD_CASE(64, false, false) FA_FWD_CASE(64, false, true)
-  FA_FWD_CASE(64, true, false) FA_FWD_CASE(64, true, true)
-  FA_FWD_CASE(128, false, false) FA_FWD_CASE(128, false, true)
-  FA_FWD_CASE(128, true, false) FA_FWD_CASE(128, true, true)
+  // a sliding window is causal; the windowed kernels are separate instantiations so
+  // that the plain ones carry none of its bookkeeping
+  const bool window = causal && a.window > 0;
+#define FA_FWD_CASE(DD, BB, CC, WW)                                \
+  if (d == DD && bf16 == BB && causal == CC && window == WW) \
+    return launch_fwd_t<DD, BB, CC, WW>(a, st);
+  FA_FWD_CASE(32, false, false, false) FA_FWD_CASE(32, false, true, false)
+  FA_FWD_CASE(32, true, false, false) FA_FWD_CASE(32, true, true, false)
+  FA_FWD_CASE(64, false, false, false) FA_FWD_CASE(64, false, true, false)
+  FA_FWD_CASE(64, true, false, false) FA_FWD_CASE(64, true, true, false)
+  FA_FWD_CASE(128, false, false, false) FA_FWD_CASE(128, false, true, false)
+  FA_FWD_CASE(128, true, false, false) FA_FWD_CASE(128, true, true, false)
+  FA_FWD_CASE(32, false, true, true) FA_FWD_CASE(32, true, true, true)
+  FA_FWD_CASE(64, false, true, true) FA_FWD_CASE(64, true, true, true)
+  FA_FWD_CASE(128, false, true, true) FA_FWD_CASE(128, true, true, true)
 #undef FA_FWD_CASE
   return cudaErrorInvalidValue;
 }

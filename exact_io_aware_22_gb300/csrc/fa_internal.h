@@ -37,6 +37,7 @@ struct FwdArgs {
   float* L;
   int N, BH;
   int group;                   // query heads per K/V head (H / Hkv; 1 without sharing)
+  int window;                  // causal sliding window of this many keys (0: none)
   float c_log2;                // scale * log2(e)
   KernelCtl ctl;
 };
@@ -54,6 +55,7 @@ struct BwdArgs {
   void* dV;
   int N, BH;                   // BH = B*H query heads
   int group;                   // query heads per K/V head; B*H/group K/V heads
+  int window;                  // causal sliding window of this many keys (0: none)
   float scale, c_log2;
   KernelCtl ctl;
 };

@@ -99,6 +99,22 @@ fa_status fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O,
                      size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int causal,
                      float scale, fa_dtype dtype, void* stream);
 
+/* Sliding-window (local) attention: causal, each query sees only the `window`
+ * most recent keys, itself included: key j is allowed for query i iff
+ * i - window < j <= i.  The docs page lists sliding windows among the features its
+ * kernels do not have yet ("Scope") and fixes no convention; this causal band is
+ * the plain reading.  Hkv as for fa_fwd_gqa (Hkv == H: no sharing).  window >=
+ * N is plain causal attention.  Only the KV tiles inside the band are computed.
+ *   Errors   as fa_fwd_gqa / fa_bwd_gqa, plus FA_ERR_INVALID_VALUE for window < 1.
+ *   Workspace of fa_bwd_swa: fa_bwd_workspace_size(B, H, N, d, 1), or NULL. */
+fa_status fa_fwd_swa(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                     int Hkv, int N, int d, int window, float scale, fa_dtype dtype,
+                     void* stream);
+fa_status fa_bwd_swa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                     size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int window,
+                     float scale, fa_dtype dtype, void* stream);
+
 /* Static description of a status code. */
 const char* fa_status_string(fa_status s);
 

@@ -30,11 +30,11 @@ TOL_L = 1e-4
 TOL_G = {"fp16": 1e-2, "bf16": 3e-2}
 
 
-def gpu_fwd_bwd(x: dict, causal: bool, scale: float, device="cuda"):
+def gpu_fwd_bwd(x: dict, causal: bool, scale: float, device="cuda", window: int = 0):
     import exact_io_aware_22_gb300 as fa
     q, k, v, do = (x[n].to(device) for n in ("q", "k", "v", "do"))
-    o, lse = fa.fwd(q, k, v, causal=causal, scale=scale)
-    dq, dk, dv = fa.bwd(q, k, v, o, lse, do, causal=causal, scale=scale)
+    o, lse = fa.fwd(q, k, v, causal=causal, scale=scale, window=window)
+    dq, dk, dv = fa.bwd(q, k, v, o, lse, do, causal=causal, scale=scale, window=window)
     torch.cuda.synchronize()
     assert fa.device_status() == 0, "a kernel reported a bounded-wait timeout"
     return {n: t.float().cpu() for n, t in
@@ -49,19 +49,21 @@ def _sel(t: torch.Tensor, heads):
     return flat[list(heads)].unsqueeze(0)
 
 
-def compare(B, H, N, d, dtype, causal, qk_std=1.0, heads=None, seed=0, scale=None, Hkv=None):
+def compare(B, H, N, d, dtype, causal, qk_std=1.0, heads=None, seed=0, scale=None, Hkv=None,
+            window=0):
     """Run the CUDA path on the whole problem and the oracle on ``heads`` (flat b*H+h
     indices; None = all).  Returns the error report; asserts the tolerances.
 
     With ``Hkv`` (K/V heads shared by groups of H/Hkv query heads) ``heads`` lists
-    flat K/V head indices b*Hkv+j, and each is compared with all its query heads."""
+    flat K/V head indices b*Hkv+j, and each is compared with all its query heads.
+    ``window`` > 0: causal sliding window of that many keys."""
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     x = inputs.make_inputs(B, H, N, d, dtype, seed=seed, qk_std=qk_std, Hkv=Hkv)
-    g = gpu_fwd_bwd(x, causal, scale)
+    g = gpu_fwd_bwd(x, causal, scale, window=window)
     if Hkv is None:
         q, k, v, do = (_sel(x[n].double(), heads).numpy() for n in ("q", "k", "v", "do"))
-        o_ref, l_ref = oracle.fwd(q, k, v, causal, scale)
-        dq_ref, dk_ref, dv_ref, _ = oracle.bwd(q, k, v, do, causal, scale)
+        o_ref, l_ref = oracle.fwd(q, k, v, causal, scale, window)
+        dq_ref, dk_ref, dv_ref, _ = oracle.bwd(q, k, v, do, causal, scale, window)
         qheads = kvheads = heads
     else:
         grp = H // Hkv
@@ -71,8 +73,8 @@ def compare(B, H, N, d, dtype, causal, qk_std=1.0, heads=None, seed=0, scale=Non
         k, v = (_sel(x[n].double(), kvheads).numpy() for n in ("k", "v"))
         if heads is not None:   # the selected groups as one batch of len(heads) K/V heads
             q, do = (t.reshape(1, len(heads) * grp, N, d) for t in (q, do))
-        o_ref, l_ref = oracle.fwd_gqa(q, k, v, causal, scale)
-        dq_ref, dk_ref, dv_ref, _ = oracle.bwd_gqa(q, k, v, do, causal, scale)
+        o_ref, l_ref = oracle.fwd_gqa(q, k, v, causal, scale, window)
+        dq_ref, dk_ref, dv_ref, _ = oracle.bwd_gqa(q, k, v, do, causal, scale, window)
     rep = {}
     # size of one dS_ij * k_j term: scale * max|dP| * max|k|, with |dP| <= |dO| |v|
     term = scale * float(np.max(np.linalg.norm(do, axis=-1)) * np.max(np.linalg.norm(v, axis=-1))

@@ -134,6 +134,20 @@ def test_gqa_rejects_like_mha(lib):
     assert bwd_gqa(lib, 4, ws_bytes=16) == INVALID
 
 
+@pytest.mark.parametrize("window", [0, -1, -128])
+def test_sliding_window_rejects_empty_windows(lib, window):
+    a = [ctypes.c_void_p(M1 * i) for i in range(1, 6)]
+    assert lib.fa_fwd_swa(*a, 1, 8, 2, 128, 64, window, 0.125, 1, None) == INVALID
+    b = [ctypes.c_void_p(M1 * i) for i in range(1, 11)]
+    assert lib.fa_bwd_swa(*b, 1 << 20, 1, 8, 2, 128, 64, window, 0.125, 1, None) == INVALID
+
+
+def test_sliding_window_checks_heads(lib):
+    a = [ctypes.c_void_p(M1 * i) for i in range(1, 6)]
+    assert lib.fa_fwd_swa(*a, 1, 8, 3, 128, 64, 16, 0.125, 1, None) == INVALID
+    assert lib.fa_fwd_swa(*a, 1, 8, 2, 128, 48, 16, 0.125, 1, None) == UNSUPPORTED
+
+
 def test_workspace_size(lib):
     f = lib.fa_bwd_workspace_size
     # D and L*log2(e), fp32, padded to 128-row blocks

@@ -77,3 +77,29 @@ def test_gqa_full_size_sampled():
     # 1 x 32 query heads x 8 K/V heads x 8192 x 128, bf16 causal; K/V heads 0 and 7, each
     # with its four query heads, compared in full
     print(compare(1, 32, 8192, 128, "bf16", True, heads=(0, 7), Hkv=8))
+
+
+# Causal sliding window of W keys: (B, H, Hkv, N, d, dtype, W)
+WINDOW_CASES = [
+    (1, 2, 2, 300, 128, "bf16", 1),          # every row sees only itself
+    (1, 2, 2, 300, 128, "bf16", 64),
+    (1, 2, 2, 256, 128, "fp16", 128),        # window of exactly one tile
+    (1, 2, 2, 257, 128, "fp16", 127),
+    (2, 2, 2, 1000, 64, "fp16", 200),
+    (1, 2, 2, 383, 32, "bf16", 100),
+    (1, 4, 2, 517, 128, "bf16", 129),        # with shared K/V heads
+    (1, 2, 2, 700, 128, "bf16", 333),
+    (1, 2, 2, 300, 64, "bf16", 5000),        # window longer than N: plain causal
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=[str(c) for c in WINDOW_CASES])
+def test_sliding_window(case):
+    B, H, Hkv, N, d, dt, W = case
+    print(case, compare(B, H, N, d, dt, True, seed=13, Hkv=None if Hkv == H else Hkv, window=W))
+
+
+def test_sliding_window_full_size_sampled():
+    # 1 x 32 query heads x 8 K/V heads x 16384 x 128, bf16, window 4096; K/V heads 0 and 7
+    # compared in full with their query heads
+    print(compare(1, 32, 16384, 128, "bf16", True, heads=(0, 7), Hkv=8, window=4096))
