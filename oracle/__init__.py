@@ -17,6 +17,11 @@ Contents
     consecutive query heads.  Defined as the plain attention of every query head
     with its group's K/V head; the gradient of a shared head is the sum over the
     query heads that read it (chain rule).
+  * ``fwd_varlen``/``bwd_varlen``: variable-length batches (docs page "Scope":
+    not yet): sequences of different lengths packed one after another, Q/O/dO
+    (total, H, d), K/V (total, Hkv, d), L (H, total), sequence b holding tokens
+    cu_seqlens[b] .. cu_seqlens[b+1]-1.  Defined as attention of every sequence
+    on its own, no token seeing another sequence's keys.
   * ``window`` (fwd, bwd and the GQA pair): a causal sliding window of W keys,
     query i seeing keys i - W < j <= i (docs page "Scope" lists sliding windows
     as not yet supported and fixes no convention; this is the plain reading).
@@ -135,6 +140,38 @@ class Oracle:
         return (dq, dk.reshape(B, Hkv, g, N, d).sum(axis=2), dv.reshape(B, Hkv, g, N, d).sum(axis=2),
                 D)
 
+    def fwd_varlen(self, q, k, v, cu_seqlens, causal: bool, scale: float, window: int = 0):
+        """O (total, H, d), L (H, total) for packed sequences (K, V: (total, Hkv, d))."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        total, H, d = q.shape
+        o = np.zeros_like(q)
+        lse = np.full((H, total), -np.inf)
+        for b in range(len(cu_seqlens) - 1):
+            a, e = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+            if e == a:
+                continue
+            qs, ks, vs = (x[a:e].transpose(1, 0, 2)[None] for x in (q, k, v))
+            ob, lb = self.fwd_gqa(qs, ks, vs, causal, scale, window)
+            o[a:e] = ob[0].transpose(1, 0, 2)
+            lse[:, a:e] = lb[0]
+        return o, lse
+
+    def bwd_varlen(self, q, k, v, do, cu_seqlens, causal: bool, scale: float, window: int = 0):
+        """dQ (total, H, d), dK, dV (total, Hkv, d) and D (H, total) for packed sequences."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+        total, H, d = q.shape
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        D = np.zeros((H, total))
+        for b in range(len(cu_seqlens) - 1):
+            a, e = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+            if e == a:
+                continue
+            qs, ks, vs, dos = (x[a:e].transpose(1, 0, 2)[None] for x in (q, k, v, do))
+            gq, gk, gv, Db = self.bwd_gqa(qs, ks, vs, dos, causal, scale, window)
+            dq[a:e], dk[a:e], dv[a:e] = (g[0].transpose(1, 0, 2) for g in (gq, gk, gv))
+            D[:, a:e] = Db[0]
+        return dq, dk, dv, D
+
     def fwd_online(self, q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):
         """O, L by the per-tile online update (docs page Fig. 3), key tiles of ``tile``."""
         q, k, v = _f64(q), _f64(k), _f64(v)
@@ -198,6 +235,14 @@ def fwd_gqa(q, k, v, causal: bool, scale: float, window: int = 0):
 
 def bwd_gqa(q, k, v, do, causal: bool, scale: float, window: int = 0):
     return get().bwd_gqa(q, k, v, do, causal, scale, window)
+
+
+def fwd_varlen(q, k, v, cu_seqlens, causal: bool, scale: float, window: int = 0):
+    return get().fwd_varlen(q, k, v, cu_seqlens, causal, scale, window)
+
+
+def bwd_varlen(q, k, v, do, cu_seqlens, causal: bool, scale: float, window: int = 0):
+    return get().bwd_varlen(q, k, v, do, cu_seqlens, causal, scale, window)
 
 
 def fwd_online(q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):

@@ -329,6 +329,50 @@ def pin_window(orc, shapes=((1, 2, 70, 16, 5), (2, 1, 130, 8, 17), (1, 2, 64, 8,
         _close(dv, tv.grad.numpy(), 1e-10, f"window dV vs SDPA {tag}")
 
 
+def pin_varlen(orc):
+    """Variable-length batches.  Library special case: the packed sequence as one
+    attention problem under a block-diagonal mask (each token sees only its own
+    sequence's keys; causal or a sliding window inside the block), torch's
+    scaled_dot_product_attention in fp64 with autograd; shared K/V heads through
+    enable_gqa.  Empty sequences contribute nothing."""
+    import torch
+    rng = np.random.default_rng(12)
+    for lens, H, Hkv, d, causal, W in (((5, 17, 1, 40), 2, 2, 8, True, 0),
+                                       ((33, 0, 20), 4, 2, 8, False, 0),
+                                       ((64, 70, 3), 2, 1, 16, True, 9)):
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        T = int(cu[-1])
+        q, do = _rand(rng, T, H, d), _rand(rng, T, H, d)
+        k, v = _rand(rng, T, Hkv, d), _rand(rng, T, Hkv, d)
+        seg = np.repeat(np.arange(len(lens)), lens)
+        i, j = np.arange(T)[:, None], np.arange(T)[None, :]
+        allow = seg[:, None] == seg[None, :]
+        if causal:
+            allow &= j <= i
+        if W:
+            allow &= i - j < W
+        scale = 1.0 / math.sqrt(d)
+        tq, tk, tv = (torch.tensor(x.transpose(1, 0, 2)[None], dtype=torch.float64,
+                                   requires_grad=True) for x in (q, k, v))
+        to = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk, tv, attn_mask=torch.tensor(allow), scale=scale, enable_gqa=Hkv != H)
+        to.backward(torch.tensor(do.transpose(1, 0, 2)[None], dtype=torch.float64))
+        o, lse = orc.fwd_varlen(q, k, v, cu, causal, scale, W)
+        dq, dk, dv, _ = orc.bwd_varlen(q, k, v, do, cu, causal, scale, W)
+        tag = f"lens={lens} H={H} Hkv={Hkv} causal={causal} W={W}"
+        back = lambda t: t.detach().numpy()[0].transpose(1, 0, 2)
+        _close(o, back(to), 1e-10, f"varlen O vs SDPA {tag}")
+        _close(dq, back(tq.grad), 1e-10, f"varlen dQ vs SDPA {tag}")
+        _close(dk, back(tk.grad), 1e-10, f"varlen dK vs SDPA {tag}")
+        _close(dv, back(tv.grad), 1e-10, f"varlen dV vs SDPA {tag}")
+        # L of every token: the logsumexp of its allowed scaled scores
+        s_ = np.einsum("ihc,jhc->hij", q, np.repeat(k, H // Hkv, axis=1)) * scale
+        s_ = np.where(allow[None], s_, -np.inf)
+        mx = s_.max(-1, keepdims=True)
+        _close(lse, (mx + np.log(np.exp(s_ - mx).sum(-1, keepdims=True)))[..., 0], 1e-11,
+               f"varlen L {tag}")
+
+
 def pin_page_sizes(iomodel):
     """Sizes the pages print (tests/golden/page_sizes.json) from the byte model."""
     with open(os.path.join(GOLDEN, "page_sizes.json")) as f:
@@ -346,4 +390,4 @@ def pin_page_sizes(iomodel):
 
 ORACLE_PINS = [pin_rows_sum_to_one, pin_constant_keys, pin_causal_first_row,
                pin_online_matches_safe, pin_L_is_logsumexp, pin_merge, pin_finite_differences,
-               pin_gradient_invariants, pin_torch_sdpa, pin_gqa, pin_window]
+               pin_gradient_invariants, pin_torch_sdpa, pin_gqa, pin_window, pin_varlen]

@@ -84,6 +84,9 @@ def test_mutant_is_caught(name, tmp_path):
 # real compiled core.
 PY_SRC = os.path.join(os.path.dirname(oracle.__file__), "__init__.py")
 GQA_MUTANTS = {
+    "varlen: a sequence sees the next one's first key": (
+        "qs, ks, vs = (x[a:e].transpose(1, 0, 2)[None] for x in (q, k, v))",
+        "qs, ks, vs = (x[a:min(e + 1, total)].transpose(1, 0, 2)[None] for x in (q, k, v))"),
     "GQA: dK averaged over the group": (
         "return (dq, dk.reshape(B, Hkv, g, N, d).sum(axis=2),",
         "return (dq, dk.reshape(B, Hkv, g, N, d).mean(axis=2),"),
@@ -104,5 +107,8 @@ def test_gqa_mutant_is_caught(name):
     ns = {"__name__": "oracle_mutant", "__file__": PY_SRC}
     exec(compile(text.replace(before, after), "oracle_mutant", "exec"), ns)
     orc = ns["Oracle"](oracle.build())
-    with pytest.raises(AssertionError):
-        pins.pin_gqa(orc, shapes=((1, 4, 2, 21, 8, True),))
+    with pytest.raises((AssertionError, ValueError)):
+        if name.startswith("varlen"):
+            pins.pin_varlen(orc)
+        else:
+            pins.pin_gqa(orc, shapes=((1, 4, 2, 21, 8, True),))
