@@ -50,6 +50,17 @@ WORKLOADS = {
     "gqa8_n8k_causal_d128_bf16": (1, 32, 8192, 128, "bf16", True, 8),
     "swa4k_gqa8_n16k_d128_bf16": (1, 32, 16384, 128, "bf16", True, 8, 4096),
 }
+# packed variable-length batches: name: (sequences, min len, max len, H, Hkv, d, dtype,
+# causal); lengths uniform in [min, max] from a fixed seed
+VARLEN_WORKLOADS = {
+    "varlen64_gqa8_d128_bf16": (64, 256, 8192, 32, 8, 128, "bf16", True),
+}
+
+
+def varlen_lengths(name):
+    import numpy as np
+    n, lo, hi = VARLEN_WORKLOADS[name][:3]
+    return [int(x) for x in np.random.default_rng(2026).integers(lo, hi + 1, n)]
 
 
 def workload(name):
@@ -103,7 +114,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=list(WORKLOADS) + list(VARLEN_WORKLOADS),
+                    default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -264,18 +276,39 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    B, H, Hkv, N, d, dtype, causal, window = workload(args.workload)
+    varlen = args.workload in VARLEN_WORKLOADS
+    if varlen:
+        _, _, _, H, Hkv, d, dtype, causal = VARLEN_WORKLOADS[args.workload]
+        lens = varlen_lengths(args.workload)
+        B, N, window = len(lens), max(lens), 0
+        fwd_f = bwd_f = 0.0
+        for n_b in lens:
+            f1, b1 = attn_flops(1, H, n_b, d, causal)
+            fwd_f, bwd_f = fwd_f + f1, bwd_f + b1
+        x = inputs.make_packed_inputs(lens, H, d, dtype, seed=rank, Hkv=Hkv)
+        cu = x["cu_seqlens"].to(dev)
+        lse_shape = (H, int(sum(lens)))
+        ws_bytes = int(fa.load_library().fa_bwd_varlen_workspace_size(B, N, H, d))
+    else:
+        B, H, Hkv, N, d, dtype, causal, window = workload(args.workload)
+        fwd_f, bwd_f = attn_flops(B, H, N, d, causal, window)
+        x = inputs.make_inputs(B, H, N, d, dtype, seed=rank, Hkv=Hkv)
+        lse_shape = (B, H, N)
+        ws_bytes = fa.bwd_workspace_size(B, H, N, d, causal)
     scale = 1.0 / math.sqrt(d)
-    fwd_f, bwd_f = attn_flops(B, H, N, d, causal, window)
-    x = inputs.make_inputs(B, H, N, d, dtype, seed=rank, Hkv=Hkv)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(fa.bwd_workspace_size(B, H, N, d, causal), dtype=torch.uint8, device=dev)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
+        if varlen:
+            fa.fwd_varlen(q, k, v, cu, N, causal=causal, scale=scale, out=o, lse=lse)
+            fa.bwd_varlen(q, k, v, o, lse, do, cu, N, causal=causal, scale=scale, dq=dq, dk=dk,
+                          dv=dv, workspace=ws)
+            return
         fa.fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse, window=window)
         fa.bwd(q, k, v, o, lse, do, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws,
                window=window)
@@ -343,14 +376,14 @@ def run_ours(args, rank, world, local_rank):
     peaks = load_peaks()
     # algorithmic work of one launch of each kernel
     elem = 2
-    n_bytes = B * H * N * d * elem
+    n_bytes = q.numel() * elem
     Np = (N + 127) // 128 * 128
     alg = {
         "fwd_kernel": ("tensor", fwd_f),
         "bwd_dkdv_kernel": ("tensor", 0.8 * bwd_f),     # S, dP recompute, dV, dK: 4 of 5 products
         "bwd_dq_kernel": ("tensor", 0.2 * bwd_f),       # dQ: 1 of 5 products (S, dP recomputed)
         # reads O, dO, L; writes D and L*log2e
-        "bwd_pre_kernel": ("hbm", 2 * n_bytes + 4 * B * H * N + 2 * 4 * B * H * Np),
+        "bwd_pre_kernel": ("hbm", 2 * n_bytes + 4 * lse.numel() + 2 * 4 * B * H * Np),
     }
     top = max(traced, key=lambda kk: traced[kk][0])
     bound, work = alg[top]
@@ -402,7 +435,7 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(x, B, H, N, d, causal, scale, window=window)
+        cpu = None if varlen else cpu_baseline(x, B, H, N, d, causal, scale, window=window)
 
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -412,7 +445,10 @@ def run_ours(args, rank, world, local_rank):
                "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d,
                           "causal": causal, "Hkv": Hkv, "window": window,
                           "parallelism": f"replicas x{world}",
-                          "l2": l2_note},
+                          "l2": l2_note,
+                          **({"packed_tokens": int(q.shape[0]), "max_seqlen": N,
+                              "lengths": "uniform 256..8192, 64 sequences, seed 2026"}
+                             if varlen else {})},
                "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                "fwd_tflops": fwd_f / (fwd_ms / 1e3) / 1e12 if fwd_ms else None,
                "bwd_tflops": bwd_f / (bwd_ms / 1e3) / 1e12 if bwd_ms else None,

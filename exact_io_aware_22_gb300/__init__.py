@@ -70,6 +70,13 @@ def load_library(path: str | None = None):
     lib.fa_bwd_swa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, i,
                                vp]
     lib.fa_bwd_swa.restype = i
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_varlen.restype = i
+    lib.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_varlen_workspace_size.restype = sz
+    lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, i, i, i, i, i, i,
+                                  i, i, f, i, vp]
+    lib.fa_bwd_varlen.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_cuda_error.restype = i
@@ -232,6 +239,74 @@ def bwd(q, k, v, o, lse, do, causal: bool = True, scale: float | None = None,
         _check(lib.fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                               _ptr(dk), _ptr(dv), ws_ptr, ws_bytes, B, H, Hkv, N, d, int(causal),
                               float(scale), _dtype_code(q), _stream()), "fa_bwd_gqa")
+    return dq, dk, dv
+
+
+def _packed(q, k, v, cu_seqlens):
+    """(B, total, H, Hkv, d) of packed sequences q (total, H, d), k, v (total, Hkv, d)."""
+    import torch
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape:
+        raise ValueError("packed q must be (total, H, d) and k, v one (total, Hkv, d) shape")
+    total, H, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape[0] != total or k.shape[2] != d or Hkv < 1 or H % Hkv:
+        raise ValueError("k, v must be (total, Hkv, d) with H a multiple of Hkv")
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor of B+1 offsets")
+    return cu_seqlens.numel() - 1, total, H, Hkv, d
+
+
+def fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = True,
+               scale: float | None = None, window: int = 0, out=None, lse=None):
+    """O, L of packed variable-length sequences: q (total, H, d), k and v (total, Hkv, d),
+    sequence b at rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (int32 CUDA tensor, B+1
+    entries), each attending only to its own keys; max_seqlen bounds every length.
+    L is (H, total) fp32.  ``window`` and shared K/V heads as in ``fwd``."""
+    import torch
+    _need_cuda(q, k, v, cu_seqlens)
+    B, total, H, Hkv, d = _packed(q, k, v, cu_seqlens)
+    window = _window(causal, window)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need_cuda(out, lse)
+    if out.shape != q.shape or out.dtype != q.dtype or lse.shape != (H, total) \
+            or lse.dtype != torch.float32:
+        raise ValueError("out must match q; lse must be (H, total) fp32")
+    _check(load_library().fa_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens), B, total,
+        int(max_seqlen), H, Hkv, d, int(causal), window, float(scale), _dtype_code(q), _stream()),
+        "fa_fwd_varlen")
+    return out, lse
+
+
+def bwd_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen: int, causal: bool = True,
+               scale: float | None = None, window: int = 0, dq=None, dk=None, dv=None,
+               workspace=None):
+    """dQ (total, H, d), dK, dV (total, Hkv, d) of packed variable-length sequences (see
+    ``fwd_varlen``); ``o`` and ``lse`` are its outputs.  ``workspace``: optional CUDA
+    uint8 tensor of fa_bwd_varlen_workspace_size bytes."""
+    import torch
+    _need_cuda(q, k, v, o, lse, do, cu_seqlens)
+    B, total, H, Hkv, d = _packed(q, k, v, cu_seqlens)
+    window = _window(causal, window)
+    if o.shape != q.shape or do.shape != q.shape or lse.shape != (H, total):
+        raise ValueError("o and do must match q; lse must be (H, total)")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _need_cuda(dq, dk, dv)
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        _need_cuda(workspace)
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    _check(load_library().fa_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        ws_ptr, ws_bytes, _ptr(cu_seqlens), B, total, int(max_seqlen), H, Hkv, d, int(causal),
+        window, float(scale), _dtype_code(q), _stream()), "fa_bwd_varlen")
     return dq, dk, dv
 
 

@@ -87,6 +87,29 @@ fa_status make_map(CUtensorMap* m, const void* base, int d, int N, long long BH,
   return FA_OK;
 }
 
+// 3-D map (d, Hx, total) over packed sequences (total, Hx, d): box = one head of one
+// 128-row tile of one swizzle width, laid out in shared memory as make_map's tile.
+// Rows >= total read as zeros.
+fa_status make_map_packed(CUtensorMap* m, const void* base, int d, int Hx, int total, bool bf16) {
+  EncodeTiledFn enc;
+  fa_status st = get_encoder(&enc);
+  if (st != FA_OK) return st;
+  const fa::FwdTileInfo ti = fa::fwd_tile_info(d);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hx),
+                        static_cast<cuuint64_t>(total)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(Hx) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(ti.box_cols), 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   ti.swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return FA_OK;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -255,18 +278,29 @@ static fa_status check_heads(int H, int Hkv) {
   return FA_OK;
 }
 
+// Packed variable-length sequences (cu_seqlens != NULL): N is the longest sequence,
+// `total` the packed row count; Q, O (total, H, d), K, V (total, Hkv, d), L (H, total).
+static fa_status check_packed(const int* cu_seqlens, int total) {
+  if (!cu_seqlens || total < 1) return FA_ERR_INVALID_VALUE;
+  if (!aligned(cu_seqlens, 4)) return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
 static fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* L, int B,
                           int H, int Hkv, int N, int d, int causal, float scale, fa_dtype dtype,
-                          void* stream, int window = 0) {
+                          void* stream, int window = 0, const int* cu_seqlens = nullptr,
+                          int total = 0) {
   fa_status st = check_common(B, H, N, d, causal, scale, static_cast<int>(dtype));
   if (st != FA_OK) return st;
   if ((st = check_heads(H, Hkv)) != FA_OK) return st;
+  if (cu_seqlens && (st = check_packed(cu_seqlens, total)) != FA_OK) return st;
   if (!Q || !K || !V || !O || !L) return FA_ERR_INVALID_VALUE;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(L, 4))
     return FA_ERR_MISALIGNED;
   const long long BH = static_cast<long long>(B) * H, BHkv = static_cast<long long>(B) * Hkv;
-  const size_t nbytes = static_cast<size_t>(BH) * N * d * 2, lbytes = static_cast<size_t>(BH) * N * 4;
-  const size_t kvbytes = static_cast<size_t>(BHkv) * N * d * 2;
+  const size_t rows = cu_seqlens ? static_cast<size_t>(total) : static_cast<size_t>(B) * N;
+  const size_t nbytes = rows * H * d * 2, lbytes = rows * H * 4;
+  const size_t kvbytes = rows * Hkv * d * 2;
   const void* ins[3] = {Q, K, V};
   const size_t insz[3] = {nbytes, kvbytes, kvbytes};
   for (int i = 0; i < 3; ++i)
@@ -277,10 +311,19 @@ static fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, 
   const bool bf16 = dtype == FA_BF16;
   fa::FwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  if ((st = make_map(&a.tmQ, Q, d, N, BH, bf16)) != FA_OK) return st;
-  if ((st = make_map(&a.tmK, K, d, N, BHkv, bf16)) != FA_OK) return st;
-  if ((st = make_map(&a.tmV, V, d, N, BHkv, bf16)) != FA_OK) return st;
+  if (cu_seqlens) {
+    if ((st = make_map_packed(&a.tmQ, Q, d, H, total, bf16)) != FA_OK) return st;
+    if ((st = make_map_packed(&a.tmK, K, d, Hkv, total, bf16)) != FA_OK) return st;
+    if ((st = make_map_packed(&a.tmV, V, d, Hkv, total, bf16)) != FA_OK) return st;
+  } else {
+    if ((st = make_map(&a.tmQ, Q, d, N, BH, bf16)) != FA_OK) return st;
+    if ((st = make_map(&a.tmK, K, d, N, BHkv, bf16)) != FA_OK) return st;
+    if ((st = make_map(&a.tmV, V, d, N, BHkv, bf16)) != FA_OK) return st;
+  }
   if ((st = ctl_for_launch(&a.ctl)) != FA_OK) return st;
+  a.cu_seqlens = cu_seqlens;
+  a.H = H;
+  a.total = total;
   a.O = O;
   a.L = L;
   a.N = N;
@@ -320,10 +363,11 @@ static fa_status bwd_impl(const void* Q, const void* K, const void* V, const voi
                           const void* dO, const float* L, void* dQ, void* dK, void* dV,
                           void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
                           int d, int causal, float scale, fa_dtype dtype, void* stream,
-                          int window = 0) {
+                          int window = 0, const int* cu_seqlens = nullptr, int total = 0) {
   fa_status st = check_common(B, H, N, d, causal, scale, static_cast<int>(dtype));
   if (st != FA_OK) return st;
   if ((st = check_heads(H, Hkv)) != FA_OK) return st;
+  if (cu_seqlens && (st = check_packed(cu_seqlens, total)) != FA_OK) return st;
   if (!Q || !K || !V || !O || !dO || !L || !dQ || !dK || !dV) return FA_ERR_INVALID_VALUE;
   for (const void* p : {Q, K, V, O, dO, static_cast<const void*>(dQ), static_cast<const void*>(dK),
                         static_cast<const void*>(dV)})
@@ -333,8 +377,9 @@ static fa_status bwd_impl(const void* Q, const void* K, const void* V, const voi
   const size_t need = fa::bwd_workspace_bytes(BH, N, d);
   if (workspace && workspace_bytes < need) return FA_ERR_INVALID_VALUE;
   const long long BHkv = static_cast<long long>(B) * Hkv;
-  const size_t nbytes = static_cast<size_t>(BH) * N * d * 2, lbytes = static_cast<size_t>(BH) * N * 4;
-  const size_t kvbytes = static_cast<size_t>(BHkv) * N * d * 2;
+  const size_t rows = cu_seqlens ? static_cast<size_t>(total) : static_cast<size_t>(B) * N;
+  const size_t nbytes = rows * H * d * 2, lbytes = rows * H * 4;
+  const size_t kvbytes = rows * Hkv * d * 2;
   const void* outs[3] = {dQ, dK, dV};
   const size_t outsz[3] = {nbytes, kvbytes, kvbytes};
   const void* ins[5] = {Q, K, V, O, dO};
@@ -351,12 +396,23 @@ static fa_status bwd_impl(const void* Q, const void* K, const void* V, const voi
   const bool bf16 = dtype == FA_BF16;
   fa::BwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  if ((st = make_map(&a.tmQ, Q, d, N, BH, bf16)) != FA_OK) return st;
-  if ((st = make_map(&a.tmK, K, d, N, BHkv, bf16)) != FA_OK) return st;
-  if ((st = make_map(&a.tmV, V, d, N, BHkv, bf16)) != FA_OK) return st;
-  if ((st = make_map(&a.tmO, O, d, N, BH, bf16)) != FA_OK) return st;
-  if ((st = make_map(&a.tmdO, dO, d, N, BH, bf16)) != FA_OK) return st;
+  if (cu_seqlens) {
+    if ((st = make_map_packed(&a.tmQ, Q, d, H, total, bf16)) != FA_OK) return st;
+    if ((st = make_map_packed(&a.tmK, K, d, Hkv, total, bf16)) != FA_OK) return st;
+    if ((st = make_map_packed(&a.tmV, V, d, Hkv, total, bf16)) != FA_OK) return st;
+    if ((st = make_map_packed(&a.tmO, O, d, H, total, bf16)) != FA_OK) return st;
+    if ((st = make_map_packed(&a.tmdO, dO, d, H, total, bf16)) != FA_OK) return st;
+  } else {
+    if ((st = make_map(&a.tmQ, Q, d, N, BH, bf16)) != FA_OK) return st;
+    if ((st = make_map(&a.tmK, K, d, N, BHkv, bf16)) != FA_OK) return st;
+    if ((st = make_map(&a.tmV, V, d, N, BHkv, bf16)) != FA_OK) return st;
+    if ((st = make_map(&a.tmO, O, d, N, BH, bf16)) != FA_OK) return st;
+    if ((st = make_map(&a.tmdO, dO, d, N, BH, bf16)) != FA_OK) return st;
+  }
   if ((st = ctl_for_launch(&a.ctl)) != FA_OK) return st;
+  a.cu_seqlens = cu_seqlens;
+  a.H = H;
+  a.total = total;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = workspace;
   bool owned = false;
@@ -411,6 +467,28 @@ fa_status fa_bwd_swa(const void* Q, const void* K, const void* V, const void* O,
   if (window < 1) return FA_ERR_INVALID_VALUE;
   return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, B, H, Hkv, N, d, 1,
                   scale, dtype, stream, window);
+}
+
+fa_status fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* L,
+                        const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv,
+                        int d, int causal, int window, float scale, fa_dtype dtype, void* stream) {
+  if (!cu_seqlens || window < 0 || (window > 0 && !causal)) return FA_ERR_INVALID_VALUE;
+  return fwd_impl(Q, K, V, O, L, B, H, Hkv, max_seqlen, d, causal, scale, dtype, stream, window,
+                  cu_seqlens, total);
+}
+
+size_t fa_bwd_varlen_workspace_size(int B, int max_seqlen, int H, int d) {
+  return fa_bwd_workspace_size(B, H, max_seqlen, d, 1);
+}
+
+fa_status fa_bwd_varlen(const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* L, void* dQ, void* dK, void* dV,
+                        void* workspace, size_t workspace_bytes, const int* cu_seqlens, int B,
+                        int total, int max_seqlen, int H, int Hkv, int d, int causal, int window,
+                        float scale, fa_dtype dtype, void* stream) {
+  if (!cu_seqlens || window < 0 || (window > 0 && !causal)) return FA_ERR_INVALID_VALUE;
+  return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, B, H, Hkv, max_seqlen,
+                  d, causal, scale, dtype, stream, window, cu_seqlens, total);
 }
 
 }  // extern "C"

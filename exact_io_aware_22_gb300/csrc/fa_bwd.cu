@@ -65,24 +65,36 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
 }
 
 // ---------------------------------------------------------------- pre-pass
-// Dp[bh][r] = sum_c dO[r][c] O[r][c] (fp32), Lp[bh][r] = L[r] * log2(e);
-// rows r in [N, Np) get Dp = 0, Lp = +inf.
+// Dp[bh][r] = sum_c dO[r][c] O[r][c] (fp32), Lp[bh][r] = L[r] * log2(e), for every
+// flat head bh and padded row r; rows past the end of the sequence (N, or the packed
+// sequence's own length) get Dp = 0, Lp = +inf, which makes their P exactly 0.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) pre_kernel(const void* __restrict__ O,
                                                   const void* __restrict__ dO,
                                                   const float* __restrict__ L,
                                                   float* __restrict__ Dp, float* __restrict__ Lp,
-                                                  int N, int Np, long long rows_p) {
+                                                  int N, int Np, long long rows_p,
+                                                  const int* __restrict__ cu_seqlens, int H,
+                                                  int total) {
   constexpr int TPR = D / 8;   // threads per row, 16 bytes each
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long rp = gt / TPR;
   const int part = static_cast<int>(gt % TPR);
   float acc = 0.f;
-  long long src = -1;
+  long long src = -1, lsrc = -1;              // row of O / dO (in rows of D), index of L
   if (rp < rows_p) {
     const long long bh = rp / Np;
     const int r = static_cast<int>(rp % Np);
-    if (r < N) src = bh * N + r;
+    if (cu_seqlens) {
+      const int hl = static_cast<int>(bh % H);
+      const SeqRows sr = seq_rows(cu_seqlens, static_cast<int>(bh / H), N, total);
+      if (r < sr.n) {
+        src = static_cast<long long>(sr.base + r) * H + hl;
+        lsrc = static_cast<long long>(hl) * total + sr.base + r;
+      }
+    } else if (r < N) {
+      src = lsrc = bh * N + r;
+    }
   }
   if (src >= 0) {
     const uint4 a = reinterpret_cast<const uint4*>(O)[src * TPR + part];
@@ -99,7 +111,7 @@ __global__ void __launch_bounds__(256) pre_kernel(const void* __restrict__ O,
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (rp < rows_p && part == 0) {
     Dp[rp] = src >= 0 ? acc : 0.f;
-    Lp[rp] = src >= 0 ? L[src] * LOG2E : INFINITY;
+    Lp[rp] = src >= 0 ? L[lsrc] * LOG2E : INFINITY;
   }
 }
 
@@ -125,8 +137,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dK,
-                void* __restrict__ dV, int N, int Np, int group, int window, float scale,
-                float c_log2, KernelCtl ctl) {
+                void* __restrict__ dV, int N, int Np, int group, int window,
+                const int* __restrict__ cu_seqlens, int H, int total, float scale, float c_log2,
+                KernelCtl ctl) {
   using G = Geo<D>;
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -141,10 +154,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bkv = bp.bh;                    // K/V head; its query heads are bkv*group + g
   const int kb = bp.rank;                   // key block (causal: block 0 has the most work)
   const int i0 = CAUSAL ? kb : 0;           // BM == BN: the diagonal query block
+  const int Hkv = H / group;
+  const SeqRows sr = seq_rows(cu_seqlens, bkv / Hkv, N, total);
+  const int hk = sr.packed ? bkv % Hkv : bkv;            // K/V head coordinate
+  const int nq_r = (sr.n + BM - 1) / BM;                 // query blocks of this sequence
   // query blocks per query head: from the diagonal to the last one that sees a key of
   // this block (a window of W keys reaches query rows up to the block's last key + W - 1)
-  const int n_head = ((CAUSAL && window > 0) ? min(nqb, (kb * BN + BN - 1 + window - 1) / BM + 1)
-                                             : nqb) - i0;
+  const int n_head = kb * BN >= sr.n ? 0
+      : ((CAUSAL && window > 0) ? min(nq_r, (kb * BN + BN - 1 + window - 1) / BM + 1) : nq_r) - i0;
   const int n_iter = group * n_head;        // every query head of the group in turn
 
   auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };
@@ -171,8 +188,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && n_iter > 0) {
       bool ok = true;
       mbar_arrive_expect_tx(bar(B_KV), 2 * G::TILE_BYTES);
-      load_tile<D>(sb + C::K_OFF, &tmK, bar(B_KV), kb * BN, bkv);
-      load_tile<D>(sb + C::V_OFF, &tmV, bar(B_KV), kb * BN, bkv);
+      load_tile<D>(sb + C::K_OFF, &tmK, bar(B_KV), sr.y(kb * BN, hk), sr.z(kb * BN, hk));
+      load_tile<D>(sb + C::V_OFF, &tmV, bar(B_KV), sr.y(kb * BN, hk), sr.z(kb * BN, hk));
       int it = 0;
       for (; it < n_iter; ++it) {
         const int s = it % G::STAGES;
@@ -181,8 +198,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(bar(B_QF(s)), 2 * G::TILE_BYTES);
         const int g = it / n_head;
         const int qrow = (i0 + it - g * n_head) * BM, bhq = bkv * group + g;
-        load_tile<D>(sb + C::Q_OFF + s * G::TILE_BYTES, &tmQ, bar(B_QF(s)), qrow, bhq);
-        load_tile<D>(sb + C::DO_OFF + s * G::TILE_BYTES, &tmdO, bar(B_QF(s)), qrow, bhq);
+        const int hq = sr.packed ? bhq % H : bhq;
+        load_tile<D>(sb + C::Q_OFF + s * G::TILE_BYTES, &tmQ, bar(B_QF(s)), sr.y(qrow, hq),
+                     sr.z(qrow, hq));
+        load_tile<D>(sb + C::DO_OFF + s * G::TILE_BYTES, &tmdO, bar(B_QF(s)), sr.y(qrow, hq),
+                     sr.z(qrow, hq));
       }
       if (!ok) {
         mbar_wait(bar(B_KV), 0, ctl);
@@ -311,8 +331,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok && mbar_wait_warp(bar(B_OF), 0, ctl)) {
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      const bool valid = gkey < N;
-      const size_t roff = (static_cast<size_t>(bkv) * N + gkey) * D;
+      const bool valid = gkey < sr.n;
+      const size_t roff = sr.off(gkey, hk, Hkv, N, D);
       constexpr int HALF = D / 2;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
@@ -366,7 +386,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dQ,
-              int N, int Np, int group, int window, float scale, float c_log2, KernelCtl ctl) {
+              int N, int Np, int group, int window, const int* __restrict__ cu_seqlens, int H,
+              int total, float scale, float c_log2, KernelCtl ctl) {
   using G = Geo<D>;
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -376,14 +397,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = Np / BM;
-  const int nkb = (N + BN - 1) / BN;
   const BlockPos bp = block_pos(nqb);
   const int bh = bp.bh;
   const int qb = nqb - 1 - bp.rank;                // causal: the last query blocks have the most work
   // key blocks j_lo .. diagonal (a window of W keys starts at the block holding the
   // block's first row - W + 1); loop position it is key block j_lo + it
+  const SeqRows sr = seq_rows(cu_seqlens, bh / H, N, total);
+  const int hq = sr.packed ? bh % H : bh, hk = sr.packed ? (bh % H) / group : bh / group;
+  const int nk_r = (sr.n + BN - 1) / BN;                 // key blocks of this sequence
   const int j_lo = (CAUSAL && window > 0) ? max(0, qb * BM - window + 1) / BN : 0;
-  const int n_iter = (CAUSAL ? min(qb + 1, nkb) : nkb) - j_lo;
+  const int n_iter = qb * BM >= sr.n ? 0 : (CAUSAL ? min(qb + 1, nk_r) : nk_r) - j_lo;
 
   auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };
   const int B_QF = 0;
@@ -409,18 +432,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && n_iter > 0) {
       bool ok = true;
       mbar_arrive_expect_tx(bar(B_QF), 2 * G::TILE_BYTES);
-      load_tile<D>(sb + C::Q_OFF, &tmQ, bar(B_QF), qb * BM, bh);
-      load_tile<D>(sb + C::DO_OFF, &tmdO, bar(B_QF), qb * BM, bh);
+      load_tile<D>(sb + C::Q_OFF, &tmQ, bar(B_QF), sr.y(qb * BM, hq), sr.z(qb * BM, hq));
+      load_tile<D>(sb + C::DO_OFF, &tmdO, bar(B_QF), sr.y(qb * BM, hq), sr.z(qb * BM, hq));
       int it = 0;
       for (; it < n_iter; ++it) {
         const int s = it % G::STAGES;
         const uint32_t ph = (it / G::STAGES) & 1;
         if (!(ok = mbar_wait(bar(B_KE(s)), ph ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_KF(s)), 2 * G::TILE_BYTES);
-        load_tile<D>(sb + C::K_OFF + s * G::TILE_BYTES, &tmK, bar(B_KF(s)), (j_lo + it) * BN,
-                     bh / group);
-        load_tile<D>(sb + C::V_OFF + s * G::TILE_BYTES, &tmV, bar(B_KF(s)), (j_lo + it) * BN,
-                     bh / group);
+        const int krow = (j_lo + it) * BN;
+        load_tile<D>(sb + C::K_OFF + s * G::TILE_BYTES, &tmK, bar(B_KF(s)), sr.y(krow, hk),
+                     sr.z(krow, hk));
+        load_tile<D>(sb + C::V_OFF + s * G::TILE_BYTES, &tmV, bar(B_KF(s)), sr.y(krow, hk),
+                     sr.z(krow, hk));
       }
       if (!ok) {
         mbar_wait(bar(B_QF), 0, ctl);
@@ -497,6 +521,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int k0 = (j_lo + it) * BN + h * 64;
       const bool diag = CAUSAL && j_lo + it == qb;
       const bool wedge = CAUSAL && window > 0 && qb * BM + BM - 1 - (j_lo + it) * BN >= window;
+      // keys past the end of the sequence: zero-filled rows when dense, but the next
+      // sequence's keys when packed
+      const bool kedge = k0 + 64 > sr.n;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         float p0 = ex2(fmaf(__uint_as_float(s[2 * i]), c_log2, -lsub));
@@ -508,6 +535,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (wedge) {
           if (grow - (k0 + 2 * i) >= window) p0 = 0.f;
           if (grow - (k0 + 2 * i + 1) >= window) p1 = 0.f;
+        }
+        if (kedge) {
+          if (k0 + 2 * i >= sr.n) p0 = 0.f;
+          if (k0 + 2 * i + 1 >= sr.n) p1 = 0.f;
         }
         const float ds0 = p0 * (__uint_as_float(dp[2 * i]) - dr);
         const float ds1 = p1 * (__uint_as_float(dp[2 * i + 1]) - dr);
@@ -522,7 +553,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       constexpr int HALF = D / 2;
-      T* dst = reinterpret_cast<T*>(dQ) + (static_cast<size_t>(bh) * N + grow) * D + h * HALF;
+      T* dst = reinterpret_cast<T*>(dQ) + sr.off(grow, hq, H, N, D) + h * HALF;
 #pragma unroll
       for (int cc = 0; cc < HALF / 16; ++cc) {
         uint32_t v[16];
@@ -532,7 +563,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           w[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
-        if (grow < N) {
+        if (grow < sr.n) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * cc);
           d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
           d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -560,7 +591,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     trace_begin(TR_BWD_PRE, st);
     pre_kernel<D, BF16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        a.O, a.dO, a.L, a.Dvec, Lp, a.N, Np, rows_p);
+        a.O, a.dO, a.L, a.Dvec, Lp, a.N, Np, rows_p, a.cu_seqlens, a.H, a.total);
     trace_end(TR_BWD_PRE, st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -574,8 +605,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     const long long grid = static_cast<long long>(nqb) * (a.BH / a.group);   // per K/V head
     trace_begin(TR_BWD_DKDV, st);
     kern<<<static_cast<unsigned>(grid), THREADS, DkdvCfg<D>::SMEM_BYTES, st>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.window, a.scale,
-        a.c_log2, a.ctl);
+        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.window,
+        a.cu_seqlens, a.H, a.total, a.scale, a.c_log2, a.ctl);
     trace_end(TR_BWD_DKDV, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -588,8 +619,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     const long long grid = static_cast<long long>(nqb) * a.BH;
     trace_begin(TR_BWD_DQ, st);
     kern<<<static_cast<unsigned>(grid), THREADS, DqCfg<D>::SMEM_BYTES, st>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.window, a.scale,
-        a.c_log2, a.ctl);
+        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.window, a.cu_seqlens,
+        a.H, a.total, a.scale, a.c_log2, a.ctl);
     trace_end(TR_BWD_DQ, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                    const float* __restrict__ Dp, const float* __restrict__ Lp,
                    void* __restrict__ dK, void* __restrict__ dV, int N, int Np, int group,
-                   int window, float scale, float c_log2, KernelCtl ctl) {
+                   int window, const int* __restrict__ cu_seqlens, int H, int total, float scale,
+                   float c_log2, KernelCtl ctl) {
   using namespace kv;
   extern __shared__ __align__(1024) uint8_t sg[];
   const uint32_t sb = smem_u32(sg);
@@ -143,10 +144,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bkv = bp.bh;                           // K/V head; its query heads: bkv*group + g
   const int kb = bp.rank;                          // causal: block 0 has the most work
   const int q_start = CAUSAL ? kb : 0;             // the diagonal query tile
+  const int Hkv = H / group;
+  const SeqRows sr = seq_rows(cu_seqlens, bkv / Hkv, N, total);
+  const int hk = sr.packed ? bkv % Hkv : bkv;      // K/V head coordinate
+  const int nq_r = (sr.n + BT - 1) / BT;           // query tiles of this sequence
   // query tiles per query head: from the diagonal to the last tile that sees a key of
   // this block (with a window of W keys, query rows up to the block's last key + W - 1)
-  const int n_head = ((CAUSAL && window > 0) ? min(nq, (kb * BT + BT - 1 + window - 1) / BT + 1)
-                                             : nq) - q_start;
+  const int n_head = kb * BT >= sr.n ? 0
+      : ((CAUSAL && window > 0) ? min(nq_r, (kb * BT + BT - 1 + window - 1) / BT + 1) : nq_r) -
+            q_start;
   const int n_iter = group * n_head;               // the group's query heads one after another
 
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
@@ -179,8 +185,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(bar(B_KV), 2 * TILE);
       for (int c = 0; c < 2; ++c) {
-        tma_load_3d(sb + K_OFF + c * CHUNK, &tmK, bar(B_KV), c * 64, kb * BT, bkv);
-        tma_load_3d(sb + V_OFF + c * CHUNK, &tmV, bar(B_KV), c * 64, kb * BT, bkv);
+        tma_load_3d(sb + K_OFF + c * CHUNK, &tmK, bar(B_KV), c * 64, sr.y(kb * BT, hk),
+                    sr.z(kb * BT, hk));
+        tma_load_3d(sb + V_OFF + c * CHUNK, &tmV, bar(B_KV), c * 64, sr.y(kb * BT, hk),
+                    sr.z(kb * BT, hk));
       }
       // Q with L*log2e in a three-stage ring, dO with D in a two-stage ring (L and D:
       // padded per-row arrays, 512-byte aligned per tile).  Both stages of a tile are
@@ -191,18 +199,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int s = it % Q_STAGES, g = it % DO_STAGES;
         const int gh = it / n_head;                // which query head of the group
         const int qrow = (q_start + it - gh * n_head) * BT, bhq = bkv * group + gh;
+        const int hq = sr.packed ? bhq % H : bhq;
         const size_t row = static_cast<size_t>(bhq) * Np + qrow;
         if (!(ok = mbar_wait(bar(B_QE(s)), ((it / Q_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_QF(s)), TILE + 512);
         for (int c = 0; c < 2; ++c)
-          tma_load_3d(sb + Q_OFF + s * TILE + c * CHUNK, &tmQ, bar(B_QF(s)), c * 64, qrow, bhq);
+          tma_load_3d(sb + Q_OFF + s * TILE + c * CHUNK, &tmQ, bar(B_QF(s)), c * 64,
+                      sr.y(qrow, hq), sr.z(qrow, hq));
         bulk_load(sb + L_OFF + s * 512, Lp + row, 512, bar(B_QF(s)));
         ++nq_issued;
         if (!(ok = mbar_wait(bar(B_GE(g)), ((it / DO_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_GF(g)), TILE + 512);
         for (int c = 0; c < 2; ++c)
-          tma_load_3d(sb + DO_OFF + g * TILE + c * CHUNK, &tmdO, bar(B_GF(g)), c * 64, qrow,
-                      bhq);
+          tma_load_3d(sb + DO_OFF + g * TILE + c * CHUNK, &tmdO, bar(B_GF(g)), c * 64,
+                      sr.y(qrow, hq), sr.z(qrow, hq));
         bulk_load(sb + D_OFF + g * 512, Dp + row, 512, bar(B_GF(g)));
         ++ng_issued;
       }
@@ -406,8 +416,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok && mbar_wait_warp(bar(B_OF), 0, ctl)) {
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      const bool valid = gkey < N;
-      const size_t roff = (static_cast<size_t>(bkv) * N + gkey) * HD + 64 * h;
+      const bool valid = gkey < sr.n;
+      const size_t roff = sr.off(gkey, hk, Hkv, N, HD) + 64 * h;
       store_row64<BF16>(tmem + lane_off + DV_COL + 64 * h, 1.f, reinterpret_cast<T*>(dV) + roff,
                         valid);
       store_row64<BF16>(tmem + lane_off + DK_COL + 64 * h, scale, reinterpret_cast<T*>(dK) + roff,
@@ -444,8 +454,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     dq128_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmdO, const void* __restrict__ Q,
                  const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dQ,
-                 int N, int Np, int group, int window, float scale, float c_log2,
-                 KernelCtl ctl) {
+                 int N, int Np, int group, int window, const int* __restrict__ cu_seqlens, int H,
+                 int total, float scale, float c_log2, KernelCtl ctl) {
   using namespace qd;
   extern __shared__ __align__(1024) uint8_t sg[];
   const uint32_t sb = smem_u32(sg);
@@ -455,7 +465,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = Np / BT;
-  const int nkb = (N + BT - 1) / BT;
   const BlockPos bp = block_pos(nqb);
   const int bh = bp.bh;
   const int qb = nqb - 1 - bp.rank;                // causal: the last query tiles have the most work
@@ -463,7 +472,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   // key blocks j_lo .. diagonal; with a window of W keys, from the block holding the
   // tile's first row - W + 1
   const int j_lo = (CAUSAL && window > 0) ? max(0, qb * BT - window + 1) / BT : 0;
-  const int n_iter = (CAUSAL ? min(qb + 1, nkb) : nkb) - j_lo;   // loop position j: block j_lo + j
+  const SeqRows sr = seq_rows(cu_seqlens, bh / H, N, total);
+  const int hq = sr.packed ? bh % H : bh, hk = sr.packed ? (bh % H) / group : bkv;
+  const int nk_r = (sr.n + BT - 1) / BT;           // key blocks of this sequence
+  const int n_iter = qb * BT >= sr.n ? 0           // loop position j: key block j_lo + j
+                                     : (CAUSAL ? min(qb + 1, nk_r) : nk_r) - j_lo;
 
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
   const int B_DOF = 0;
@@ -495,7 +508,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(bar(B_DOF), TILE);
       for (int c = 0; c < 2; ++c)
-        tma_load_3d(sb + DO_OFF + c * CHUNK, &tmdO, bar(B_DOF), c * 64, qb * BT, bh);
+        tma_load_3d(sb + DO_OFF + c * CHUNK, &tmdO, bar(B_DOF), c * 64, sr.y(qb * BT, hq),
+                    sr.z(qb * BT, hq));
       bool ok = true;
       int j = 0;
       for (; j < n_iter; ++j) {
@@ -504,9 +518,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(bar(B_KF(s)), 2 * TILE);
         for (int c = 0; c < 2; ++c) {
           tma_load_3d(sb + K_OFF + s * TILE + c * CHUNK, &tmK, bar(B_KF(s)), c * 64,
-                      (j_lo + j) * BT, bkv);
+                      sr.y((j_lo + j) * BT, hk), sr.z((j_lo + j) * BT, hk));
           tma_load_3d(sb + V_OFF + s * TILE + c * CHUNK, &tmV, bar(B_KF(s)), c * 64,
-                      (j_lo + j) * BT, bkv);
+                      sr.y((j_lo + j) * BT, hk), sr.z((j_lo + j) * BT, hk));
         }
       }
       if (!ok) {
@@ -585,13 +599,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     if (h == 0) {
       // this row of Q into TMEM as 16-bit pairs (A operand of S = Q K^T); rows past N are zero
-      const uint4* src = reinterpret_cast<const uint4*>(Q) + (static_cast<size_t>(bh) * N + grow) * (HD / 8);
+      const uint4* src = reinterpret_cast<const uint4*>(Q) + sr.off(grow, hq, H, N, HD) / 8;
       uint32_t w[32];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 v = grow < N ? __ldg(src + 8 * half + i) : make_uint4(0, 0, 0, 0);
+          const uint4 v = grow < sr.n ? __ldg(src + 8 * half + i) : make_uint4(0, 0, 0, 0);
           w[4 * i] = v.x;
           w[4 * i + 1] = v.y;
           w[4 * i + 2] = v.z;
@@ -640,6 +654,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < 64; ++c)
           if (grow - (k0 + c) >= window) p[c] = 0.f;
       }
+      if (k0 + 64 > sr.n) {
+        // keys past the end of the sequence: zero-filled rows when dense, but the next
+        // sequence's keys when packed
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (k0 + c >= sr.n) p[c] = 0.f;
+      }
       if (!(ok = mbar_wait_warp(bar(B_DPF), j & 1, ctl))) break;
       tc_fence_after();
       tmem_ld32(tmem + lane_off + DP_COL + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
@@ -668,8 +689,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok && mbar_wait_warp(bar(B_OF), 0, ctl)) {
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      T* dst = reinterpret_cast<T*>(dQ) + (static_cast<size_t>(bh) * N + grow) * HD + 64 * h;
-      store_row64<BF16>(tmem + lane_off + DQ_COL + 64 * h, scale, dst, grow < N);
+      T* dst = reinterpret_cast<T*>(dQ) + sr.off(grow, hq, H, N, HD) + 64 * h;
+      store_row64<BF16>(tmem + lane_off + DQ_COL + 64 * h, scale, dst, grow < sr.n);
     }
   }
   tc_fence_before();
@@ -693,8 +714,8 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DKDV, st);
     kern<<<static_cast<unsigned>(nblk_kv), THREADS, kv::SMEM_BYTES, st>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.window, a.scale,
-        a.c_log2, a.ctl);
+        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.window,
+        a.cu_seqlens, a.H, a.total, a.scale, a.c_log2, a.ctl);
     trace_end(TR_BWD_DKDV, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -706,8 +727,8 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DQ, st);
     kern<<<static_cast<unsigned>(nblk), THREADS, qd::SMEM_BYTES, st>>>(
-        a.tmK, a.tmV, a.tmdO, a.Q, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.window, a.scale,
-        a.c_log2, a.ctl);
+        a.tmK, a.tmV, a.tmdO, a.Q, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.window, a.cu_seqlens,
+        a.H, a.total, a.scale, a.c_log2, a.ctl);
     trace_end(TR_BWD_DQ, st);
     return cudaGetLastError();
   }

@@ -71,7 +71,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, void* __restrict__ Out,
                float* __restrict__ Lout, int N, int n_qblk, int group, int window,
-               float c_log2, KernelCtl ctl) {
+               const int* __restrict__ cu_seqlens, int H, int total, float c_log2,
+               KernelCtl ctl) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -83,16 +84,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bh = bp.bh;
   const int qblk = n_qblk - 1 - bp.rank;        // causal: the last query tiles have the most work
   const int bkv = bh / group;                   // the K/V head of this query head (b-major heads)
+  // Rows of this (batch, head): dense (B, H, N, d) maps are (d, N, B*H), a row at
+  // (row, flat head); packed sequences (total, H, d) have maps (d, H, total), a row at
+  // (head within the batch, first token + row), and their own length Nr.
+  const SeqRows sr = seq_rows(cu_seqlens, bh / H, N, total);
+  const int Nr = sr.n;
+  const int hq = sr.packed ? bh % H : bh, hk = sr.packed ? (bh % H) / group : bkv;
+  auto cy = [&](int r, int head) { return sr.y(r, head); };
+  auto cz = [&](int r, int head) { return sr.z(r, head); };
   const int row0 = qblk * (NT * BM);
-  const int nkv = (N + BN - 1) / BN;
+  const int nkv = (Nr + BN - 1) / BN;
   // KV tiles [lo_t[t], n_t[t]) of Q tile t: up to the diagonal when causal; with a
   // sliding window of W keys, from the tile holding key (first row - W + 1)
   int n_t[NT], lo_t[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const int r = row0 + t * BM;
-    if (r >= N) n_t[t] = 0;
-    else if (CAUSAL) n_t[t] = min(nkv, min(r + BM - 1, N - 1) / BN + 1);
+    if (r >= Nr) n_t[t] = 0;
+    else if (CAUSAL) n_t[t] = min(nkv, min(r + BM - 1, Nr - 1) / BN + 1);
     else n_t[t] = nkv;
     lo_t[t] = WINDOW ? max(0, r - window + 1) / BN : 0;
   }
@@ -138,7 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int t = 0; t < NT; ++t)
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(sb + C::Q_OFF + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, bar(B_QF),
-                      c * C::ATOM, row0 + t * BM, bh);
+                      c * C::ATOM, cy(row0 + t * BM, hq), cz(row0 + t * BM, hq));
       int j = 0;                                // stream position: KV tile j0 + j
       for (; j < n_stream; ++j) {
         const int s = j % C::STAGES;
@@ -148,12 +157,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(bar(B_KF(s)), C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(sb + C::K_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmK, bar(B_KF(s)),
-                      c * C::ATOM, krow, bkv);
+                      c * C::ATOM, cy(krow, hk), cz(krow, hk));
         if (!(ok = mbar_wait(bar(B_VE(s)), ph ^ 1, ctl))) { ++j; break; }
         mbar_arrive_expect_tx(bar(B_VF(s)), C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(sb + C::V_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV, bar(B_VF(s)),
-                      c * C::ATOM, krow, bkv);
+                      c * C::ATOM, cy(krow, hk), cz(krow, hk));
       }
       if (!ok) {
         // drain: wait (bounded) for every copy this thread issued, so no bulk
@@ -270,10 +279,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int kbase = (lo_t[t] + j) * BN;
       // masks: causal on the diagonal tile, key padding on the last tile, and with a
       // window the tiles reaching left of some row's first allowed key
-      const bool need_mask = (CAUSAL && kbase + BN - 1 > tile_row0) || (kbase + BN > N) ||
+      const bool need_mask = (CAUSAL && kbase + BN - 1 > tile_row0) || (kbase + BN > Nr) ||
                              (WINDOW && kbase < tile_row0 + BM - window);
       if (need_mask) {
-        const int lim = CAUSAL ? min(grow + 1, N) : N;   // keys in [lo_key, lim) are allowed
+        const int lim = CAUSAL ? min(grow + 1, Nr) : Nr;   // keys in [lo_key, lim) are allowed
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (kbase + c >= lim || (WINDOW && kbase + c < lo_key)) sr[c] = __float_as_uint(-INFINITY);
@@ -337,9 +346,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok && nt > 0 && mbar_wait_warp(bar(B_OF(t)), 0, ctl)) {
       tc_fence_after();
       const float inv_l = 1.f / l_run;
-      const bool valid = grow < N;
+      const bool valid = grow < Nr;
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      T* orow = reinterpret_cast<T*>(Out) + (static_cast<size_t>(bh) * N + grow) * D;
+      T* orow = reinterpret_cast<T*>(Out) + sr.off(grow, hq, H, N, D);
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -358,7 +367,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (valid)
-        Lout[static_cast<size_t>(bh) * N + grow] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+        Lout[sr.packed ? static_cast<size_t>(hq) * total + sr.base + grow
+                       : static_cast<size_t>(bh) * N + grow] =
+            (m_run + log2f(l_run)) * 0.69314718055994531f;
     }
   }
   // ------------------------------------------------------------ teardown
@@ -382,7 +393,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   trace_begin(TR_FWD, st);
   kern<<<static_cast<unsigned>(grid), THREADS, C::SMEM_BYTES, st>>>(
-      a.tmQ, a.tmK, a.tmV, a.O, a.L, a.N, n_qblk, a.group, a.window, a.c_log2, a.ctl);
+      a.tmQ, a.tmK, a.tmV, a.O, a.L, a.N, n_qblk, a.group, a.window, a.cu_seqlens, a.H, a.total,
+      a.c_log2, a.ctl);
   trace_end(TR_FWD, st);
   return cudaGetLastError();
 }

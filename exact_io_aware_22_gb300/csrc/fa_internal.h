@@ -38,6 +38,11 @@ struct FwdArgs {
   int N, BH;
   int group;                   // query heads per K/V head (H / Hkv; 1 without sharing)
   int window;                  // causal sliding window of this many keys (0: none)
+  // packed variable-length sequences (NULL: dense (B, H, N, d)): device int32
+  // offsets [B+1]; Q, O (total, H, d), K, V (total, H/group, d), L (H, total); N is
+  // then the longest sequence
+  const int* cu_seqlens;
+  int H, total;
   float c_log2;                // scale * log2(e)
   KernelCtl ctl;
 };
@@ -56,6 +61,8 @@ struct BwdArgs {
   int N, BH;                   // BH = B*H query heads
   int group;                   // query heads per K/V head; B*H/group K/V heads
   int window;                  // causal sliding window of this many keys (0: none)
+  const int* cu_seqlens;       // packed variable-length sequences, as in FwdArgs
+  int H, total;
   float scale, c_log2;
   KernelCtl ctl;
 };

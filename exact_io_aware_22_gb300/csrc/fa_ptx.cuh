@@ -322,6 +322,35 @@ __device__ __forceinline__ BlockPos block_pos(int nblk) {
   return block_pos(nblk, static_cast<int>(blockIdx.x));
 }
 
+// ---------------------------------------------------------------- sequence rows
+// Where the rows of one attention head live.  Dense (B, H, N, d) tensors have TMA
+// maps (d, N, B*H): row r of flat head bh sits at (y, z) = (r, bh).  Packed
+// variable-length sequences (total, Hx, d) have maps (d, Hx, total): row r of head
+// hx of batch b sits at (hx, first token of b + r), and the sequence has its own
+// length.  `head` below is the flat head index for dense tensors and the head within
+// the batch for packed ones.
+struct SeqRows {
+  int base;      // packed: first token of the sequence
+  int n;         // rows of the sequence (dense: N)
+  bool packed;
+  __device__ __forceinline__ int y(int r, int head) const { return packed ? head : r; }
+  __device__ __forceinline__ int z(int r, int head) const { return packed ? base + r : head; }
+  // element offset of row r of `head` in a tensor of Hx heads of d columns
+  __device__ __forceinline__ size_t off(int r, int head, int Hx, int N, int d) const {
+    return (packed ? static_cast<size_t>(base + r) * Hx + head
+                   : static_cast<size_t>(head) * N + r) * d;
+  }
+};
+// Offsets come from the caller: a sequence is clamped to [0, total) and to N rows
+// (the longest sequence), so malformed offsets cannot send a kernel outside the
+// tensors -- rows outside are simply not computed.
+__device__ __forceinline__ SeqRows seq_rows(const int* __restrict__ cu, int b, int N, int total) {
+  if (!cu) return {0, N, false};
+  const int a = min(max(__ldg(cu + b), 0), total);
+  const int e = min(max(__ldg(cu + b + 1), a), total);
+  return {a, min(e - a, N), true};
+}
+
 // ---------------------------------------------------------------- numerics
 __device__ __forceinline__ float ex2(float x) {
   float y;

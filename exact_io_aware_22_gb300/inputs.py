@@ -36,6 +36,25 @@ def make_inputs(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int =
     return {"q": q.to(t), "k": k.to(t), "v": v.to(t), "do": do.to(t)}
 
 
+def make_packed_inputs(lens, H: int, d: int, dtype: str = "bf16", seed: int = 0,
+                       Hkv: int | None = None):
+    """Packed variable-length sequences: dict(q, k, v, do) of CPU tensors, q and do
+    (total, H, d), k and v (total, Hkv, d), drawn in that order like make_inputs, plus
+    cu_seqlens (int32, len(lens) + 1 offsets)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    total = int(sum(lens))
+    kvh = H if Hkv is None else Hkv
+    q = torch.randn((total, H, d), generator=g, dtype=torch.float32)
+    k = torch.randn((total, kvh, d), generator=g, dtype=torch.float32)
+    v = torch.randn((total, kvh, d), generator=g, dtype=torch.float32)
+    do = torch.randn((total, H, d), generator=g, dtype=torch.float32)
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(list(lens), dtype=torch.int64), 0).to(torch.int32)
+    t = DTYPES[dtype]
+    return {"q": q.to(t), "k": k.to(t), "v": v.to(t), "do": do.to(t), "cu_seqlens": cu}
+
+
 # Workloads: (name, B, H, N, d, dtype, causal, qk_std)
 WORKLOADS = {
     "tiny_full_d64_fp16": (1, 1, 128, 64, "fp16", False, 1.0),

@@ -115,6 +115,35 @@ fa_status fa_bwd_swa(const void* Q, const void* K, const void* V, const void* O,
                      size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int window,
                      float scale, fa_dtype dtype, void* stream);
 
+/* Variable-length batches: B sequences of different lengths packed one after
+ * another (the docs page lists "variable-length batches" among the features its
+ * kernels do not have yet, "Scope").  Sequence b holds rows cu_seqlens[b] ..
+ * cu_seqlens[b+1]-1 of every tensor and attends only to its own keys (causal and
+ * window as in fa_fwd / fa_fwd_swa, measured from the sequence's first row; window
+ * 0 = none; window > 0 needs causal); K/V heads shared as in fa_fwd_gqa.
+ *   Layout   Q, O, dO, dQ: (total, H, d); K, V, dK, dV: (total, Hkv, d), rows
+ *            row-major with heads inside a row; L: (H, total) fp32.
+ *   cu_seqlens  device int32 [B+1]: 0 = cu[0] <= cu[1] <= ... <= cu[B] = total.
+ *            max_seqlen >= every cu[b+1] - cu[b] (it sizes the grid).  The kernels
+ *            clamp every sequence to rows [0, total) and to max_seqlen rows, so
+ *            offsets that break these rules leave rows uncomputed but never make a
+ *            kernel touch memory outside the tensors.
+ *   Workspace of fa_bwd_varlen: fa_bwd_varlen_workspace_size(B, max_seqlen, H, d),
+ *            or NULL.
+ *   Errors   as fa_fwd_gqa / fa_bwd_gqa (max_seqlen in the role of N), plus
+ *            FA_ERR_INVALID_VALUE for cu_seqlens NULL, total < 1, window < 0 or a
+ *            window without causal; FA_ERR_MISALIGNED if cu_seqlens is not 4-byte
+ *            aligned. */
+fa_status fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* L,
+                        const int* cu_seqlens, int B, int total, int max_seqlen, int H, int Hkv,
+                        int d, int causal, int window, float scale, fa_dtype dtype, void* stream);
+size_t fa_bwd_varlen_workspace_size(int B, int max_seqlen, int H, int d);
+fa_status fa_bwd_varlen(const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* L, void* dQ, void* dK, void* dV,
+                        void* workspace, size_t workspace_bytes, const int* cu_seqlens, int B,
+                        int total, int max_seqlen, int H, int Hkv, int d, int causal, int window,
+                        float scale, fa_dtype dtype, void* stream);
+
 /* Static description of a status code. */
 const char* fa_status_string(fa_status s);
 

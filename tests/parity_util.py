@@ -95,3 +95,39 @@ def compare(B, H, N, d, dtype, causal, qk_std=1.0, heads=None, seed=0, scale=Non
     for n in ("dq", "dk", "dv"):
         assert rep[n] <= TOL_G[dtype], rep
     return rep
+
+
+def compare_varlen(lens, H, d, dtype, causal, Hkv=None, window=0, seed=0, scale=None):
+    """Packed variable-length sequences through fwd_varlen / bwd_varlen against the
+    oracle, every sequence and head compared; same tolerances as ``compare``."""
+    import exact_io_aware_22_gb300 as fa
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    x = inputs.make_packed_inputs(lens, H, d, dtype, seed=seed, Hkv=Hkv)
+    cu = x["cu_seqlens"]
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    cug = cu.cuda()
+    max_len = max(max(lens), 1)
+    o, lse = fa.fwd_varlen(q, k, v, cug, max_len, causal=causal, scale=scale, window=window)
+    dq, dk, dv = fa.bwd_varlen(q, k, v, o, lse, do, cug, max_len, causal=causal, scale=scale,
+                               window=window)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0, "a kernel reported a bounded-wait timeout"
+    xd = {n: x[n].double().numpy() for n in ("q", "k", "v", "do")}
+    cun = cu.numpy()
+    o_ref, l_ref = oracle.fwd_varlen(xd["q"], xd["k"], xd["v"], cun, causal, scale, window)
+    dq_ref, dk_ref, dv_ref, _ = oracle.bwd_varlen(xd["q"], xd["k"], xd["v"], xd["do"], cun, causal,
+                                                  scale, window)
+    rep = {}
+    for name, got, ref in (("o", o, o_ref), ("lse", lse, l_ref), ("dq", dq, dq_ref),
+                           ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
+        g = got.double().cpu().numpy()
+        assert np.isfinite(g).all(), f"{name}: non-finite values"
+        err = float(np.max(np.abs(g - ref)))
+        if name in ("dq", "dk", "dv"):
+            err /= max(float(np.max(np.abs(ref))), 1e-30)
+        rep[name] = err
+    assert rep["o"] <= TOL_O[dtype], rep
+    assert rep["lse"] <= TOL_L, rep
+    for n in ("dq", "dk", "dv"):
+        assert rep[n] <= TOL_G[dtype], rep
+    return rep

@@ -148,6 +148,31 @@ def test_sliding_window_checks_heads(lib):
     assert lib.fa_fwd_swa(*a, 1, 8, 2, 128, 48, 16, 0.125, 1, None) == UNSUPPORTED
 
 
+def fwd_varlen(lib, **kw):
+    a = dict(Q=M1, K=2 * M1, V=3 * M1, O=4 * M1, L=5 * M1, cu=6 * M1, B=2, total=300,
+             max_len=200, H=4, Hkv=2, d=64, causal=1, window=0, scale=0.125, dtype=1)
+    a.update(kw)
+    ptrs = [ctypes.c_void_p(a[k]) for k in ("Q", "K", "V", "O", "L", "cu")]
+    return lib.fa_fwd_varlen(*ptrs, a["B"], a["total"], a["max_len"], a["H"], a["Hkv"], a["d"],
+                             a["causal"], a["window"], a["scale"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu=0), INVALID), (dict(total=0), INVALID), (dict(window=-1), INVALID),
+    (dict(window=16, causal=0), INVALID), (dict(cu=6 * M1 + 2), MISALIGNED),
+    (dict(Hkv=3), INVALID), (dict(max_len=0), INVALID), (dict(d=48), UNSUPPORTED),
+    (dict(O=M1 + 4096), INVALID),                     # O inside Q (300 x 4 x 64 x 2 bytes)
+])
+def test_varlen_rejects(lib, kw, code):
+    assert fwd_varlen(lib, **kw) == code
+
+
+def test_varlen_workspace_size(lib):
+    assert lib.fa_bwd_varlen_workspace_size(2, 200, 4, 64) == lib.fa_bwd_workspace_size(
+        2, 4, 200, 64, 1)
+    assert lib.fa_bwd_varlen_workspace_size(2, 0, 4, 64) == 0
+
+
 def test_workspace_size(lib):
     f = lib.fa_bwd_workspace_size
     # D and L*log2(e), fp32, padded to 128-row blocks

@@ -5,7 +5,7 @@ and the full-size long-context ones (sampled heads, each compared in full:
 heads are independent), plus ragged and degenerate sizes."""
 import pytest
 
-from tests.parity_util import compare
+from tests.parity_util import compare, compare_varlen
 
 pytestmark = pytest.mark.gpu
 
@@ -103,3 +103,29 @@ def test_sliding_window_full_size_sampled():
     # 1 x 32 query heads x 8 K/V heads x 16384 x 128, bf16, window 4096; K/V heads 0 and 7
     # compared in full with their query heads
     print(compare(1, 32, 16384, 128, "bf16", True, heads=(0, 7), Hkv=8, window=4096))
+
+
+# Packed variable-length batches: (lengths, H, Hkv, d, dtype, causal, window)
+VARLEN_CASES = [
+    ((1, 127, 128, 129, 500, 37), 2, 2, 128, "bf16", True, 0),
+    ((300, 0, 64, 257), 4, 2, 128, "fp16", True, 0),        # an empty sequence, shared K/V
+    ((200, 383, 1), 2, 2, 128, "bf16", False, 0),
+    ((700, 90, 333), 4, 1, 128, "bf16", True, 100),          # MQA with a window
+    ((129, 64, 255), 2, 2, 64, "fp16", True, 0),
+    ((96, 400), 3, 1, 64, "bf16", False, 0),
+    ((33, 250, 130), 2, 2, 32, "fp16", True, 50),
+    ((1000,), 2, 2, 128, "bf16", True, 0),                   # one sequence
+]
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=[str(c) for c in VARLEN_CASES])
+def test_varlen(case):
+    lens, H, Hkv, d, dt, causal, W = case
+    print(case, compare_varlen(lens, H, d, dt, causal, Hkv=Hkv, window=W, seed=17))
+
+
+def test_varlen_many_sequences():
+    # 32 sequences from 1 to 2000 tokens, 8 query heads over 2 K/V heads, d = 128
+    import numpy as np
+    lens = tuple(int(x) for x in np.random.default_rng(5).integers(1, 2000, 32))
+    print(compare_varlen(lens, 8, 128, "bf16", True, Hkv=2, seed=19))
