@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_head = kb * BN >= sr.n ? 0
       : ((CAUSAL && window > 0) ? min(nq_r, (kb * BN + BN - 1 + window - 1) / BM + 1) : nq_r) - i0;
   const int n_iter = group * n_head;        // every query head of the group in turn
+  if (n_iter <= 0) return;                  // a key block past the end of its packed sequence
 
   auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };
   const int B_KV = 0;
@@ -407,6 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nk_r = (sr.n + BN - 1) / BN;                 // key blocks of this sequence
   const int j_lo = (CAUSAL && window > 0) ? max(0, qb * BM - window + 1) / BN : 0;
   const int n_iter = qb * BM >= sr.n ? 0 : (CAUSAL ? min(qb + 1, nk_r) : nk_r) - j_lo;
+  if (n_iter <= 0) return;                  // a query block past the end of its packed sequence
 
   auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };
   const int B_QF = 0;

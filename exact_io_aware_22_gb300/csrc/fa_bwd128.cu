@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       : ((CAUSAL && window > 0) ? min(nq_r, (kb * BT + BT - 1 + window - 1) / BT + 1) : nq_r) -
             q_start;
   const int n_iter = group * n_head;               // the group's query heads one after another
+  if (n_iter <= 0) return;                         // a key block past the end of its packed sequence
 
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
   const int B_KV = 0;
@@ -449,7 +450,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
 constexpr uint32_t DQ_COL = 0, S_COL = 128, DP_COL = 256, Z_COL = 384, QT_COL = 448;
 }  // namespace qd
 
-template <bool BF16, bool CAUSAL>
+template <bool BF16, bool CAUSAL, bool WINDOW, bool PACKED>
 __global__ void __launch_bounds__(THREADS, 1)
     dq128_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmdO, const void* __restrict__ Q,
@@ -471,12 +472,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bkv = bh / group;                      // the K/V head of this query head
   // key blocks j_lo .. diagonal; with a window of W keys, from the block holding the
   // tile's first row - W + 1
-  const int j_lo = (CAUSAL && window > 0) ? max(0, qb * BT - window + 1) / BT : 0;
-  const SeqRows sr = seq_rows(cu_seqlens, bh / H, N, total);
+  const int j_lo = WINDOW ? max(0, qb * BT - window + 1) / BT : 0;
+  const SeqRows sr = seq_rows_t<PACKED>(cu_seqlens, bh / H, N, total);
   const int hq = sr.packed ? bh % H : bh, hk = sr.packed ? (bh % H) / group : bkv;
   const int nk_r = (sr.n + BT - 1) / BT;           // key blocks of this sequence
   const int n_iter = qb * BT >= sr.n ? 0           // loop position j: key block j_lo + j
                                      : (CAUSAL ? min(qb + 1, nk_r) : nk_r) - j_lo;
+  if (n_iter <= 0) return;                         // a query tile past the end of its packed sequence
 
   auto bar = [&](int i) -> uint32_t { return sb + BAR_OFF + 8 * i; };
   const int B_DOF = 0;
@@ -648,15 +650,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < 64; ++c)
           if (k0 + c > grow) p[c] = 0.f;
       }
-      if (CAUSAL && window > 0 && qb * BT + BT - 1 - (j_lo + j) * BT >= window) {
+      if (WINDOW && qb * BT + BT - 1 - (j_lo + j) * BT >= window) {
         // window edge: zero where the query is W or more rows past the key
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (grow - (k0 + c) >= window) p[c] = 0.f;
       }
-      if (k0 + 64 > sr.n) {
-        // keys past the end of the sequence: zero-filled rows when dense, but the next
-        // sequence's keys when packed
+      if (PACKED && k0 + 64 > sr.n) {
+        // keys past the end of a packed sequence are the next sequence's keys (past N
+        // in a dense tensor they are zero-filled rows, whose dQ term vanishes)
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (k0 + c >= sr.n) p[c] = 0.f;
@@ -721,7 +723,12 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   {
-    auto kern = dq128_kernel<BF16, CAUSAL>;
+    // windowed and packed-sequence dQ kernels are separate instantiations
+    auto kern = CAUSAL && a.window > 0
+        ? (a.cu_seqlens ? dq128_kernel<BF16, CAUSAL, CAUSAL, true>
+                        : dq128_kernel<BF16, CAUSAL, CAUSAL, false>)
+        : (a.cu_seqlens ? dq128_kernel<BF16, CAUSAL, false, true>
+                        : dq128_kernel<BF16, CAUSAL, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          qd::SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -66,7 +66,7 @@ __device__ __forceinline__ uint32_t kmajor_koff(int kk) {
   return (e / C::ATOM) * C::CHUNK_BYTES + (e % C::ATOM) * 2;
 }
 
-template <int D, bool BF16, bool CAUSAL, bool WINDOW>
+template <int D, bool BF16, bool CAUSAL, bool WINDOW, bool PACKED>
 __global__ void __launch_bounds__(THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, void* __restrict__ Out,
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // Rows of this (batch, head): dense (B, H, N, d) maps are (d, N, B*H), a row at
   // (row, flat head); packed sequences (total, H, d) have maps (d, H, total), a row at
   // (head within the batch, first token + row), and their own length Nr.
-  const SeqRows sr = seq_rows(cu_seqlens, bh / H, N, total);
+  const SeqRows sr = seq_rows_t<PACKED>(cu_seqlens, bh / H, N, total);
   const int Nr = sr.n;
   const int hq = sr.packed ? bh % H : bh, hk = sr.packed ? (bh % H) / group : bkv;
   auto cy = [&](int r, int head) { return sr.y(r, head); };
@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int j0 = lo_t[0];                       // the stream starts at tile 0's first KV tile
   const int n_max = max(n_t[0], n_t[1]);
   const int n_stream = n_max - j0;              // KV tiles loaded, j0 .. n_max - 1
+  if (n_stream <= 0) return;                    // query tiles past the end of a packed sequence
 
   auto bar = [&](int i) -> uint32_t { return sb + C::BAR_OFF + 8 * i; };
   const int B_QF = 0;
@@ -381,10 +382,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int D, bool BF16, bool CAUSAL, bool WINDOW>
+template <int D, bool BF16, bool CAUSAL, bool WINDOW, bool PACKED>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = fwd_kernel<D, BF16, CAUSAL, WINDOW>;
+  auto kern = fwd_kernel<D, BF16, CAUSAL, WINDOW, PACKED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -409,24 +410,36 @@ FwdTileInfo fwd_tile_info(int d) {
   return t;
 }
 
-cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
-  // a sliding window is causal; the windowed kernels are separate instantiations so
-  // that the plain ones carry none of its bookkeeping
-  const bool window = causal && a.window > 0;
-#define FA_FWD_CASE(DD, BB, CC, WW)                                \
-  if (d == DD && bf16 == BB && causal == CC && window == WW) \
-    return launch_fwd_t<DD, BB, CC, WW>(a, st);
-  FA_FWD_CASE(32, false, false, false) FA_FWD_CASE(32, false, true, false)
-  FA_FWD_CASE(32, true, false, false) FA_FWD_CASE(32, true, true, false)
-  FA_FWD_CASE(64, false, false, false) FA_FWD_CASE(64, false, true, false)
-  FA_FWD_CASE(64, true, false, false) FA_FWD_CASE(64, true, true, false)
-  FA_FWD_CASE(128, false, false, false) FA_FWD_CASE(128, false, true, false)
-  FA_FWD_CASE(128, true, false, false) FA_FWD_CASE(128, true, true, false)
-  FA_FWD_CASE(32, false, true, true) FA_FWD_CASE(32, true, true, true)
-  FA_FWD_CASE(64, false, true, true) FA_FWD_CASE(64, true, true, true)
-  FA_FWD_CASE(128, false, true, true) FA_FWD_CASE(128, true, true, true)
-#undef FA_FWD_CASE
+template <bool BF16, bool CAUSAL, bool WINDOW, bool PACKED>
+cudaError_t launch_fwd_dd(const FwdArgs& a, int d, cudaStream_t st) {
+  if (d == 32) return launch_fwd_t<32, BF16, CAUSAL, WINDOW, PACKED>(a, st);
+  if (d == 64) return launch_fwd_t<64, BF16, CAUSAL, WINDOW, PACKED>(a, st);
+  if (d == 128) return launch_fwd_t<128, BF16, CAUSAL, WINDOW, PACKED>(a, st);
   return cudaErrorInvalidValue;
+}
+
+template <bool BF16>
+cudaError_t launch_fwd_b(const FwdArgs& a, int d, bool causal, bool window, bool packed,
+                         cudaStream_t st) {
+  if (!causal) return packed ? launch_fwd_dd<BF16, false, false, true>(a, d, st)
+                             : launch_fwd_dd<BF16, false, false, false>(a, d, st);
+  if (window) return packed ? launch_fwd_dd<BF16, true, true, true>(a, d, st)
+                            : launch_fwd_dd<BF16, true, true, false>(a, d, st);
+  return packed ? launch_fwd_dd<BF16, true, false, true>(a, d, st)
+                : launch_fwd_dd<BF16, true, false, false>(a, d, st);
+}
+
+cudaError_t launch_fwd_d(const FwdArgs& a, int d, bool bf16, bool causal, bool window, bool packed,
+                         cudaStream_t st) {
+  return bf16 ? launch_fwd_b<true>(a, d, causal, window, packed, st)
+              : launch_fwd_b<false>(a, d, causal, window, packed, st);
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
+  // a sliding window is causal; windowed and packed-sequence kernels are separate
+  // instantiations, so the plain dense ones carry none of their bookkeeping
+  const bool window = causal && a.window > 0, packed = a.cu_seqlens != nullptr;
+  return launch_fwd_d(a, d, bf16, causal, window, packed, st);
 }
 
 }  // namespace fa

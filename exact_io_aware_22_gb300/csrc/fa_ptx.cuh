@@ -350,6 +350,18 @@ __device__ __forceinline__ SeqRows seq_rows(const int* __restrict__ cu, int b, i
   const int e = min(max(__ldg(cu + b + 1), a), total);
   return {a, min(e - a, N), true};
 }
+// The same for a kernel instantiated for one layout: PACKED is then a compile-time
+// fact, and the dense instantiation carries none of the packed addressing.
+template <bool PACKED>
+__device__ __forceinline__ SeqRows seq_rows_t(const int* __restrict__ cu, int b, int N, int total) {
+  if constexpr (PACKED) {
+    const int a = min(max(__ldg(cu + b), 0), total);
+    const int e = min(max(__ldg(cu + b + 1), a), total);
+    return {a, min(e - a, N), true};
+  } else {
+    return {0, N, false};
+  }
+}
 
 // ---------------------------------------------------------------- numerics
 __device__ __forceinline__ float ex2(float x) {
