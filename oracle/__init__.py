@@ -22,6 +22,10 @@ Contents
     (total, H, d), K/V (total, Hkv, d), L (H, total), sequence b holding tokens
     cu_seqlens[b] .. cu_seqlens[b+1]-1.  Defined as attention of every sequence
     on its own, no token seeing another sequence's keys.
+  * ``decode``: one new query per sequence against a key/value cache of
+    cache_seqlens[b] rows (split-KV decoding, with the two-partial merge of the
+    tutorial page, "Softmax in pieces"): the plain safe softmax of the row over
+    all cached keys, K/V heads shared as in GQA.
   * ``window`` (fwd, bwd and the GQA pair): a causal sliding window of W keys,
     query i seeing keys i - W < j <= i (docs page "Scope" lists sliding windows
     as not yet supported and fixes no convention; this is the plain reading).
@@ -172,6 +176,26 @@ class Oracle:
             D[:, a:e] = Db[0]
         return dq, dk, dv, D
 
+    def decode(self, q, kc, vc, cache_seqlens, scale: float):
+        """O (B, H, d), L (B, H) of one query row per (batch, head) against the first
+        cache_seqlens[b] rows of the caches kc, vc (B, Hkv, Nmax, d); an empty cache gives
+        O = 0, L = -inf.  One key tile spanning the whole cache: the safe softmax."""
+        q, kc, vc = _f64(q), _f64(kc), _f64(vc)
+        B, H, d = q.shape
+        g = H // kc.shape[1]
+        o = np.zeros((B, H, d))
+        lse = np.full((B, H), -np.inf)
+        for b in range(B):
+            n = int(cache_seqlens[b])
+            if n == 0:
+                continue
+            for h in range(H):
+                m, l, acc = self.row_partial(q[b, h], kc[b, h // g, :n], vc[b, h // g, :n], 0, 0,
+                                             n, False, scale, n)
+                o[b, h] = acc / l
+                lse[b, h] = m + np.log(l)
+        return o, lse
+
     def fwd_online(self, q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):
         """O, L by the per-tile online update (docs page Fig. 3), key tiles of ``tile``."""
         q, k, v = _f64(q), _f64(k), _f64(v)
@@ -243,6 +267,10 @@ def fwd_varlen(q, k, v, cu_seqlens, causal: bool, scale: float, window: int = 0)
 
 def bwd_varlen(q, k, v, do, cu_seqlens, causal: bool, scale: float, window: int = 0):
     return get().bwd_varlen(q, k, v, do, cu_seqlens, causal, scale, window)
+
+
+def decode(q, kc, vc, cache_seqlens, scale: float):
+    return get().decode(q, kc, vc, cache_seqlens, scale)
 
 
 def fwd_online(q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):

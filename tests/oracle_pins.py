@@ -373,6 +373,29 @@ def pin_varlen(orc):
                f"varlen L {tag}")
 
 
+def pin_decode(orc):
+    """Split-KV decoding: the new query of sequence b against its first n_b cached keys is
+    the last row of the causal forward over those n_b rows (query n_b - 1 sees keys
+    0 .. n_b - 1), with K/V heads shared as in GQA; an empty cache gives O = 0, L = -inf.
+    The split/merge algebra itself is pinned by pin_merge."""
+    rng = np.random.default_rng(13)
+    B, H, Hkv, Nmax, d = 3, 4, 2, 50, 8
+    kc, vc = _rand(rng, B, Hkv, Nmax, d), _rand(rng, B, Hkv, Nmax, d)
+    q = _rand(rng, B, H, d)
+    lens = (37, 0, 50)
+    o, lse = orc.decode(q, kc, vc, lens, 0.4)
+    for b, n in enumerate(lens):
+        if n == 0:
+            _close(o[b], np.zeros((H, d)), 0.0, "empty cache: O = 0")
+            assert np.all(lse[b] == -np.inf), "empty cache: L = -inf"
+            continue
+        qq = np.zeros((1, H, n, d))
+        qq[0, :, n - 1] = q[b]
+        of, lf = orc.fwd_gqa(qq, kc[b:b + 1, :, :n], vc[b:b + 1, :, :n], True, 0.4)
+        _close(o[b], of[0, :, n - 1], 1e-12, f"decode O = last causal row (n={n})")
+        _close(lse[b], lf[0, :, n - 1], 1e-12, f"decode L = last causal row (n={n})")
+
+
 def pin_page_sizes(iomodel):
     """Sizes the pages print (tests/golden/page_sizes.json) from the byte model."""
     with open(os.path.join(GOLDEN, "page_sizes.json")) as f:
@@ -390,4 +413,5 @@ def pin_page_sizes(iomodel):
 
 ORACLE_PINS = [pin_rows_sum_to_one, pin_constant_keys, pin_causal_first_row,
                pin_online_matches_safe, pin_L_is_logsumexp, pin_merge, pin_finite_differences,
-               pin_gradient_invariants, pin_torch_sdpa, pin_gqa, pin_window, pin_varlen]
+               pin_gradient_invariants, pin_torch_sdpa, pin_gqa, pin_window, pin_varlen,
+               pin_decode]

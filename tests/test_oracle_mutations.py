@@ -84,6 +84,11 @@ def test_mutant_is_caught(name, tmp_path):
 # real compiled core.
 PY_SRC = os.path.join(os.path.dirname(oracle.__file__), "__init__.py")
 GQA_MUTANTS = {
+    "decode: last cached key dropped": (
+        "m, l, acc = self.row_partial(q[b, h], kc[b, h // g, :n], vc[b, h // g, :n], 0, 0,\n"
+        "                                             n, False, scale, n)",
+        "m, l, acc = self.row_partial(q[b, h], kc[b, h // g, :n], vc[b, h // g, :n], 0, 0,\n"
+        "                                             n - 1, False, scale, n)"),
     "varlen: a sequence sees the next one's first key": (
         "qs, ks, vs = (x[a:e].transpose(1, 0, 2)[None] for x in (q, k, v))",
         "qs, ks, vs = (x[a:min(e + 1, total)].transpose(1, 0, 2)[None] for x in (q, k, v))"),
@@ -110,5 +115,7 @@ def test_gqa_mutant_is_caught(name):
     with pytest.raises((AssertionError, ValueError)):
         if name.startswith("varlen"):
             pins.pin_varlen(orc)
+        elif name.startswith("decode"):
+            pins.pin_decode(orc)
         else:
             pins.pin_gqa(orc, shapes=((1, 4, 2, 21, 8, True),))
