@@ -55,6 +55,18 @@ WORKLOADS = {
 VARLEN_WORKLOADS = {
     "varlen64_gqa8_d128_bf16": (64, 256, 8192, 32, 8, 128, "bf16", True),
 }
+# split-KV decoding: name: (B, H, Hkv, Nmax, d, dtype); one query row per (batch, head)
+# against K/V caches of lengths uniform in [Nmax/2, Nmax] from a fixed seed
+DECODE_WORKLOADS = {
+    "decode_b16_gqa8_kv32k_d128_bf16": (16, 32, 8, 32768, 128, "bf16"),
+}
+DECODE_METRIC = "split-KV decode KV-cache read GB/s (B=16,H=32,Hkv=8,cache<=32K,d=128,bf16)"
+
+
+def decode_lengths(name):
+    import numpy as np
+    B, _, _, Nmax = DECODE_WORKLOADS[name][:4]
+    return [int(x) for x in np.random.default_rng(2027).integers(Nmax // 2, Nmax + 1, B)]
 
 
 def varlen_lengths(name):
@@ -76,6 +88,7 @@ KERNEL_SOURCES = {
     "bwd_pre_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
     "bwd_dkdv_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd128.cu",
     "bwd_dq_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd128.cu",
+    "decode_split_kernel": "exact_io_aware_22_gb300/csrc/fa_decode.cu",
 }
 
 
@@ -114,7 +127,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOADS) + list(VARLEN_WORKLOADS),
+    ap.add_argument("--workload",
+                    choices=list(WORKLOADS) + list(VARLEN_WORKLOADS) + list(DECODE_WORKLOADS),
                     default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -459,13 +473,201 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(out), flush=True)
 
 
+def decode_bytes(lens, H, Hkv, d):
+    """Algorithmic HBM bytes of one decoding step: every cached K and V row in use read
+    once (16-bit), q read, O written, L written."""
+    return sum(lens) * Hkv * d * 2 * 2 + len(lens) * H * (d * 2 * 2 + 4)
+
+
+def decode_cpu_sample(x, lens, H, Hkv, d, scale, budget_s=10.0):
+    """Time the fp64 oracle's decode as it stands on the host cores, whole batch entries
+    (all heads) at a time until ``budget_s`` is spent (at least one)."""
+    import oracle
+    done, t_total, nbytes = 0, 0.0, 0
+    B = len(lens)
+    while done < B and (done == 0 or t_total < budget_s):
+        sl = slice(done, done + 1)
+        q = x["q"][sl].double().numpy()
+        kc = x["k_cache"][sl, :, :lens[done]].double().numpy()
+        vc = x["v_cache"][sl, :, :lens[done]].double().numpy()
+        t0 = time.perf_counter()
+        oracle.decode(q, kc, vc, [lens[done]], scale)
+        t_total += time.perf_counter() - t0
+        nbytes += decode_bytes([lens[done]], H, Hkv, d)
+        done += 1
+    return nbytes / t_total / 1e9, done, t_total
+
+
+def run_decode_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from exact_io_aware_22_gb300 import inputs
+    B, H, Hkv, Nmax, d, dtype = DECODE_WORKLOADS[args.workload]
+    lens = decode_lengths(args.workload)
+    scale = 1.0 / math.sqrt(d)
+    x = inputs.make_decode_inputs(B, H, Hkv, Nmax, d, lens, dtype, seed=0)
+
+    def step(i):
+        b = i % B
+        oracle.decode(x["q"][b:b + 1].double().numpy(),
+                      x["k_cache"][b:b + 1, :, :lens[b]].double().numpy(),
+                      x["v_cache"][b:b + 1, :, :lens[b]].double().numpy(), [lens[b]], scale)
+        return decode_bytes([lens[b]], H, Hkv, d)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    nbytes = sum(step(args.warmup + i) for i in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    sample = f"one batch entry (all {H} heads, its whole cache) per step, fp64 oracle"
+    out = {"metric": DECODE_METRIC, "value": value, "unit": "GB/s", "impl": "reference",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": args.workload, "B": B, "H": H, "Hkv": Hkv, "Nmax": Nmax,
+                      "d": d, "step_unit": "one batch entry"},
+           "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def run_decode(args, rank, world, local_rank):
+    """One step = one decoding call over the whole batch (split kernel + merge kernel)."""
+    import torch
+    import torch.distributed as dist
+
+    import exact_io_aware_22_gb300 as fa
+    from exact_io_aware_22_gb300 import inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    B, H, Hkv, Nmax, d, dtype = DECODE_WORKLOADS[args.workload]
+    lens = decode_lengths(args.workload)
+    scale = 1.0 / math.sqrt(d)
+    x = inputs.make_decode_inputs(B, H, Hkv, Nmax, d, lens, dtype, seed=rank)
+    q, kc, vc, cl = (x[n].to(dev) for n in ("q", "k_cache", "v_cache", "cache_seqlens"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.decode_workspace_size(B, H, Hkv, Nmax, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    alg_bytes = decode_bytes(lens, H, Hkv, d)
+    flops = 4.0 * sum(lens) * H * d
+
+    def step():
+        fa.decode(q, kc, vc, cl, scale=scale, out=o, lse=lse, workspace=ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.device_status() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout during warm-up")
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.2)
+    barrier()
+    torch.cuda.synchronize()
+    fa.trace_enable(True)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    fa.trace_enable(False)
+    clocks = sampler.stop()
+    if fa.device_status() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
+    value = world * alg_bytes / (ms / 1e3) / 1e9
+    traced = {kk: v for kk, v in fa.trace_read().items() if v[1] > 0}
+    launches = sum(n for _, n in traced.values())
+    per = {kk: tot / n for kk, (tot, n) in traced.items()}
+    peaks = load_peaks()
+    split_ms = per["decode_split_kernel"]
+    achieved = alg_bytes / (split_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": traffic_from_profiles("decode_split_kernel", args.workload),
+                "peak_source": f"{peaks['source']} (burst)",
+                "algorithmic_work_per_launch": alg_bytes, "avg_launch_ms": split_ms}
+
+    e2e = None
+    if not args.no_e2e:
+        hx = {n: x[n].pin_memory() for n in ("q", "k_cache", "v_cache", "cache_seqlens")}
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dst = {"q": q, "k_cache": kc, "v_cache": vc, "cache_seqlens": cl}
+
+        def e2e_step():
+            for n, t in hx.items():
+                dst[n].copy_(t, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        ke = max(1, min(args.steps, 10))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
+        e2e = {"value": world * alg_bytes / (ems / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hx.values()),
+               "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * 4,
+               "ms_per_step": ems, "steps": ke,
+               "note": "the whole K/V cache is copied host to device every step"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        v_cpu, done, t_cpu = decode_cpu_sample(x, lens, H, Hkv, d, scale)
+        cpu = {"value": v_cpu, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{done} of {B} batch entries (all heads, whole caches), "
+                         f"{t_cpu:.1f} s on host cores"}
+    if rank == 0:
+        out = {"metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+               "data": "synthetic",
+               "config": {"workload": args.workload, "B": B, "H": H, "Hkv": Hkv, "Nmax": Nmax,
+                          "d": d, "cached_keys": sum(lens),
+                          "lengths": f"uniform {Nmax // 2}..{Nmax}, seed 2027",
+                          "parallelism": f"replicas x{world}",
+                          "l2": f"inputs larger than L2 ({alg_bytes >> 20} MiB of K/V rows "
+                                "read per step), no flush"},
+               "tflops": world * flops / (ms / 1e3) / 1e12,
+               "kernels_ms": per, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+               "gpu_launches": launches, "clocks": clocks}
+        print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    decode = args.workload in DECODE_WORKLOADS
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        (run_decode_reference if decode else run_reference)(args, rank, world)
         return
     if world > 1:
         import torch
@@ -473,7 +675,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        run_ours(args, rank, world, local_rank)
+        (run_decode if decode else run_ours)(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

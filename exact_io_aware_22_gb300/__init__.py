@@ -77,6 +77,10 @@ def load_library(path: str | None = None):
     lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, i, i, i, i, i, i,
                                   i, i, f, i, vp]
     lib.fa_bwd_varlen.restype = i
+    lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_decode_workspace_size.restype = sz
+    lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
+    lib.fa_decode.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_cuda_error.restype = i
@@ -308,6 +312,46 @@ def bwd_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen: int, causal: bool = 
         ws_ptr, ws_bytes, _ptr(cu_seqlens), B, total, int(max_seqlen), H, Hkv, d, int(causal),
         window, float(scale), _dtype_code(q), _stream()), "fa_bwd_varlen")
     return dq, dk, dv
+
+
+def decode_workspace_size(B: int, H: int, Hkv: int, Nmax: int, d: int) -> int:
+    return int(load_library().fa_decode_workspace_size(B, H, Hkv, Nmax, d))
+
+
+def decode(q, k_cache, v_cache, cache_seqlens, scale: float | None = None, out=None, lse=None,
+           workspace=None):
+    """O (B, H, d), L (B, H) fp32 of one query row per (batch, head) against the first
+    cache_seqlens[b] rows of k_cache, v_cache (B, Hkv, Nmax, d); cache_seqlens is an
+    int32 CUDA tensor of B lengths.  Query head h uses K/V head h // (H // Hkv).  A
+    sequence with no cached key gets O = 0, L = -inf.  ``workspace``: an optional uint8
+    CUDA tensor of at least decode_workspace_size(...) bytes (else one is allocated
+    per call on the current stream)."""
+    import torch
+    _need_cuda(q, k_cache, v_cache, cache_seqlens)
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("q must be (B, H, d) and the caches one (B, Hkv, Nmax, d) shape")
+    B, H, d = q.shape
+    Bk, Hkv, Nmax, dk = k_cache.shape
+    if Bk != B or dk != d or Hkv < 1 or H % Hkv:
+        raise ValueError("caches must be (B, Hkv, Nmax, d) with H a multiple of Hkv")
+    if cache_seqlens.dtype != torch.int32 or cache_seqlens.shape != (B,):
+        raise ValueError("cache_seqlens must be an int32 tensor of B lengths")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need_cuda(out, lse)
+    if out.shape != q.shape or out.dtype != q.dtype or lse.shape != (B, H) \
+            or lse.dtype != torch.float32:
+        raise ValueError("out must match q; lse must be (B, H) fp32")
+    ws, ws_bytes = None, 0
+    if workspace is not None:
+        _need_cuda(workspace)
+        ws, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    _check(load_library().fa_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens), _ptr(out), _ptr(lse), ws,
+        ws_bytes, B, H, Hkv, Nmax, d, float(scale), _dtype_code(q), _stream()), "fa_decode")
+    return out, lse
 
 
 def device_status() -> int:

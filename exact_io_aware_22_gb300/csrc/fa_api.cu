@@ -161,8 +161,9 @@ bool g_trace_on = false;
 int g_trace_n = 0;
 int g_trace_open = -1;   // record whose stop event is pending
 
-const char* const kTraceNames[fa::TR_NKINDS] = {"fwd_kernel", "bwd_pre_kernel", "bwd_dkdv_kernel",
-                                                "bwd_dq_kernel"};
+const char* const kTraceNames[fa::TR_NKINDS] = {"fwd_kernel",      "bwd_pre_kernel",
+                                                 "bwd_dkdv_kernel", "bwd_dq_kernel",
+                                                 "decode_split_kernel", "decode_merge_kernel"};
 
 }  // namespace
 
@@ -489,6 +490,84 @@ fa_status fa_bwd_varlen(const void* Q, const void* K, const void* V, const void*
   if (!cu_seqlens || window < 0 || (window > 0 && !causal)) return FA_ERR_INVALID_VALUE;
   return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, B, H, Hkv, max_seqlen,
                   d, causal, scale, dtype, stream, window, cu_seqlens, total);
+}
+
+// Split-KV decoding: one query row per (batch, head) against the first
+// cache_seqlens[b] rows of K/V caches (B, Hkv, Nmax, d).
+size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nmax, int d) {
+  if (check_common(B, H, Nmax, d, 0, 1.0f, FA_FP16) != FA_OK || check_heads(H, Hkv) != FA_OK)
+    return 0;
+  int chunk = 0;
+  const int splits = fa::decode_parts(B, H, Hkv, Nmax, &chunk);
+  return static_cast<size_t>(B) * H * splits * (d + 4) * sizeof(float);
+}
+
+fa_status fa_decode(const void* Q, const void* Kc, const void* Vc, const int* cache_seqlens,
+                    void* O, float* L, void* workspace, size_t workspace_bytes, int B, int H,
+                    int Hkv, int Nmax, int d, float scale, fa_dtype dtype, void* stream) {
+  fa_status st = check_common(B, H, Nmax, d, 0, scale, static_cast<int>(dtype));
+  if (st != FA_OK) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
+  if (Nmax > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if (!Q || !Kc || !Vc || !cache_seqlens || !O || !L) return FA_ERR_INVALID_VALUE;
+  if (!aligned(Q, 16) || !aligned(Kc, 16) || !aligned(Vc, 16) || !aligned(O, 16) ||
+      !aligned(L, 4) || !aligned(cache_seqlens, 4) || (workspace && !aligned(workspace, 16)))
+    return FA_ERR_MISALIGNED;
+  int chunk = 0;
+  const int splits = fa::decode_parts(B, H, Hkv, Nmax, &chunk);
+  const long long ctas = static_cast<long long>(B) * Hkv * splits *
+                         ((H / Hkv) / fa::decode_rows(H, Hkv));
+  if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const size_t need = fa_decode_workspace_size(B, H, Hkv, Nmax, d);
+  if (workspace && workspace_bytes < need) return FA_ERR_INVALID_VALUE;
+  const size_t qbytes = static_cast<size_t>(B) * H * d * 2, lbytes = static_cast<size_t>(B) * H * 4;
+  const size_t cbytes = static_cast<size_t>(B) * Hkv * Nmax * d * 2;
+  const void* ins[4] = {Q, Kc, Vc, cache_seqlens};
+  const size_t insz[4] = {qbytes, cbytes, cbytes, static_cast<size_t>(B) * 4};
+  for (int i = 0; i < 4; ++i) {
+    if (overlap(ins[i], insz[i], O, qbytes) || overlap(ins[i], insz[i], L, lbytes))
+      return FA_ERR_INVALID_VALUE;
+    if (workspace && overlap(ins[i], insz[i], workspace, need)) return FA_ERR_INVALID_VALUE;
+  }
+  if (overlap(O, qbytes, L, lbytes)) return FA_ERR_INVALID_VALUE;
+  if (workspace && (overlap(workspace, need, O, qbytes) || overlap(workspace, need, L, lbytes)))
+    return FA_ERR_INVALID_VALUE;
+
+  const bool bf16 = dtype == FA_BF16;
+  fa::DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const long long BHkv = static_cast<long long>(B) * Hkv;
+  const int rows = fa::decode_key_rows(d);
+  if ((st = make_map(&a.tmK, Kc, d, Nmax, BHkv, bf16, rows)) != FA_OK) return st;
+  if ((st = make_map(&a.tmV, Vc, d, Nmax, BHkv, bf16, rows)) != FA_OK) return st;
+  if ((st = ctl_for_launch(&a.ctl)) != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  bool owned = false;
+  if (!ws) {
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    owned = true;
+  }
+  a.Q = Q;
+  a.seqlens = cache_seqlens;
+  a.O = O;
+  a.L = L;
+  a.part = static_cast<float*>(ws);
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Nmax = Nmax;
+  a.n_splits = splits;
+  a.chunk = chunk;
+  a.c_log2 = scale * 1.4426950408889634f;
+  cudaError_t e = fa::launch_decode(a, d, bf16, s);
+  if (owned) {
+    cudaError_t e2 = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
 }
 
 }  // extern "C"

@@ -17,7 +17,9 @@ enum TraceKind {
   TR_BWD_PRE = 1,
   TR_BWD_DKDV = 2,
   TR_BWD_DQ = 3,
-  TR_NKINDS = 4
+  TR_DEC_SPLIT = 4,
+  TR_DEC_MERGE = 5,
+  TR_NKINDS = 6
 };
 // Record an event before / after one kernel launch on `st` (no-op unless tracing).
 void trace_begin(int kind, cudaStream_t st);
@@ -70,5 +72,25 @@ cudaError_t launch_bwd(const BwdArgs& a, int d, bool bf16, bool causal, cudaStre
 cudaError_t launch_bwd128(const BwdArgs& a, bool bf16, bool causal, cudaStream_t st);
 // Workspace: D and L*log2(e) per padded row.
 size_t bwd_workspace_bytes(long long BH, int N, int d);
+
+struct DecodeArgs {
+  CUtensorMap tmK, tmV;        // 3-D maps (d, Nmax, B*Hkv) of the caches, box decode_key_rows(d) rows
+  const void* Q;               // (B, H, d) one query row per head
+  const int* seqlens;          // device int32 [B]: cached keys per sequence
+  void* O;                     // (B, H, d)
+  float* L;                    // (B, H) fp32, natural log
+  float* part;                 // workspace: (B*H, n_splits, d+4) partial states
+  int B, H, Hkv, Nmax;
+  int n_splits, chunk;         // splits of the cache and keys per split
+  float c_log2;                // scale * log2(e)
+  KernelCtl ctl;
+};
+// Query rows that one decode CTA serves from each K/V row (a power of two dividing H/Hkv).
+int decode_rows(int H, int Hkv);
+// Keys per ring stage of the decode kernel (the TMA box height).
+int decode_key_rows(int d);
+// Splits and keys per split (written to *chunk) for caches of Nmax keys.
+int decode_parts(int B, int H, int Hkv, int Nmax, int* chunk);
+cudaError_t launch_decode(const DecodeArgs& a, int d, bool bf16, cudaStream_t st);
 
 }  // namespace fa

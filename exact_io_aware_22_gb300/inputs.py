@@ -8,7 +8,8 @@ order Q, K, V, dO, each i.i.d. N(0, 1) in fp32 of shape (B, H, N, d); Q and K
 are then multiplied by ``qk_std`` (4 for the large-row-maximum stress case);
 finally every tensor is rounded to the 16-bit dtype.  The oracle consumes the
 rounded values upcast exactly to fp64.  With ``Hkv`` (grouped-query attention)
-K and V are drawn with Hkv heads instead of H, in the same order.
+K and V are drawn with Hkv heads instead of H, in the same order.  Decoding
+inputs draw one query row per (batch, head) and then the K and V caches.
 """
 from __future__ import annotations
 
@@ -53,6 +54,30 @@ def make_packed_inputs(lens, H: int, d: int, dtype: str = "bf16", seed: int = 0,
     cu[1:] = torch.cumsum(torch.tensor(list(lens), dtype=torch.int64), 0).to(torch.int32)
     t = DTYPES[dtype]
     return {"q": q.to(t), "k": k.to(t), "v": v.to(t), "do": do.to(t), "cu_seqlens": cu}
+
+
+def make_decode_inputs(B: int, H: int, Hkv: int, Nmax: int, d: int, lens, dtype: str = "bf16",
+                       seed: int = 0, fill: float | None = None):
+    """One query row per (batch, head) and K/V caches: dict(q (B, H, d), k_cache, v_cache
+    (B, Hkv, Nmax, d)) of CPU tensors in ``dtype``, drawn in that order i.i.d. N(0, 1),
+    plus cache_seqlens (int32, the B values of ``lens``).  With ``fill`` every cache row
+    at or past its sequence's length is overwritten with that value (e.g. NaN), rows
+    that no result may depend on."""
+    if len(lens) != B:
+        raise ValueError("lens must hold B lengths")
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((B, H, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, Hkv, Nmax, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, Hkv, Nmax, d), generator=g, dtype=torch.float32)
+    t = DTYPES[dtype]
+    q, k, v = q.to(t), k.to(t), v.to(t)
+    if fill is not None:
+        for b, n in enumerate(lens):
+            k[b, :, int(n):] = fill
+            v[b, :, int(n):] = fill
+    return {"q": q, "k_cache": k, "v_cache": v,
+            "cache_seqlens": torch.tensor([int(n) for n in lens], dtype=torch.int32)}
 
 
 # Workloads: (name, B, H, N, d, dtype, causal, qk_std)

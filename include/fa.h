@@ -144,6 +144,35 @@ fa_status fa_bwd_varlen(const void* Q, const void* K, const void* V, const void*
                         int total, int max_seqlen, int H, int Hkv, int d, int causal, int window,
                         float scale, fa_dtype dtype, void* stream);
 
+/* Split-KV decoding: one new query row per (batch, head) attends to the first
+ * cache_seqlens[b] cached keys of its sequence.  The key range is cut into
+ * pieces whose softmax partial states (running max m, sum l, unnormalised
+ * output acc) are merged exactly on the GPU: the tutorial page "What is
+ * FlashAttention?", "Softmax in pieces" (merging two partial results), applied
+ * to a key/value cache (the FlashAttention note lists inference serving with a
+ * KV cache among the method's uses: "Applications and Use Cases").
+ *   Q            (B, H, d) fp16/bf16, one query row per head.
+ *   Kc, Vc       (B, Hkv, Nmax, d) caches; rows at and past cache_seqlens[b]
+ *                are never used (their contents may be anything).
+ *   cache_seqlens  device int32 [B]; values are clamped to [0, Nmax].  A
+ *                sequence with no cached key gets O = 0, L = -inf.
+ *   O            (B, H, d) output, same dtype.
+ *   L            (B, H) fp32, the natural-log logsumexp of each row's scores.
+ *   workspace    fa_decode_workspace_size(B, H, Hkv, Nmax, d) bytes of device
+ *                memory (16-byte aligned) for the partial states, or NULL: the
+ *                library then allocates and frees it on `stream`.
+ *   Query head h uses K/V head h / (H / Hkv).  Q, Kc, Vc and O 16-byte aligned.
+ *   Errors: FA_ERR_INVALID_VALUE for NULL pointers, B, H or Nmax < 1, H not a
+ *   multiple of Hkv, a non-positive or non-finite scale, a short workspace or
+ *   overlapping buffers; FA_ERR_UNSUPPORTED for d not 32/64/128, another dtype,
+ *   Nmax above 2^30 or sizes past the index limits; FA_ERR_MISALIGNED for the
+ *   alignment rules.
+ *   Asynchronous on `stream`; nothing is read back. */
+size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nmax, int d);
+fa_status fa_decode(const void* Q, const void* Kc, const void* Vc, const int* cache_seqlens,
+                    void* O, float* L, void* workspace, size_t workspace_bytes, int B, int H,
+                    int Hkv, int Nmax, int d, float scale, fa_dtype dtype, void* stream);
+
 /* Static description of a status code. */
 const char* fa_status_string(fa_status s);
 
@@ -178,7 +207,8 @@ fa_status fa_selftest_timeout(unsigned long long limit_ns, void* stream);
 fa_status fa_trace_enable(int on);
 
 /* Name of trace kind `kind` (0: forward kernel, 1: backward pre-pass, 2:
- * backward dK/dV kernel, 3: backward dQ kernel); NULL when out of range. */
+ * backward dK/dV kernel, 3: backward dQ kernel, 4: decode split kernel, 5:
+ * decode merge kernel); NULL when out of range. */
 const char* fa_trace_kind_name(int kind);
 
 /* Waits for the recorded events of kind `kind`, then writes the summed GPU

@@ -188,3 +188,37 @@ def test_binding_refuses_without_library(tmp_path):
     import exact_io_aware_22_gb300 as fa
     with pytest.raises(RuntimeError, match="not built"):
         fa.load_library(str(tmp_path / "missing.so"))
+
+
+def decode(lib, **kw):
+    a = dict(Q=M1, K=2 * M1, V=3 * M1, lens=4 * M1, O=5 * M1, L=6 * M1, ws=0, ws_bytes=0, B=2,
+             H=8, Hkv=2, Nmax=300, d=64, scale=0.125, dtype=1)
+    a.update(kw)
+    ptrs = [ctypes.c_void_p(a[k]) for k in ("Q", "K", "V", "lens", "O", "L", "ws")]
+    return lib.fa_decode(*ptrs, a["ws_bytes"], a["B"], a["H"], a["Hkv"], a["Nmax"], a["d"],
+                         a["scale"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Q=0), INVALID), (dict(lens=0), INVALID), (dict(L=0), INVALID),
+    (dict(B=0), INVALID), (dict(Nmax=0), INVALID), (dict(Hkv=3), INVALID),
+    (dict(Hkv=0), INVALID), (dict(scale=0.0), INVALID), (dict(scale=float("nan")), INVALID),
+    (dict(d=48), UNSUPPORTED), (dict(dtype=7), UNSUPPORTED), (dict(Nmax=(1 << 30) + 1), UNSUPPORTED),
+    (dict(K=2 * M1 + 8), MISALIGNED), (dict(lens=4 * M1 + 2), MISALIGNED),
+    (dict(O=M1 + 512), INVALID),                        # O inside Q (2 x 8 x 64 x 2 bytes)
+    (dict(O=3 * M1 + 4096), INVALID),                   # O inside the V cache
+    (dict(ws=8 * M1, ws_bytes=16), INVALID),            # workspace too small
+    (dict(ws=5 * M1 + 64, ws_bytes=1 << 19), INVALID),  # workspace over O
+])
+def test_decode_rejects(lib, kw, code):
+    assert decode(lib, **kw) == code
+
+
+def test_decode_workspace_size(lib):
+    f = lib.fa_decode_workspace_size
+    # (B*H rows) x splits partial states of d + 4 floats.  16 x 8 K/V heads, 32768
+    # cached keys: 128 CTA rows, 19 splits of 1728 keys (a multiple of 64)
+    assert f(16, 32, 8, 32768, 128) == 16 * 32 * 19 * 132 * 4
+    # one key: one split
+    assert f(1, 1, 1, 1, 32) == 1 * 1 * 1 * 36 * 4
+    assert f(0, 1, 1, 1, 32) == 0 and f(1, 4, 3, 10, 64) == 0 and f(1, 1, 1, 10, 48) == 0
