@@ -9,7 +9,8 @@ are then multiplied by ``qk_std`` (4 for the large-row-maximum stress case);
 finally every tensor is rounded to the 16-bit dtype.  The oracle consumes the
 rounded values upcast exactly to fp64.  With ``Hkv`` (grouped-query attention)
 K and V are drawn with Hkv heads instead of H, in the same order.  Decoding
-inputs draw one query row per (batch, head) and then the K and V caches.
+inputs draw one query row per (batch, head) and then the K and V caches.  FP8
+inputs are the fp32 draws divided by a per-tensor scale and rounded to E4M3.
 """
 from __future__ import annotations
 
@@ -78,6 +79,27 @@ def make_decode_inputs(B: int, H: int, Hkv: int, Nmax: int, d: int, lens, dtype:
             v[b, :, int(n):] = fill
     return {"q": q, "k_cache": k, "v_cache": v,
             "cache_seqlens": torch.tensor([int(n) for n in lens], dtype=torch.int32)}
+
+
+def make_fp8_inputs(B: int, H: int, N: int, d: int, seed: int = 0, Hkv: int | None = None):
+    """8-bit E4M3 inputs with per-tensor scales: Q, K, V drawn like make_inputs (fp32
+    N(0, 1), in that order), each divided by its scale amax / 448 (so the largest
+    magnitude lands on the largest finite E4M3 value) and rounded to E4M3 by torch's
+    float8_e4m3fn conversion (round to nearest even).  Returns dict(q8, k8, v8, vt8)
+    of uint8 code tensors -- q8 (B, H, N, d), k8 and v8 (B, Hkv, N, d), vt8 = v8 with
+    the last two axes swapped (B, Hkv, d, N) -- and the scales q_scale, k_scale,
+    v_scale (Python floats, exact fp32 values)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    kvh = H if Hkv is None else Hkv
+    out = {}
+    for name, heads in (("q", H), ("k", kvh), ("v", kvh)):
+        x = torch.randn((B, heads, N, d), generator=g, dtype=torch.float32)
+        sc = torch.tensor(float(x.abs().max()) / 448.0, dtype=torch.float32)
+        out[name + "8"] = (x / sc).to(torch.float8_e4m3fn).view(torch.uint8)
+        out[name + "_scale"] = float(sc)
+    out["vt8"] = out["v8"].transpose(-1, -2).contiguous()
+    return out
 
 
 # Workloads: (name, B, H, N, d, dtype, causal, qk_std)

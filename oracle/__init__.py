@@ -29,6 +29,10 @@ Contents
   * ``window`` (fwd, bwd and the GQA pair): a causal sliding window of W keys,
     query i seeing keys i - W < j <= i (docs page "Scope" lists sliding windows
     as not yet supported and fixes no convention; this is the plain reading).
+  * ``e4m3_values``/``fwd_fp8``: attention on 8-bit E4M3 inputs (the FP8 of
+    the note's FlashAttention-3 entry, "Versions and Evolution") with per-tensor
+    descale factors, defined as the exact attention of the values the codes
+    stand for; the codes are decoded from the format's definition.
   * ``fwd_online``/``row_partial``/``merge``: the separate naive online-softmax
     oracle of the docs page's Fig. 3 and the two-partial merge of the tutorial
     page ("Softmax in pieces").
@@ -196,6 +200,30 @@ class Oracle:
                 lse[b, h] = m + np.log(l)
         return o, lse
 
+    @staticmethod
+    def e4m3_values(codes) -> np.ndarray:
+        """fp64 values of 8-bit E4M3 codes: sign bit 7, exponent bits 6..3 with bias 7,
+        mantissa bits 2..0; exponent field 0 holds the subnormals (m/8) 2^-6; the
+        pattern with every exponent and mantissa bit set is NaN, and there is no
+        infinity (the E4M3 variant of the OCP 8-bit floating-point formats)."""
+        c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+        sign = np.where(c & 0x80, -1.0, 1.0)
+        e = (c >> 3) & 0xF
+        m = (c & 0x7).astype(np.float64)
+        mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+        return np.where((e == 15) & (m == 7), np.nan, sign * mag)
+
+    def fwd_fp8(self, q8, k8, v8, q_scale: float, k_scale: float, v_scale: float, causal: bool,
+                scale: float):
+        """O, L of attention on 8-bit E4M3 inputs with per-tensor descale factors: the
+        exact attention of q_scale Q, k_scale K, v_scale V, the values the codes stand
+        for (q8 (B, H, N, d); k8, v8 (B, Hkv, N, d), shared as in GQA).  FP8 is the
+        precision the note's FlashAttention-3 entry adds ("Versions and Evolution")."""
+        q = self.e4m3_values(q8) * q_scale
+        k = self.e4m3_values(k8) * k_scale
+        v = self.e4m3_values(v8) * v_scale
+        return self.fwd_gqa(q, k, v, causal, scale)
+
     def fwd_online(self, q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):
         """O, L by the per-tile online update (docs page Fig. 3), key tiles of ``tile``."""
         q, k, v = _f64(q), _f64(k), _f64(v)
@@ -271,6 +299,14 @@ def bwd_varlen(q, k, v, do, cu_seqlens, causal: bool, scale: float, window: int 
 
 def decode(q, kc, vc, cache_seqlens, scale: float):
     return get().decode(q, kc, vc, cache_seqlens, scale)
+
+
+def e4m3_values(codes):
+    return Oracle.e4m3_values(codes)
+
+
+def fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool, scale: float):
+    return get().fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal, scale)
 
 
 def fwd_online(q, k, v, causal: bool, scale: float, tile: int, base2: bool = False):

@@ -411,7 +411,45 @@ def pin_page_sizes(iomodel):
     assert abs(r / c3["ratio_approx"] - 1) <= c3["rel_tol"]
 
 
+def pin_fp8(orc):
+    """8-bit E4M3 inputs.  The code table against torch's float8_e4m3fn decoding
+    (library) over all 256 codes, plus closed forms of the format (1.0, the largest
+    finite value 448, the smallest normal 2^-6 and subnormal 2^-9, NaN patterns).
+    Attention on the codes: torch SDPA (fp64, enable_gqa) on the decoded values;
+    the descale factors enter as q_scale k_scale times the softmax scale (powers of
+    two: exact) and v_scale multiplies O and leaves L."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    got = orc.e4m3_values(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2, "E4M3 NaN codes"
+    assert np.array_equal(got[~nan], ref[~nan]), "E4M3 code table vs torch"
+    for c, val in ((0x38, 1.0), (0x7E, 448.0), (0x08, 2.0 ** -6), (0x01, 2.0 ** -9),
+                   (0xB8, -1.0), (0x00, 0.0), (0x44, 3.0)):
+        assert orc.e4m3_values([c])[0] == val, f"E4M3 code {c:#x} = {val}"
+    rng = np.random.default_rng(14)
+    for B, H, Hkv, N, d, causal in ((1, 4, 2, 40, 16, True), (2, 2, 1, 33, 8, False)):
+        q8, k8, v8 = (rng.integers(0, 256, (B, hh, N, d)).astype(np.uint8) for hh in (H, Hkv, Hkv))
+        for a in (q8, k8, v8):
+            a[(a & 0x7F) == 0x7F] = 0x3C          # no NaN codes in the inputs
+        q8 &= 0xBF                                # |q| < 2: keep the scores moderate
+        k8 &= 0xBF
+        scale = 0.3
+        o, lse = orc.fwd_fp8(q8, k8, v8, 1.0, 1.0, 1.0, causal, scale)
+        tq, tk, tv = (torch.tensor(orc.e4m3_values(x)) for x in (q8, k8, v8))
+        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal,
+                                                              scale=scale, enable_gqa=True)
+        _close(o, to.numpy(), 1e-10, f"FP8 O vs SDPA on the decoded values {B, H, Hkv, N, d}")
+        o2, l2 = orc.fwd_fp8(q8, k8, v8, 2.0, 0.25, 1.0, causal, 2.0 * scale)
+        _close(o2, o, 1e-12, "FP8: q_scale k_scale fold into the softmax scale (O)")
+        _close(l2, lse, 1e-12, "FP8: q_scale k_scale fold into the softmax scale (L)")
+        o3, l3 = orc.fwd_fp8(q8, k8, v8, 1.0, 1.0, 0.125, causal, scale)
+        _close(o3, 0.125 * o, 1e-12, "FP8: v_scale multiplies O")
+        _close(l3, lse, 1e-12, "FP8: v_scale leaves L")
+
+
 ORACLE_PINS = [pin_rows_sum_to_one, pin_constant_keys, pin_causal_first_row,
                pin_online_matches_safe, pin_L_is_logsumexp, pin_merge, pin_finite_differences,
                pin_gradient_invariants, pin_torch_sdpa, pin_gqa, pin_window, pin_varlen,
-               pin_decode]
+               pin_decode, pin_fp8]

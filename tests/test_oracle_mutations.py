@@ -84,6 +84,12 @@ def test_mutant_is_caught(name, tmp_path):
 # real compiled core.
 PY_SRC = os.path.join(os.path.dirname(oracle.__file__), "__init__.py")
 GQA_MUTANTS = {
+    "fp8: exponent bias 8": (
+        "np.exp2(e - 7.0)", "np.exp2(e - 8.0)"),
+    "fp8: subnormals read as normals": (
+        "(m / 8.0) * 2.0 ** -6", "(1.0 + m / 8.0) * 2.0 ** -7"),
+    "fp8: v descale dropped": (
+        "v = self.e4m3_values(v8) * v_scale", "v = self.e4m3_values(v8)"),
     "decode: last cached key dropped": (
         "m, l, acc = self.row_partial(q[b, h], kc[b, h // g, :n], vc[b, h // g, :n], 0, 0,\n"
         "                                             n, False, scale, n)",
@@ -117,5 +123,7 @@ def test_gqa_mutant_is_caught(name):
             pins.pin_varlen(orc)
         elif name.startswith("decode"):
             pins.pin_decode(orc)
+        elif name.startswith("fp8"):
+            pins.pin_fp8(orc)
         else:
             pins.pin_gqa(orc, shapes=((1, 4, 2, 21, 8, True),))
