@@ -63,6 +63,13 @@ DECODE_WORKLOADS = {
 DECODE_METRIC = "split-KV decode KV-cache read GB/s (B=16,H=32,Hkv=8,cache<=32K,d=128,bf16)"
 
 
+# forward on 8-bit E4M3 inputs: name: (B, H, Hkv, N, causal), d = 128
+FP8_WORKLOADS = {
+    "fp8_n8k_causal_d128": (1, 32, 32, 8192, True),
+}
+FP8_METRIC = "attention fwd TFLOP/s on E4M3 inputs (N=8K,d=128,causal); % of GB300 fp8 tensor peak"
+
+
 def decode_lengths(name):
     import numpy as np
     B, _, _, Nmax = DECODE_WORKLOADS[name][:4]
@@ -89,6 +96,7 @@ KERNEL_SOURCES = {
     "bwd_dkdv_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd128.cu",
     "bwd_dq_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd128.cu",
     "decode_split_kernel": "exact_io_aware_22_gb300/csrc/fa_decode.cu",
+    "fwd_fp8_kernel": "exact_io_aware_22_gb300/csrc/fa_fwd8.cu",
 }
 
 
@@ -128,7 +136,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload",
-                    choices=list(WORKLOADS) + list(VARLEN_WORKLOADS) + list(DECODE_WORKLOADS),
+                    choices=list(WORKLOADS) + list(VARLEN_WORKLOADS) + list(DECODE_WORKLOADS)
+                    + list(FP8_WORKLOADS),
                     default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -660,14 +669,191 @@ def run_decode(args, rank, world, local_rank):
         print(json.dumps(out), flush=True)
 
 
+def run_fp8_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from exact_io_aware_22_gb300 import inputs
+    B, H, Hkv, N, causal = FP8_WORKLOADS[args.workload]
+    d = 128
+    scale = 1.0 / math.sqrt(d)
+    x = inputs.make_fp8_inputs(B, H, N, d, seed=0, Hkv=Hkv)
+    q8, k8, v8 = (x[n].numpy().reshape(-1, N, d) for n in ("q8", "k8", "v8"))
+    fwd_f, _ = attn_flops(1, 1, N, d, causal)
+
+    def step(i):
+        h = i % (B * H)
+        hk = (h // H) * Hkv + (h % H) // (H // Hkv)
+        oracle.fwd_fp8(q8[h][None, None], k8[hk][None, None], v8[hk][None, None], x["q_scale"],
+                       x["k_scale"], x["v_scale"], causal, scale)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = fwd_f * args.steps / dt / 1e12
+    sample = f"one (batch, head) pair per step, full N={N}, forward, fp64 oracle on the E4M3 codes"
+    out = {"metric": FP8_METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": args.workload, "B": B, "H": H, "Hkv": Hkv, "N": N, "d": d,
+                      "causal": causal, "step_unit": "one (batch, head) pair"},
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def run_fp8(args, rank, world, local_rank):
+    """One step = one forward on the E4M3 inputs (already quantised, in HBM)."""
+    import torch
+    import torch.distributed as dist
+
+    import exact_io_aware_22_gb300 as fa
+    from exact_io_aware_22_gb300 import inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    B, H, Hkv, N, causal = FP8_WORKLOADS[args.workload]
+    d = 128
+    scale = 1.0 / math.sqrt(d)
+    x = inputs.make_fp8_inputs(B, H, N, d, seed=rank, Hkv=Hkv)
+    qs, ks, vs = x["q_scale"], x["k_scale"], x["v_scale"]
+    q8, k8, vt8 = (x[n].to(dev) for n in ("q8", "k8", "vt8"))
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    fwd_f, _ = attn_flops(B, H, N, d, causal)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fwd_fp8(q8, k8, vt8, qs, ks, vs, causal=causal, scale=scale, out=o, lse=lse)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.device_status() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout during warm-up")
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local_rank)
+    # inputs (96 MiB) fit in L2: a buffer four times L2 is written between steps
+    flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.2)
+    barrier()
+    torch.cuda.synchronize()
+    fa.trace_enable(True)
+    spans = []
+    for _ in range(args.steps):
+        flush.zero_()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        step()
+        t1.record(stream)
+        spans.append((t0, t1))
+    torch.cuda.synchronize()
+    barrier()
+    fa.trace_enable(False)
+    clocks = sampler.stop()
+    if fa.device_status() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in spans) / args.steps, world, dev)
+    value = world * fwd_f / (ms / 1e3) / 1e12
+    traced = {kk: v for kk, v in fa.trace_read().items() if v[1] > 0}
+    launches = sum(n for _, n in traced.values())
+    k_ms = traced["fwd_fp8_kernel"][0] / traced["fwd_fp8_kernel"][1]
+    peaks = load_peaks()
+    peak8 = 2.0 * peaks["bf16_tflops"]          # fp8 dense rate = 2 x bf16 (4.5 vs 2.25 PF nominal)
+    achieved = fwd_f / (k_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "fwd_fp8_kernel", "achieved": achieved,
+                "peak": peak8, "unit": "TFLOP/s", "frac": achieved / peak8,
+                "traffic": traffic_from_profiles("fwd_fp8_kernel", args.workload),
+                "peak_source": f"{peaks['source']} bf16 (burst) x 2, the nominal fp8/bf16 ratio",
+                "algorithmic_work_per_launch": fwd_f, "avg_launch_ms": k_ms}
+    e2e = None
+    if not args.no_e2e:
+        hx = {n: x[n].pin_memory() for n in ("q8", "k8", "vt8")}
+        dst = {"q8": q8, "k8": k8, "vt8": vt8}
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+        def e2e_step():
+            for n, t in hx.items():
+                dst[n].copy_(t, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        ke = max(1, min(args.steps, 20))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
+        e2e = {"value": world * fwd_f / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(t.numel() for t in hx.values()),
+               "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4,
+               "ms_per_step": ems, "steps": ke}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        fwd1, _ = attn_flops(1, 1, N, d, causal)
+        heads, t_cpu = 0, 0.0
+        q8c, k8c, v8c = (x[n].numpy().reshape(-1, N, d) for n in ("q8", "k8", "v8"))
+        while heads < B * H and (heads == 0 or t_cpu < 10.0):
+            hk = (heads // H) * Hkv + (heads % H) // (H // Hkv)
+            t0c = time.perf_counter()
+            oracle.fwd_fp8(q8c[heads][None, None], k8c[hk][None, None], v8c[hk][None, None],
+                           qs, ks, vs, causal, scale)
+            t_cpu += time.perf_counter() - t0c
+            heads += 1
+        cpu = {"value": heads * fwd1 / t_cpu / 1e12, "unit": "TFLOP/s",
+               "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{heads} of {B * H} (batch, head) pairs, full N={N}, forward, "
+                         f"{t_cpu:.1f} s on host cores"}
+    if rank == 0:
+        out = {"metric": FP8_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+               "data": "synthetic",
+               "config": {"workload": args.workload, "B": B, "H": H, "Hkv": Hkv, "N": N, "d": d,
+                          "causal": causal, "output": "bf16",
+                          "parallelism": f"replicas x{world}",
+                          "l2": "inputs fit in L2 (96 MiB of E4M3 Q, K, V^T): "
+                                f"{flush.numel() * 4 >> 20} MiB written between steps, "
+                                "outside the timed spans"},
+               "kernels_ms": {kk: v[0] / v[1] for kk, v in traced.items()},
+               "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+               "gpu_launches": launches, "clocks": clocks}
+        print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     decode = args.workload in DECODE_WORKLOADS
+    fp8 = args.workload in FP8_WORKLOADS
     if args.impl == "reference":
-        (run_decode_reference if decode else run_reference)(args, rank, world)
+        (run_decode_reference if decode else run_fp8_reference if fp8 else run_reference)(
+            args, rank, world)
         return
     if world > 1:
         import torch
@@ -675,7 +861,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        (run_decode if decode else run_ours)(args, rank, world, local_rank)
+        (run_decode if decode else run_fp8 if fp8 else run_ours)(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -81,6 +81,10 @@ def load_library(path: str | None = None):
     lib.fa_decode_workspace_size.restype = sz
     lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
     lib.fa_decode.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, f, f, vp]
+    lib.fa_fwd_fp8.restype = i
+    lib.fa_quantize_fp8.argtypes = [vp, vp, ctypes.c_longlong, i, i, f, i, i, vp]
+    lib.fa_quantize_fp8.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_cuda_error.restype = i
@@ -312,6 +316,58 @@ def bwd_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen: int, causal: bool = 
         ws_ptr, ws_bytes, _ptr(cu_seqlens), B, total, int(max_seqlen), H, Hkv, d, int(causal),
         window, float(scale), _dtype_code(q), _stream()), "fa_bwd_varlen")
     return dq, dk, dv
+
+
+def fwd_fp8(q8, k8, vt8, q_scale: float, k_scale: float, v_scale: float, causal: bool = True,
+            scale: float | None = None, out=None, lse=None):
+    """O (bf16, B x H x N x 128) and L (fp32, B x H x N) of attention on 8-bit E4M3 codes:
+    q8 (B, H, N, 128), k8 (B, Hkv, N, 128) and vt8 (B, Hkv, 128, N) -- V with its last two
+    axes swapped -- as uint8 (or float8_e4m3fn) CUDA tensors standing for q_scale * Q,
+    k_scale * K and v_scale * V.  N must be a multiple of 16."""
+    import torch
+    _need_cuda(q8, k8, vt8)
+    if q8.dim() != 4 or k8.dim() != 4 or vt8.dim() != 4:
+        raise ValueError("q8, k8 must be (B, H|Hkv, N, 128) and vt8 (B, Hkv, 128, N)")
+    for t in (q8, k8, vt8):
+        if t.element_size() != 1:
+            raise ValueError("FP8 inputs must be 1-byte tensors (uint8 or float8_e4m3fn)")
+    B, H, N, d = q8.shape
+    Hkv = k8.shape[1]
+    if k8.shape != (B, Hkv, N, d) or vt8.shape != (B, Hkv, d, N) or Hkv < 1 or H % Hkv:
+        raise ValueError("k8 must be (B, Hkv, N, d) and vt8 (B, Hkv, d, N), H a multiple of Hkv")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _need_cuda(out, lse)
+    if out.shape != (B, H, N, d) or out.dtype != torch.bfloat16 or lse.shape != (B, H, N) \
+            or lse.dtype != torch.float32:
+        raise ValueError("out must be (B, H, N, d) bf16 and lse (B, H, N) fp32")
+    _check(load_library().fa_fwd_fp8(
+        _ptr(q8), _ptr(k8), _ptr(vt8), _ptr(out), _ptr(lse), B, H, Hkv, N, d, int(causal),
+        float(scale), float(q_scale), float(k_scale), float(v_scale), _stream()), "fa_fwd_fp8")
+    return out, lse
+
+
+def quantize_fp8(x, inv_scale: float, transpose: bool = False, out=None):
+    """E4M3 codes (uint8) of x * inv_scale, rounded to nearest even and saturated at
+    +-448, for a 16-bit CUDA tensor x of shape (..., rows, cols); with ``transpose``
+    the result is (..., cols, rows)."""
+    import torch
+    _need_cuda(x)
+    if x.dim() < 2:
+        raise ValueError("x must have at least two dimensions")
+    rows, cols = x.shape[-2], x.shape[-1]
+    mats = x.numel() // max(rows * cols, 1)
+    shape = tuple(x.shape[:-2]) + ((cols, rows) if transpose else (rows, cols))
+    out = torch.empty(shape, dtype=torch.uint8, device=x.device) if out is None else out
+    _need_cuda(out)
+    if tuple(out.shape) != shape or out.element_size() != 1:
+        raise ValueError("out must be a 1-byte tensor of the result's shape")
+    _check(load_library().fa_quantize_fp8(
+        _ptr(x), _ptr(out), mats, rows, cols, float(inv_scale), int(transpose), _dtype_code(x),
+        _stream()), "fa_quantize_fp8")
+    return out
 
 
 def decode_workspace_size(B: int, H: int, Hkv: int, Nmax: int, d: int) -> int:

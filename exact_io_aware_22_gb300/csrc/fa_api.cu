@@ -110,6 +110,26 @@ fa_status make_map_packed(CUtensorMap* m, const void* base, int d, int Hx, int t
   return FA_OK;
 }
 
+// 3-D map over bytes (inner, rows, depth), box 128 x 128 x 1 in the 128-byte
+// swizzle: the 8-bit tiles of the E4M3 forward.  Elements past the edges read as 0.
+fa_status make_map_bytes(CUtensorMap* m, const void* base, long long inner, long long rows,
+                         long long depth) {
+  EncodeTiledFn enc;
+  fa_status st = get_encoder(&enc);
+  if (st != FA_OK) return st;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(depth)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner),
+                           static_cast<cuuint64_t>(inner) * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return FA_OK;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -163,7 +183,8 @@ int g_trace_open = -1;   // record whose stop event is pending
 
 const char* const kTraceNames[fa::TR_NKINDS] = {"fwd_kernel",      "bwd_pre_kernel",
                                                  "bwd_dkdv_kernel", "bwd_dq_kernel",
-                                                 "decode_split_kernel", "decode_merge_kernel"};
+                                                 "decode_split_kernel", "decode_merge_kernel",
+                                                 "fwd_fp8_kernel"};
 
 }  // namespace
 
@@ -490,6 +511,64 @@ fa_status fa_bwd_varlen(const void* Q, const void* K, const void* V, const void*
   if (!cu_seqlens || window < 0 || (window > 0 && !causal)) return FA_ERR_INVALID_VALUE;
   return bwd_impl(Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, B, H, Hkv, max_seqlen,
                   d, causal, scale, dtype, stream, window, cu_seqlens, total);
+}
+
+// Forward on 8-bit E4M3 inputs with per-tensor descale factors (d = 128).
+fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* Vt8, void* O, float* L, int B,
+                     int H, int Hkv, int N, int d, int causal, float scale, float q_scale,
+                     float k_scale, float v_scale, void* stream) {
+  fa_status st = check_common(B, H, N, d, causal, scale, FA_BF16);
+  if (st != FA_OK) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
+  for (float x : {q_scale, k_scale, v_scale})
+    if (!(std::isfinite(x) && x > 0.f)) return FA_ERR_INVALID_VALUE;
+  if (d != 128 || N % 16 != 0) return FA_ERR_UNSUPPORTED;
+  if (!Q8 || !K8 || !Vt8 || !O || !L) return FA_ERR_INVALID_VALUE;
+  if (!aligned(Q8, 16) || !aligned(K8, 16) || !aligned(Vt8, 16) || !aligned(O, 16) ||
+      !aligned(L, 4))
+    return FA_ERR_MISALIGNED;
+  const long long BH = static_cast<long long>(B) * H, BHkv = static_cast<long long>(B) * Hkv;
+  const size_t qbytes = static_cast<size_t>(BH) * N * d, kvbytes = static_cast<size_t>(BHkv) * N * d;
+  const size_t obytes = qbytes * 2, lbytes = static_cast<size_t>(BH) * N * 4;
+  const void* ins[3] = {Q8, K8, Vt8};
+  const size_t insz[3] = {qbytes, kvbytes, kvbytes};
+  for (int i = 0; i < 3; ++i)
+    if (overlap(ins[i], insz[i], O, obytes) || overlap(ins[i], insz[i], L, lbytes))
+      return FA_ERR_INVALID_VALUE;
+  if (overlap(O, obytes, L, lbytes)) return FA_ERR_INVALID_VALUE;
+  fa::Fwd8Args a;
+  std::memset(&a, 0, sizeof(a));
+  if ((st = make_map_bytes(&a.tmQ, Q8, d, N, BH)) != FA_OK) return st;
+  if ((st = make_map_bytes(&a.tmK, K8, d, N, BHkv)) != FA_OK) return st;
+  if ((st = make_map_bytes(&a.tmVt, Vt8, N, d, BHkv)) != FA_OK) return st;
+  if ((st = ctl_for_launch(&a.ctl)) != FA_OK) return st;
+  a.O = O;
+  a.L = L;
+  a.N = N;
+  a.BH = static_cast<int>(BH);
+  a.group = H / Hkv;
+  a.c_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
+  a.o_scale = v_scale;
+  cudaError_t e = fa::launch_fwd8(a, causal != 0, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+fa_status fa_quantize_fp8(const void* X, void* X8, long long mats, int rows, int cols,
+                          float inv_scale, int transpose, fa_dtype dtype, void* stream) {
+  if (mats < 1 || rows < 1 || cols < 1 || (transpose != 0 && transpose != 1))
+    return FA_ERR_INVALID_VALUE;
+  if (!(std::isfinite(inv_scale) && inv_scale > 0.f)) return FA_ERR_INVALID_VALUE;
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (transpose && (mats > 65535 || (rows + 31) / 32 > 65535)) return FA_ERR_UNSUPPORTED;
+  if (!X || !X8) return FA_ERR_INVALID_VALUE;
+  if (!aligned(X, 2)) return FA_ERR_MISALIGNED;
+  const size_t n = static_cast<size_t>(mats) * rows * cols;
+  if (overlap(X, n * 2, X8, n)) return FA_ERR_INVALID_VALUE;
+  cudaError_t e = fa::launch_quant8(X, X8, mats, rows, cols, inv_scale, transpose != 0,
+                                    dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
 }
 
 // Split-KV decoding: one query row per (batch, head) against the first

@@ -19,7 +19,8 @@ enum TraceKind {
   TR_BWD_DQ = 3,
   TR_DEC_SPLIT = 4,
   TR_DEC_MERGE = 5,
-  TR_NKINDS = 6
+  TR_FWD8 = 6,
+  TR_NKINDS = 7
 };
 // Record an event before / after one kernel launch on `st` (no-op unless tracing).
 void trace_begin(int kind, cudaStream_t st);
@@ -92,5 +93,22 @@ int decode_key_rows(int d);
 // Splits and keys per split (written to *chunk) for caches of Nmax keys.
 int decode_parts(int B, int H, int Hkv, int Nmax, int* chunk);
 cudaError_t launch_decode(const DecodeArgs& a, int d, bool bf16, cudaStream_t st);
+
+// Forward on 8-bit E4M3 inputs, d = 128, dense (B, H, N, 128) layout.
+struct Fwd8Args {
+  CUtensorMap tmQ, tmK;        // 3-D byte maps (128, N, B*H) / (128, N, B*Hkv), box 128 x 128
+  CUtensorMap tmVt;            // 3-D byte map (N, 128, B*Hkv) of V^T, box 128 x 128
+  void* O;                     // (B, H, N, 128) bf16
+  float* L;                    // (B, H, N) fp32
+  int N, BH, group;
+  float c_log2;                // scale * q_scale * k_scale * log2(e)
+  float o_scale;               // v_scale
+  KernelCtl ctl;
+};
+cudaError_t launch_fwd8(const Fwd8Args& a, bool causal, cudaStream_t st);
+// E4M3 codes of x * inv_scale for `mats` row-major rows x cols matrices of 16-bit
+// values, optionally transposing each matrix.
+cudaError_t launch_quant8(const void* X, void* Y, long long mats, int rows, int cols,
+                          float inv_scale, bool transpose, bool bf16, cudaStream_t st);
 
 }  // namespace fa

@@ -144,6 +144,43 @@ fa_status fa_bwd_varlen(const void* Q, const void* K, const void* V, const void*
                         int total, int max_seqlen, int H, int Hkv, int d, int causal, int window,
                         float scale, fa_dtype dtype, void* stream);
 
+/* Forward on 8-bit E4M3 inputs (the FP8 precision that the FlashAttention note
+ * credits to FlashAttention-3, "Versions and Evolution"), head dim 128.  The
+ * inputs are E4M3 codes with per-tensor descale factors: the result is the
+ * attention of q_scale*Q, k_scale*K and v_scale*V, computed as the 16-bit
+ * forward does ("flash-attn-triton" docs page, Fig. 3) with both products on the
+ * tensor cores in 8 bits: S = Q K^T from the codes (fp32 accumulation), and
+ * O += P V with P rounded to E4M3 (p <= 2^8 by the running-max rule); the sum l
+ * is taken over the unrounded p.
+ *   Q8     (B, H, N, 128) codes, one byte each.
+ *   K8     (B, Hkv, N, 128) codes.
+ *   Vt8    (B, Hkv, 128, N) codes of V with its last two axes swapped (see
+ *          fa_quantize_fp8).
+ *   O      (B, H, N, 128) bf16 output.  L (B, H, N) fp32, natural log, of the
+ *          scores scale * q_scale * k_scale * (Q8 . K8).
+ *   Query head h uses K/V head h / (H / Hkv).  N must be a multiple of 16 (the
+ *   rows of Vt8 are N bytes apart and TMA wants 16-byte strides).  Q8, K8, Vt8
+ *   and O 16-byte aligned, L 4-byte aligned.
+ *   Errors: FA_ERR_UNSUPPORTED for d != 128 or N % 16 != 0; FA_ERR_INVALID_VALUE
+ *   for NULL pointers, bad sizes, H not a multiple of Hkv, non-positive or
+ *   non-finite scale or descale factors, overlapping buffers; FA_ERR_MISALIGNED
+ *   for the alignment rules.  Asynchronous on `stream`. */
+fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* Vt8, void* O, float* L, int B,
+                     int H, int Hkv, int N, int d, int causal, float scale, float q_scale,
+                     float k_scale, float v_scale, void* stream);
+
+/* E4M3 codes of X * inv_scale, rounded to nearest even and saturated at +-448
+ * (the preparation step of fa_fwd_fp8: inv_scale is 1 / descale).  X holds `mats`
+ * row-major rows x cols matrices of 16-bit values (dtype FA_FP16 / FA_BF16); X8
+ * receives one byte per element, each matrix transposed (cols x rows) when
+ * transpose = 1.  Errors: FA_ERR_INVALID_VALUE for NULL pointers, sizes < 1, a
+ * non-positive or non-finite inv_scale or overlapping buffers;
+ * FA_ERR_UNSUPPORTED for another dtype, or with transpose for more than 65535
+ * matrices or 2^21 rows; FA_ERR_MISALIGNED if X is not 2-byte aligned.
+ * Asynchronous on `stream`. */
+fa_status fa_quantize_fp8(const void* X, void* X8, long long mats, int rows, int cols,
+                          float inv_scale, int transpose, fa_dtype dtype, void* stream);
+
 /* Split-KV decoding: one new query row per (batch, head) attends to the first
  * cache_seqlens[b] cached keys of its sequence.  The key range is cut into
  * pieces whose softmax partial states (running max m, sum l, unnormalised
@@ -208,7 +245,7 @@ fa_status fa_trace_enable(int on);
 
 /* Name of trace kind `kind` (0: forward kernel, 1: backward pre-pass, 2:
  * backward dK/dV kernel, 3: backward dQ kernel, 4: decode split kernel, 5:
- * decode merge kernel); NULL when out of range. */
+ * decode merge kernel, 6: FP8 forward kernel); NULL when out of range. */
 const char* fa_trace_kind_name(int kind);
 
 /* Waits for the recorded events of kind `kind`, then writes the summed GPU

@@ -222,3 +222,39 @@ def test_decode_workspace_size(lib):
     # one key: one split
     assert f(1, 1, 1, 1, 32) == 1 * 1 * 1 * 36 * 4
     assert f(0, 1, 1, 1, 32) == 0 and f(1, 4, 3, 10, 64) == 0 and f(1, 1, 1, 10, 48) == 0
+
+
+def fwd_fp8(lib, **kw):
+    a = dict(Q=M1, K=2 * M1, V=3 * M1, O=4 * M1, L=5 * M1, B=1, H=4, Hkv=2, N=256, d=128,
+             causal=1, scale=0.088, qs=0.01, ks=0.01, vs=0.01)
+    a.update(kw)
+    ptrs = [ctypes.c_void_p(a[k]) for k in ("Q", "K", "V", "O", "L")]
+    return lib.fa_fwd_fp8(*ptrs, a["B"], a["H"], a["Hkv"], a["N"], a["d"], a["causal"],
+                          a["scale"], a["qs"], a["ks"], a["vs"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=64), UNSUPPORTED), (dict(N=200), UNSUPPORTED), (dict(Hkv=3), INVALID),
+    (dict(qs=0.0), INVALID), (dict(vs=float("inf")), INVALID), (dict(ks=-1.0), INVALID),
+    (dict(Q=0), INVALID), (dict(L=0), INVALID), (dict(B=0), INVALID),
+    (dict(K=2 * M1 + 8), MISALIGNED), (dict(L=5 * M1 + 2), MISALIGNED),
+    (dict(O=M1 + 4096), INVALID),                       # O over Q8 (4 x 256 x 128 bytes)
+])
+def test_fwd_fp8_rejects(lib, kw, code):
+    assert fwd_fp8(lib, **kw) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 1, 1, 1.0, 0), INVALID), ((1, 0, 1, 1.0, 0), INVALID), ((1, 1, 1, 0.0, 0), INVALID),
+    ((1, 1, 1, 1.0, 2), INVALID), ((70000, 4, 4, 1.0, 1), UNSUPPORTED),
+])
+def test_quantize_rejects(lib, args, code):
+    mats, rows, cols, inv, tr = args
+    assert lib.fa_quantize_fp8(ctypes.c_void_p(M1), ctypes.c_void_p(8 * M1), mats, rows, cols,
+                               inv, tr, 1, None) == code
+    assert lib.fa_quantize_fp8(ctypes.c_void_p(M1 + 1), ctypes.c_void_p(8 * M1), 1, 4, 4, 1.0,
+                               0, 1, None) == MISALIGNED
+    assert lib.fa_quantize_fp8(ctypes.c_void_p(M1), ctypes.c_void_p(M1 + 8), 1, 4, 4, 1.0,
+                               0, 1, None) == INVALID
+    assert lib.fa_quantize_fp8(ctypes.c_void_p(M1), ctypes.c_void_p(8 * M1), 1, 4, 4, 1.0,
+                               0, 7, None) == UNSUPPORTED
