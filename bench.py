@@ -129,6 +129,85 @@ def whole_job_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
     return world * flops_per_rank / (ms_max / 1e3) / 1e12
 
 
+def e2e_measure(torch, h_in, dev_sets, h_out_sets, compute, steps, barrier):
+    """Milliseconds per step, (pipelined, sequential), of whole steps through the public
+    API with host buffers: every step copies its inputs from pinned host memory to the
+    device, computes, and copies its results back to pinned host memory.
+
+    Pipelined: step k's inputs go host -> device on one stream while step k-1 computes
+    on a second and step k-2's results go device -> host on a third (full-duplex host
+    link, copy engines beside the SMs), the device tensors double-buffered.  Sequential:
+    copy in, compute, copy out, one step after another on one stream."""
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_c = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    state = {"k": 0}
+
+    def launch():
+        k = state["k"]
+        b = k % 2
+        d, ho = dev_sets[b], h_out_sets[b]
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(ev_c[b])              # step k-2 has read set b's inputs
+            for n, t in h_in.items():
+                d[n].copy_(t, non_blocking=True)
+            ev_in[b].record(s_in)
+        with torch.cuda.stream(s_c):
+            s_c.wait_event(ev_in[b])
+            if k >= 2:
+                s_c.wait_event(ev_out[b])             # step k-2's results have left set b
+            compute(d)
+            ev_c[b].record(s_c)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_c[b])
+            for n, h in ho.items():
+                h.copy_(d[n], non_blocking=True)
+            ev_out[b].record(s_out)
+        state["k"] = k + 1
+
+    for _ in range(2):
+        launch()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for _ in range(steps):
+        launch()
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    barrier()
+    pipelined = e0.elapsed_time(e1) / steps
+
+    d, ho = dev_sets[0], h_out_sets[0]
+    st = torch.cuda.current_stream()
+
+    def seq_step():
+        for n, t in h_in.items():
+            d[n].copy_(t, non_blocking=True)
+        compute(d)
+        for n, h in ho.items():
+            h.copy_(d[n], non_blocking=True)
+
+    seq_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        seq_step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier()
+    return pipelined, e0.elapsed_time(e1) / steps
+
+
+E2E_NOTE = ("pipelined: step k's inputs copied host->device while step k-1 computes and step "
+            "k-2's results are copied device->host (three streams, device tensors "
+            "double-buffered); every step moves its own inputs and results")
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -424,37 +503,38 @@ def run_ours(args, rank, world, local_rank):
 
     e2e = None
     if not args.no_e2e:
-        hx = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
-        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        hg = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+        h_in = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
+        outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        dev_sets = [{"q": q, "k": k, "v": v, "do": do, **outs},
+                    {**{n: torch.empty_like(t) for n, t in (("q", q), ("k", k), ("v", v),
+                                                          ("do", do))},
+                     **{n: torch.empty_like(t) for n, t in outs.items()}}]
+        h_out_sets = [{n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in outs.items()}
+                      for _ in range(2)]
 
-        def e2e_step():
-            for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
-                dst.copy_(hx[n], non_blocking=True)
-            step()
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
-            for h_, g_ in zip(hg, (dq, dk, dv)):
-                h_.copy_(g_, non_blocking=True)
+        def compute(dset):
+            if varlen:
+                fa.fwd_varlen(dset["q"], dset["k"], dset["v"], cu, N, causal=causal, scale=scale,
+                              out=dset["o"], lse=dset["lse"])
+                fa.bwd_varlen(dset["q"], dset["k"], dset["v"], dset["o"], dset["lse"], dset["do"],
+                              cu, N, causal=causal, scale=scale, dq=dset["dq"], dk=dset["dk"],
+                              dv=dset["dv"], workspace=ws)
+                return
+            fa.fwd(dset["q"], dset["k"], dset["v"], causal=causal, scale=scale, out=dset["o"],
+                   lse=dset["lse"], window=window)
+            fa.bwd(dset["q"], dset["k"], dset["v"], dset["o"], dset["lse"], dset["do"],
+                   causal=causal, scale=scale, dq=dset["dq"], dk=dset["dk"], dv=dset["dv"],
+                   workspace=ws, window=window)
 
         ke = max(1, min(args.steps, 20))
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        ems = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
-        e2e = {"value": whole_job_tflops(fwd_f + bwd_f, world, ems), "unit": "TFLOP/s",
+        pms, sms = e2e_measure(torch, h_in, dev_sets, h_out_sets, compute, ke, barrier)
+        pms, sms = max_over_ranks(pms, world, dev), max_over_ranks(sms, world, dev)
+        e2e = {"value": whole_job_tflops(fwd_f + bwd_f, world, pms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": in_bytes,
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv)),
-               "ms_per_step": ems, "steps": ke}
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs.values()),
+               "ms_per_step": pms, "steps": ke, "mode": E2E_NOTE,
+               "sequential": {"value": whole_job_tflops(fwd_f + bwd_f, world, sms),
+                              "ms_per_step": sms}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -614,35 +694,27 @@ def run_decode(args, rank, world, local_rank):
 
     e2e = None
     if not args.no_e2e:
-        hx = {n: x[n].pin_memory() for n in ("q", "k_cache", "v_cache", "cache_seqlens")}
-        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        dst = {"q": q, "k_cache": kc, "v_cache": vc, "cache_seqlens": cl}
+        names = ("q", "k_cache", "v_cache", "cache_seqlens")
+        h_in = {n: x[n].pin_memory() for n in names}
+        dev_sets = [{"q": q, "k_cache": kc, "v_cache": vc, "cache_seqlens": cl, "o": o, "lse": lse},
+                    {**{n: torch.empty_like(t) for n, t in zip(names, (q, kc, vc, cl))},
+                     "o": torch.empty_like(o), "lse": torch.empty_like(lse)}]
+        h_out_sets = [{"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                       "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory()}
+                      for _ in range(2)]
 
-        def e2e_step():
-            for n, t in hx.items():
-                dst[n].copy_(t, non_blocking=True)
-            step()
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+        def compute(dset):
+            fa.decode(dset["q"], dset["k_cache"], dset["v_cache"], dset["cache_seqlens"],
+                      scale=scale, out=dset["o"], lse=dset["lse"], workspace=ws)
 
         ke = max(1, min(args.steps, 10))
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        ems = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
-        e2e = {"value": world * alg_bytes / (ems / 1e3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hx.values()),
-               "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * 4,
-               "ms_per_step": ems, "steps": ke,
+        pms, sms = e2e_measure(torch, h_in, dev_sets, h_out_sets, compute, ke, barrier)
+        pms, sms = max_over_ranks(pms, world, dev), max_over_ranks(sms, world, dev)
+        e2e = {"value": world * alg_bytes / (pms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in.values()),
+               "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * 4,
+               "ms_per_step": pms, "steps": ke, "mode": E2E_NOTE,
+               "sequential": {"value": world * alg_bytes / (sms / 1e3) / 1e9, "ms_per_step": sms},
                "note": "the whole K/V cache is copied host to device every step"}
 
     cpu = None
@@ -781,35 +853,27 @@ def run_fp8(args, rank, world, local_rank):
                 "algorithmic_work_per_launch": fwd_f, "avg_launch_ms": k_ms}
     e2e = None
     if not args.no_e2e:
-        hx = {n: x[n].pin_memory() for n in ("q8", "k8", "vt8")}
-        dst = {"q8": q8, "k8": k8, "vt8": vt8}
-        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h_in = {n: x[n].pin_memory() for n in ("q8", "k8", "vt8")}
+        dev_sets = [{"q8": q8, "k8": k8, "vt8": vt8, "o": o, "lse": lse},
+                    {"q8": torch.empty_like(q8), "k8": torch.empty_like(k8),
+                     "vt8": torch.empty_like(vt8), "o": torch.empty_like(o),
+                     "lse": torch.empty_like(lse)}]
+        h_out_sets = [{"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                       "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory()}
+                      for _ in range(2)]
 
-        def e2e_step():
-            for n, t in hx.items():
-                dst[n].copy_(t, non_blocking=True)
-            step()
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+        def compute(dset):
+            fa.fwd_fp8(dset["q8"], dset["k8"], dset["vt8"], qs, ks, vs, causal=causal, scale=scale,
+                       out=dset["o"], lse=dset["lse"])
 
         ke = max(1, min(args.steps, 20))
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        ems = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
-        e2e = {"value": world * fwd_f / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": sum(t.numel() for t in hx.values()),
-               "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4,
-               "ms_per_step": ems, "steps": ke}
+        pms, sms = e2e_measure(torch, h_in, dev_sets, h_out_sets, compute, ke, barrier)
+        pms, sms = max_over_ranks(pms, world, dev), max_over_ranks(sms, world, dev)
+        e2e = {"value": world * fwd_f / (pms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(t.numel() for t in h_in.values()),
+               "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+               "ms_per_step": pms, "steps": ke, "mode": E2E_NOTE,
+               "sequential": {"value": world * fwd_f / (sms / 1e3) / 1e12, "ms_per_step": sms}}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
