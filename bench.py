@@ -47,6 +47,8 @@ WORKLOADS = {
     "n4k_causal_d128_bf16": (2, 16, 4096, 128, "bf16", True),
     "n4k_full_d128_bf16": (2, 16, 4096, 128, "bf16", False),
     "gpt2m_causal_d64_fp16": (8, 16, 1024, 64, "fp16", True),
+    "ragged_causal_d32_fp16": (4, 8, 1000, 32, "fp16", True),
+    "tiny_full_d64_fp16": (1, 1, 128, 64, "fp16", False),
     "gqa8_n8k_causal_d128_bf16": (1, 32, 8192, 128, "bf16", True, 8),
     "swa4k_gqa8_n16k_d128_bf16": (1, 32, 16384, 128, "bf16", True, 8, 4096),
 }
@@ -315,18 +317,24 @@ def cpu_baseline(x, B, H, N, d, causal, scale, budget_s=10.0, max_heads=8, windo
     import numpy as np
     import oracle
     fwd_f, bwd_f = attn_flops(1, 1, N, d, causal, window)
-    heads, t_total = 0, 0.0
+    heads, t_fwd, t_bwd = 0, 0.0, 0.0
     flat = {n: x[n].reshape(-1, N, d) for n in ("q", "k", "v", "do")}
     grp = H * B // flat["k"].shape[0]
-    while heads < min(max_heads, B * H) and (heads == 0 or t_total < budget_s):
+    while heads < min(max_heads, B * H) and (heads == 0 or t_fwd + t_bwd < budget_s):
         sel = _head(flat, heads, grp)
         t0 = time.perf_counter()
         oracle.fwd(sel["q"], sel["k"], sel["v"], causal, scale, window)
+        t1 = time.perf_counter()
         oracle.bwd(sel["q"], sel["k"], sel["v"], sel["do"], causal, scale, window)
-        t_total += time.perf_counter() - t0
+        t2 = time.perf_counter()
+        t_fwd, t_bwd = t_fwd + (t1 - t0), t_bwd + (t2 - t1)
         heads += 1
+    t_total = t_fwd + t_bwd
     value = heads * (fwd_f + bwd_f) / t_total / 1e12
     return {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "affinity_cores": len(os.sched_getaffinity(0)),
+            "fwd_tflops": heads * fwd_f / t_fwd / 1e12, "bwd_tflops": heads * bwd_f / t_bwd / 1e12,
+            "fwd_s_per_pair": t_fwd / heads, "bwd_s_per_pair": t_bwd / heads,
             "sample": f"{heads} of {B * H} (batch, head) pairs, full N={N}, fwd+bwd, "
                       f"{t_total:.1f} s on host cores"}
 
@@ -444,12 +452,13 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     fa.trace_enable(True)
     if flush is None:
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(args.steps):
+        # one event per step boundary: back-to-back steps, per-step times for the median
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        evs[0].record(stream)
+        for i in range(args.steps):
             step()
-        t1.record(stream)
-        spans = [(t0, t1)]
+            evs[i + 1].record(stream)
+        spans = list(zip(evs[:-1], evs[1:]))
     else:
         spans = []
         for _ in range(args.steps):
@@ -465,7 +474,9 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     if fa.device_status() != 0:
         raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
-    ms = sum(a.elapsed_time(b) for a, b in spans) / args.steps
+    step_ms = [a.elapsed_time(b) for a, b in spans]
+    ms = sum(step_ms) / args.steps
+    ms_median = statistics.median(step_ms)
     traced = fa.trace_read()
     ms = max_over_ranks(ms, world, dev)
     value = whole_job_tflops(fwd_f + bwd_f, world, ms)
@@ -476,6 +487,11 @@ def run_ours(args, rank, world, local_rank):
     fwd_ms = per["fwd_kernel"][0]
     bwd_ms = sum(t for kname, (t, _) in per.items() if kname.startswith("bwd_"))
     peaks = load_peaks()
+    # algorithmic bytes of the forward (Q, K, V read, O and L written) and backward (Q, K, V,
+    # O, dO, L read; D written and read; dQ, dK, dV written)
+    qb, kvb = q.numel() * 2, k.numel() * 2
+    fwd_bytes = 2 * qb + 2 * kvb + lse.numel() * 4
+    bwd_bytes = 3 * qb + 2 * kvb + 2 * kvb + qb + 3 * lse.numel() * 4
     # algorithmic work of one launch of each kernel
     elem = 2
     n_bytes = q.numel() * elem
@@ -552,7 +568,11 @@ def run_ours(args, rank, world, local_rank):
                           **({"packed_tokens": int(q.shape[0]), "max_seqlen": N,
                               "lengths": "uniform 256..8192, 64 sequences, seed 2026"}
                              if varlen else {})},
-               "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+               "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "ms_per_step_median": ms_median,
+               "fwd_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9 if fwd_ms else None,
+               "bwd_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9 if bwd_ms else None,
+               "frac_of_hbm_peak": {"fwd": fwd_bytes / (fwd_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                    "bwd": bwd_bytes / (bwd_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
                "fwd_tflops": fwd_f / (fwd_ms / 1e3) / 1e12 if fwd_ms else None,
                "bwd_tflops": bwd_f / (bwd_ms / 1e3) / 1e12 if bwd_ms else None,
                "frac_of_peak": value / world / peaks["bf16_tflops"],
