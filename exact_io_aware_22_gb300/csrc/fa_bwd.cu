@@ -149,7 +149,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + BN - 1) / BN;
-  const int nqb = Np / BM;
   const BlockPos bp = block_pos(nkb);
   const int bkv = bp.bh;                    // K/V head; its query heads are bkv*group + g
   const int kb = bp.rank;                   // key block (causal: block 0 has the most work)

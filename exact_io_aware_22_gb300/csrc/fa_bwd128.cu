@@ -54,7 +54,6 @@ namespace {
 constexpr int HD = 128;          // head dim
 constexpr int BT = 128;          // rows of every tile (keys or queries)
 constexpr int THREADS = 384;
-constexpr int STAGES = 2;
 
 constexpr int TILE = BT * HD * 2;               // a 128-row tile: two 64-column chunks
 constexpr int CHUNK = BT * 128;                 // 16 KiB
@@ -139,7 +138,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + BT - 1) / BT;
-  const int nq = Np / BT;
   const BlockPos bp = block_pos(nkb);
   const int bkv = bp.bh;                           // K/V head; its query heads: bkv*group + g
   const int kb = bp.rank;                          // causal: block 0 has the most work
