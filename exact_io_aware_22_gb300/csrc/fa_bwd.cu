@@ -597,7 +597,10 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if constexpr (D == 128) return launch_bwd128(a, BF16, CAUSAL, st);
+  // d = 64 and 128: the TMEM-resident kernels of fa_bwd128.cu; d = 32: the kernels below
+  if constexpr (D == 128 || D == 64) {
+    return launch_bwd128(a, D, BF16, CAUSAL, st);
+  } else {
   {
     auto kern = dkdv_kernel<D, BF16, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -627,6 +630,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+  }
 }
 
 }  // namespace

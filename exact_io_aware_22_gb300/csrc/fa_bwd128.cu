@@ -51,12 +51,10 @@ namespace fa {
 
 namespace {
 
-constexpr int HD = 128;          // head dim
 constexpr int BT = 128;          // rows of every tile (keys or queries)
 constexpr int THREADS = 384;
 
-constexpr int TILE = BT * HD * 2;               // a 128-row tile: two 64-column chunks
-constexpr int CHUNK = BT * 128;                 // 16 KiB
+constexpr int CHUNK = BT * 128;                 // one 64-column chunk of a 128-row tile: 16 KiB
 
 // 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -68,9 +66,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// X^T = A B^T over the head dim into TMEM columns d_tmem: A and B are 128-row
-// K-major tiles (two 64-column chunks each), given by their descriptor low words
-// (sdesc_lo with LBO 16).
+// X^T = A B^T over the head dim HD into TMEM columns d_tmem: A and B are 128-row
+// K-major tiles (HD/64 chunks of 64 columns each), given by their descriptor low
+// words (sdesc_lo with LBO 16).
+template <int HD>
 __device__ __forceinline__ void issue_ab_t_w(uint32_t d_tmem, uint32_t alo, uint32_t blo,
                                              uint32_t idesc) {
   constexpr uint32_t hi = sdesc_hi(1024, UMMA_SW128);
@@ -104,24 +103,29 @@ __device__ __forceinline__ void store_row64(uint32_t taddr, float mul, void* dst
 
 // ============================================================== dK / dV
 namespace kv {
-constexpr int Q_STAGES = 3, DO_STAGES = 2;
-constexpr int K_OFF = 0, V_OFF = TILE, Q_OFF = 2 * TILE;
-constexpr int DO_OFF = Q_OFF + Q_STAGES * TILE;
-constexpr int L_OFF = DO_OFF + DO_STAGES * TILE;   // per Q stage: 128 L*log2e
-constexpr int D_OFF = L_OFF + Q_STAGES * 512;      // per dO stage: 128 D
-constexpr int BAR_OFF = D_OFF + DO_STAGES * 512;
-// kv_full, q_full[3], q_empty[3], do_full[2], do_empty[2], s_full, s_free, dp_full, p_ready,
-// ds_ready, out_full, done
-constexpr int NBARS = 1 + 2 * Q_STAGES + 2 * DO_STAGES + 7;
-constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
-constexpr int SMEM_BYTES = SLOT_OFF + 16;
-static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
-// dV | dK | S^T | dP^T.  Once a compute thread holds its 64 dP^T values it writes
+// shared memory of head dim HD: K, V resident; Q with L*log2e in a 3-stage ring, dO
+// with D in a 2-stage ring; barriers kv_full, q_full[3], q_empty[3], do_full[2],
+// do_empty[2], s_full, s_free, dp_full, p_ready, ds_ready, out_full, done
+template <int HD>
+struct Smem {
+  static constexpr int TILE = BT * HD * 2;
+  static constexpr int Q_STAGES = 3, DO_STAGES = 2;
+  static constexpr int K_OFF = 0, V_OFF = TILE, Q_OFF = 2 * TILE;
+  static constexpr int DO_OFF = Q_OFF + Q_STAGES * TILE;
+  static constexpr int L_OFF = DO_OFF + DO_STAGES * TILE;   // per Q stage: 128 L*log2e
+  static constexpr int D_OFF = L_OFF + Q_STAGES * 512;      // per dO stage: 128 D
+  static constexpr int BAR_OFF = D_OFF + DO_STAGES * 512;
+  static constexpr int NBARS = 1 + 2 * Q_STAGES + 2 * DO_STAGES + 7;
+  static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int SMEM_BYTES = SLOT_OFF + 16;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
+};
+// dV | dK | S^T | dP^T (dV and dK use their first HD columns).  Once a compute thread holds its 64 dP^T values it writes
 // P^T (16-bit pairs) over the first 32 of those columns and dS^T over the last 32.
 constexpr uint32_t DV_COL = 0, DK_COL = 128, S_COL = 256, DP_COL = 384;
 }  // namespace kv
 
-template <bool BF16, bool CAUSAL>
+template <int HD, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
     dkdv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -130,6 +134,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                    int window, const int* __restrict__ cu_seqlens, int H, int total, float scale,
                    float c_log2, KernelCtl ctl) {
   using namespace kv;
+  using SM = Smem<HD>;
+  constexpr int TILE = SM::TILE, Q_STAGES = SM::Q_STAGES, DO_STAGES = SM::DO_STAGES;
+  constexpr int K_OFF = SM::K_OFF, V_OFF = SM::V_OFF, Q_OFF = SM::Q_OFF, DO_OFF = SM::DO_OFF;
+  constexpr int L_OFF = SM::L_OFF, D_OFF = SM::D_OFF, BAR_OFF = SM::BAR_OFF, NBARS = SM::NBARS;
+  constexpr int SLOT_OFF = SM::SLOT_OFF;
   extern __shared__ __align__(1024) uint8_t sg[];
   const uint32_t sb = smem_u32(sg);
   if (sb & 1023u) {                                // see FA_DEV_SMEM_ALIGN
@@ -183,7 +192,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(bar(B_KV), 2 * TILE);
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < HD / 64; ++c) {
         tma_load_3d(sb + K_OFF + c * CHUNK, &tmK, bar(B_KV), c * 64, sr.y(kb * BT, hk),
                     sr.z(kb * BT, hk));
         tma_load_3d(sb + V_OFF + c * CHUNK, &tmV, bar(B_KV), c * 64, sr.y(kb * BT, hk),
@@ -202,14 +211,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         const size_t row = static_cast<size_t>(bhq) * Np + qrow;
         if (!(ok = mbar_wait(bar(B_QE(s)), ((it / Q_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_QF(s)), TILE + 512);
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < HD / 64; ++c)
           tma_load_3d(sb + Q_OFF + s * TILE + c * CHUNK, &tmQ, bar(B_QF(s)), c * 64,
                       sr.y(qrow, hq), sr.z(qrow, hq));
         bulk_load(sb + L_OFF + s * 512, Lp + row, 512, bar(B_QF(s)));
         ++nq_issued;
         if (!(ok = mbar_wait(bar(B_GE(g)), ((it / DO_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_GF(g)), TILE + 512);
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < HD / 64; ++c)
           tma_load_3d(sb + DO_OFF + g * TILE + c * CHUNK, &tmdO, bar(B_GF(g)), c * 64,
                       sr.y(qrow, hq), sr.z(qrow, hq));
         bulk_load(sb + D_OFF + g * 512, Dp + row, 512, bar(B_GF(g)));
@@ -239,11 +248,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = mbar_wait(bar(B_KV), 0, ctl) && mbar_wait(bar(B_QF(0)), 0, ctl);
       if (ok) {
         tc_fence_after();
-        issue_ab_t_w(tmem + S_COL, k_lo, q_lo, idS);
+        issue_ab_t_w<HD>(tmem + S_COL, k_lo, q_lo, idS);
         umma_commit(bar(B_SF));
         if ((ok = mbar_wait(bar(B_GF(0)), 0, ctl))) {
           tc_fence_after();
-          issue_ab_t_w(tmem + DP_COL, v_lo, o_lo, idS);
+          issue_ab_t_w<HD>(tmem + DP_COL, v_lo, o_lo, idS);
           umma_commit(bar(B_DPF));
         }
       }
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!(ok = mbar_wait(bar(B_QF(s1)), ((it + 1) / Q_STAGES) & 1, ctl))) break;
           if (!(ok = mbar_wait(bar(B_SFREE), it & 1, ctl))) break;
           tc_fence_after();
-          issue_ab_t_w(tmem + S_COL, k_lo, q_lo + s1 * STAGE_W, idS);
+          issue_ab_t_w<HD>(tmem + S_COL, k_lo, q_lo + s1 * STAGE_W, idS);
           umma_commit(bar(B_SF));
         }
         // dV += P^T dO, P^T from the first half of each warpgroup's dP^T columns
@@ -282,7 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int g1 = (it + 1) % DO_STAGES;
           if (!(ok = mbar_wait(bar(B_GF(g1)), ((it + 1) / DO_STAGES) & 1, ctl))) break;
           tc_fence_after();
-          issue_ab_t_w(tmem + DP_COL, v_lo, o_lo + g1 * STAGE_W, idS);
+          issue_ab_t_w<HD>(tmem + DP_COL, v_lo, o_lo + g1 * STAGE_W, idS);
           umma_commit(bar(B_DPF));
         }
       }
@@ -412,7 +421,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B_DR));
     }
-    if (ok && mbar_wait_warp(bar(B_OF), 0, ctl)) {
+    // epilogue: warpgroup h stores head-dim columns [64h, 64h + 64) of dV and dK
+    if (ok && mbar_wait_warp(bar(B_OF), 0, ctl) && 64 * h < HD) {
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       const bool valid = gkey < sr.n;
@@ -433,22 +443,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ============================================================== dQ
 namespace qd {
-constexpr int KV_STAGES = 3;
-constexpr int DO_OFF = 0;
-constexpr int K_OFF = TILE;
-constexpr int V_OFF = K_OFF + KV_STAGES * TILE;
-constexpr int BAR_OFF = V_OFF + KV_STAGES * TILE;
-// do_full, kv_full[S], kv_empty[S], q_ready, s_full, s_free, dp_full, dp_free, ds_full, z_free,
-// o_full, done
-constexpr int NBARS = 1 + 2 * KV_STAGES + 9;
-constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
-constexpr int SMEM_BYTES = SLOT_OFF + 16;
-static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
-// dQ accumulator | S | dP | Z (dS, 16-bit pairs) | Q (16-bit pairs)
+// shared memory of head dim HD: dO resident, K and V in a 3-stage ring; barriers
+// do_full, kv_full[S], kv_empty[S], q_ready, s_full, s_free, dp_full, dp_free, ds_full,
+// z_free, o_full, done
+template <int HD>
+struct Smem {
+  static constexpr int TILE = BT * HD * 2;
+  static constexpr int KV_STAGES = 3;
+  static constexpr int DO_OFF = 0;
+  static constexpr int K_OFF = TILE;
+  static constexpr int V_OFF = K_OFF + KV_STAGES * TILE;
+  static constexpr int BAR_OFF = V_OFF + KV_STAGES * TILE;
+  static constexpr int NBARS = 1 + 2 * KV_STAGES + 9;
+  static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int SMEM_BYTES = SLOT_OFF + 16;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
+};
+// dQ accumulator | S | dP | Z (dS, 16-bit pairs) | Q (16-bit pairs); dQ uses its first
+// HD columns, Q its first HD/2
 constexpr uint32_t DQ_COL = 0, S_COL = 128, DP_COL = 256, Z_COL = 384, QT_COL = 448;
 }  // namespace qd
 
-template <bool BF16, bool CAUSAL, bool WINDOW, bool PACKED>
+template <int HD, bool BF16, bool CAUSAL, bool WINDOW, bool PACKED>
 __global__ void __launch_bounds__(THREADS, 1)
     dq128_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmdO, const void* __restrict__ Q,
@@ -456,6 +472,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                  int N, int Np, int group, int window, const int* __restrict__ cu_seqlens, int H,
                  int total, float scale, float c_log2, KernelCtl ctl) {
   using namespace qd;
+  using SM = Smem<HD>;
+  constexpr int TILE = SM::TILE, KV_STAGES = SM::KV_STAGES, DO_OFF = SM::DO_OFF;
+  constexpr int K_OFF = SM::K_OFF, V_OFF = SM::V_OFF, BAR_OFF = SM::BAR_OFF, NBARS = SM::NBARS;
+  constexpr int SLOT_OFF = SM::SLOT_OFF;
   extern __shared__ __align__(1024) uint8_t sg[];
   const uint32_t sb = smem_u32(sg);
   if (sb & 1023u) {                                // see FA_DEV_SMEM_ALIGN
@@ -507,7 +527,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ producer (dO once, K/V ring)
     if (lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(bar(B_DOF), TILE);
-      for (int c = 0; c < 2; ++c)
+      for (int c = 0; c < HD / 64; ++c)
         tma_load_3d(sb + DO_OFF + c * CHUNK, &tmdO, bar(B_DOF), c * 64, sr.y(qb * BT, hq),
                     sr.z(qb * BT, hq));
       bool ok = true;
@@ -516,7 +536,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int s = j % KV_STAGES;
         if (!(ok = mbar_wait(bar(B_KE(s)), ((j / KV_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_KF(s)), 2 * TILE);
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < HD / 64; ++c) {
           tma_load_3d(sb + K_OFF + s * TILE + c * CHUNK, &tmK, bar(B_KF(s)), c * 64,
                       sr.y((j_lo + j) * BT, hk), sr.z((j_lo + j) * BT, hk));
           tma_load_3d(sb + V_OFF + s * TILE + c * CHUNK, &tmV, bar(B_KF(s)), c * 64,
@@ -548,7 +568,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     b0 + (((kk / 4) * CHUNK + (kk % 4) * 32) >> 4), HI, idS, kk > 0);
       };
       auto issue_dp = [&](int st) {                  // dP = dO V^T
-        issue_ab_t_w(tmem + DP_COL, o_lo, v_lo + st * STAGE_W, idS);
+        issue_ab_t_w<HD>(tmem + DP_COL, o_lo, v_lo + st * STAGE_W, idS);
       };
       bool ok = mbar_wait(bar(B_QR), 0, ctl) && mbar_wait(bar(B_DOF), 0, ctl) &&
                 mbar_wait(bar(B_KF(0)), 0, ctl);
@@ -602,7 +622,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint4* src = reinterpret_cast<const uint4*>(Q) + sr.off(grow, hq, H, N, HD) / 8;
       uint32_t w[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < HD / 64; ++half) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const uint4 v = grow < sr.n ? __ldg(src + 8 * half + i) : make_uint4(0, 0, 0, 0);
@@ -686,7 +706,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B_DSF));
     }
-    if (ok && mbar_wait_warp(bar(B_OF), 0, ctl)) {
+    // epilogue: warpgroup h stores head-dim columns [64h, 64h + 64) of dQ
+    if (ok && mbar_wait_warp(bar(B_OF), 0, ctl) && 64 * h < HD) {
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       T* dst = reinterpret_cast<T*>(dQ) + sr.off(grow, hq, H, N, HD) + 64 * h;
@@ -701,19 +722,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <bool BF16, bool CAUSAL>
+template <int HD, bool BF16, bool CAUSAL>
 cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
   const int Np = (a.N + 127) / 128 * 128;
   const float* Lp = a.Dvec + static_cast<size_t>(a.BH) * Np;
   const long long nblk = static_cast<long long>(Np / BT) * a.BH;           // dQ: per query head
   const long long nblk_kv = static_cast<long long>(Np / BT) * (a.BH / a.group);   // per K/V head
   {
-    auto kern = dkdv128_kernel<BF16, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kv::SMEM_BYTES);
+    auto kern = dkdv128_kernel<HD, BF16, CAUSAL>;
+    constexpr int smem = kv::Smem<HD>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DKDV, st);
-    kern<<<static_cast<unsigned>(nblk_kv), THREADS, kv::SMEM_BYTES, st>>>(
+    kern<<<static_cast<unsigned>(nblk_kv), THREADS, smem, st>>>(
         a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.window,
         a.cu_seqlens, a.H, a.total, a.scale, a.c_log2, a.ctl);
     trace_end(TR_BWD_DKDV, st);
@@ -723,15 +744,15 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
   {
     // windowed and packed-sequence dQ kernels are separate instantiations
     auto kern = CAUSAL && a.window > 0
-        ? (a.cu_seqlens ? dq128_kernel<BF16, CAUSAL, CAUSAL, true>
-                        : dq128_kernel<BF16, CAUSAL, CAUSAL, false>)
-        : (a.cu_seqlens ? dq128_kernel<BF16, CAUSAL, false, true>
-                        : dq128_kernel<BF16, CAUSAL, false, false>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         qd::SMEM_BYTES);
+        ? (a.cu_seqlens ? dq128_kernel<HD, BF16, CAUSAL, CAUSAL, true>
+                        : dq128_kernel<HD, BF16, CAUSAL, CAUSAL, false>)
+        : (a.cu_seqlens ? dq128_kernel<HD, BF16, CAUSAL, false, true>
+                        : dq128_kernel<HD, BF16, CAUSAL, false, false>);
+    constexpr int smem = qd::Smem<HD>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DQ, st);
-    kern<<<static_cast<unsigned>(nblk), THREADS, qd::SMEM_BYTES, st>>>(
+    kern<<<static_cast<unsigned>(nblk), THREADS, smem, st>>>(
         a.tmK, a.tmV, a.tmdO, a.Q, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.window, a.cu_seqlens,
         a.H, a.total, a.scale, a.c_log2, a.ctl);
     trace_end(TR_BWD_DQ, st);
@@ -741,9 +762,13 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_bwd128(const BwdArgs& a, bool bf16, bool causal, cudaStream_t st) {
-  if (bf16) return causal ? launch_t<true, true>(a, st) : launch_t<true, false>(a, st);
-  return causal ? launch_t<false, true>(a, st) : launch_t<false, false>(a, st);
+cudaError_t launch_bwd128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
+  if (d == 64) {
+    if (bf16) return causal ? launch_t<64, true, true>(a, st) : launch_t<64, true, false>(a, st);
+    return causal ? launch_t<64, false, true>(a, st) : launch_t<64, false, false>(a, st);
+  }
+  if (bf16) return causal ? launch_t<128, true, true>(a, st) : launch_t<128, true, false>(a, st);
+  return causal ? launch_t<128, false, true>(a, st) : launch_t<128, false, false>(a, st);
 }
 
 }  // namespace fa

@@ -70,7 +70,7 @@ struct BwdArgs {
   KernelCtl ctl;
 };
 cudaError_t launch_bwd(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
-cudaError_t launch_bwd128(const BwdArgs& a, bool bf16, bool causal, cudaStream_t st);
+cudaError_t launch_bwd128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
 // Workspace: D and L*log2(e) per padded row.
 size_t bwd_workspace_bytes(long long BH, int N, int d);
 
