@@ -8,7 +8,8 @@
 //   P = exp(S - L),  dV = P^T dO,  dP = dO V^T,  D = rowsum(dO o O),
 //   dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
 //
-// Three kernels, all on one stream:
+// Three kernels, all on one stream (at d = 64 and 128 the pre-pass is followed by
+// the kernels of fa_bwd128.cu instead of the two below, which serve d = 32):
 //   pre_kernel   D = rowsum(dO o O) and L * log2(e), both laid out per 128-row
 //                query block and padded (L -> +inf, D -> 0 past N) so the
 //                other kernels read them with aligned vector loads.

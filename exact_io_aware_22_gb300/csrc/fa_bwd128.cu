@@ -1,4 +1,5 @@
-// fa_bwd128.cu -- attention backward for head dim 128 on sm_103a.
+// fa_bwd128.cu -- attention backward for head dims 64 and 128 on sm_103a (the
+// kernels are templated on the head dim HD; d = 32 keeps the kernels of fa_bwd.cu).
 //
 // Method: "flash-attn-triton" docs page, section "Scope" (backward kernels for
 // dQ, dK, dV that rebuild P from the saved L; causal mask only on diagonal
@@ -13,7 +14,8 @@
 //
 //   dkdv_kernel  key-stationary: one CTA per 128-key block, K and V in shared
 //                memory, loop over 128-query tiles (causal: from the diagonal
-//                down).  TMEM: dV | dK | S^T | dP^T, 128 columns each.  Once a
+//                down).  TMEM: dV | dK | S^T | dP^T, 128 columns each (dV and dK
+//                use HD of theirs).  Once a
 //                compute thread holds its 64 dP^T values it writes P^T and then
 //                dS^T as 16-bit pairs over those columns, 32 each: the A
 //                operands of dV += P^T dO and dK += dS^T Q, so no score tile
@@ -28,7 +30,7 @@
 //                takes its A operand from TMEM; shared memory holds dO and a
 //                three-stage K/V ring (one block's loads take longer than its
 //                MMAs; two stages left the tensor pipe waiting).  TMEM:
-//                dQ | S | dP | Z (64) | Q (64).  S and dP have columns of their
+//                dQ | S | dP | Z (64) | Q (HD/2).  S and dP have columns of their
 //                own, so the next block's S and dP start as soon as the compute
 //                warps hold this block's; dS = P o (dP - D) goes as 16-bit pairs
 //                into Z and feeds dQ += dS K from TMEM.
@@ -41,7 +43,8 @@
 // Roles in both kernels (384 threads, one CTA per SM):
 //   warp 0       TMA producer.   warp 1  TMEM allocator; lane 0 issues MMAs.
 //   warps 4-11   two compute warpgroups, one thread per TMEM lane (a key row
-//                in dkdv, a query row in dq), 64 columns each.
+//                in dkdv, a query row in dq), 64 columns each; in the epilogue
+//                warpgroup h stores head-dim columns [64h, 64h + 64).
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
