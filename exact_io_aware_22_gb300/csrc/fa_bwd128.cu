@@ -1,5 +1,5 @@
-// fa_bwd128.cu -- attention backward for head dims 64 and 128 on sm_103a (the
-// kernels are templated on the head dim HD; d = 32 keeps the kernels of fa_bwd.cu).
+// fa_bwd128.cu -- attention backward (dK/dV and dQ) on sm_103a, templated on the
+// head dim HD = 32, 64, 128 (the pre-pass is in fa_bwd.cu).
 //
 // Method: "flash-attn-triton" docs page, section "Scope" (backward kernels for
 // dQ, dK, dV that rebuild P from the saved L; causal mask only on diagonal
@@ -57,7 +57,22 @@ namespace {
 constexpr int BT = 128;          // rows of every tile (keys or queries)
 constexpr int THREADS = 384;
 
-constexpr int CHUNK = BT * 128;                 // one 64-column chunk of a 128-row tile: 16 KiB
+// Shared-memory geometry of a 128-row tile of head dim HD as TMA writes it: chunks of
+// SPAN columns (64, or all 32 at HD = 32) side by side, each in the 128-byte swizzle
+// (64-byte at HD = 32), so that UMMA reads it as a K-major operand (k-steps of 16
+// columns) or as an MN-major one (k-steps of 16 rows).
+template <int HD>
+struct Geo {
+  static constexpr int SPAN = HD < 64 ? HD : 64;             // columns per chunk
+  static constexpr int NCH = HD / SPAN;                      // chunks per tile
+  static constexpr int ROWB = SPAN * 2;                      // bytes per chunk row
+  static constexpr int CHUNK = BT * ROWB;                    // bytes per chunk
+  static constexpr int KPC = SPAN / 16;                      // K-major k-steps per chunk
+  static constexpr uint32_t HI = sdesc_hi(8 * ROWB, ROWB == 128 ? UMMA_SW128 : UMMA_SW64);
+  static constexpr int KSTEP_MN = 16 * ROWB;                 // MN-major k-step: 16 rows
+  // byte offset of K-major k-step kk
+  static constexpr uint32_t koff(int kk) { return (kk / KPC) * CHUNK + (kk % KPC) * 32; }
+};
 
 // 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -75,20 +90,21 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 template <int HD>
 __device__ __forceinline__ void issue_ab_t_w(uint32_t d_tmem, uint32_t alo, uint32_t blo,
                                              uint32_t idesc) {
-  constexpr uint32_t hi = sdesc_hi(1024, UMMA_SW128);
+  using G = Geo<HD>;
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t o = ((kk / 4) * CHUNK + (kk % 4) * 32) >> 4;
-    umma_ss_w(d_tmem, alo + o, blo + o, hi, idesc, kk > 0);
+    const uint32_t o = G::koff(kk) >> 4;
+    umma_ss_w(d_tmem, alo + o, blo + o, G::HI, idesc, kk > 0);
   }
 }
 
-// Epilogue: 64 fp32 TMEM columns of this thread's lane, times mul, rounded to the
-// 16-bit type and stored as one contiguous 128-byte run (when valid).
-template <bool BF16>
-__device__ __forceinline__ void store_row64(uint32_t taddr, float mul, void* dst, bool valid) {
+// Epilogue: NC (32 or 64) fp32 TMEM columns of this thread's lane, times mul,
+// rounded to the 16-bit type and stored as one contiguous run of 2 NC bytes (when
+// valid).
+template <int NC, bool BF16>
+__device__ __forceinline__ void store_row(uint32_t taddr, float mul, void* dst, bool valid) {
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
+  for (int cc = 0; cc < NC / 16; ++cc) {
     uint32_t v[16];
     tmem_ld16(taddr + 16 * cc, v);
     tmem_ld_wait_regs(v);
@@ -138,6 +154,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                    float c_log2, KernelCtl ctl) {
   using namespace kv;
   using SM = Smem<HD>;
+  using G = Geo<HD>;
   constexpr int TILE = SM::TILE, Q_STAGES = SM::Q_STAGES, DO_STAGES = SM::DO_STAGES;
   constexpr int K_OFF = SM::K_OFF, V_OFF = SM::V_OFF, Q_OFF = SM::Q_OFF, DO_OFF = SM::DO_OFF;
   constexpr int L_OFF = SM::L_OFF, D_OFF = SM::D_OFF, BAR_OFF = SM::BAR_OFF, NBARS = SM::NBARS;
@@ -195,10 +212,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(bar(B_KV), 2 * TILE);
-      for (int c = 0; c < HD / 64; ++c) {
-        tma_load_3d(sb + K_OFF + c * CHUNK, &tmK, bar(B_KV), c * 64, sr.y(kb * BT, hk),
+      for (int c = 0; c < G::NCH; ++c) {
+        tma_load_3d(sb + K_OFF + c * G::CHUNK, &tmK, bar(B_KV), c * G::SPAN, sr.y(kb * BT, hk),
                     sr.z(kb * BT, hk));
-        tma_load_3d(sb + V_OFF + c * CHUNK, &tmV, bar(B_KV), c * 64, sr.y(kb * BT, hk),
+        tma_load_3d(sb + V_OFF + c * G::CHUNK, &tmV, bar(B_KV), c * G::SPAN, sr.y(kb * BT, hk),
                     sr.z(kb * BT, hk));
       }
       // Q with L*log2e in a three-stage ring, dO with D in a two-stage ring (L and D:
@@ -214,15 +231,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         const size_t row = static_cast<size_t>(bhq) * Np + qrow;
         if (!(ok = mbar_wait(bar(B_QE(s)), ((it / Q_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_QF(s)), TILE + 512);
-        for (int c = 0; c < HD / 64; ++c)
-          tma_load_3d(sb + Q_OFF + s * TILE + c * CHUNK, &tmQ, bar(B_QF(s)), c * 64,
+        for (int c = 0; c < G::NCH; ++c)
+          tma_load_3d(sb + Q_OFF + s * TILE + c * G::CHUNK, &tmQ, bar(B_QF(s)), c * G::SPAN,
                       sr.y(qrow, hq), sr.z(qrow, hq));
         bulk_load(sb + L_OFF + s * 512, Lp + row, 512, bar(B_QF(s)));
         ++nq_issued;
         if (!(ok = mbar_wait(bar(B_GE(g)), ((it / DO_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_GF(g)), TILE + 512);
-        for (int c = 0; c < HD / 64; ++c)
-          tma_load_3d(sb + DO_OFF + g * TILE + c * CHUNK, &tmdO, bar(B_GF(g)), c * 64,
+        for (int c = 0; c < G::NCH; ++c)
+          tma_load_3d(sb + DO_OFF + g * TILE + c * G::CHUNK, &tmdO, bar(B_GF(g)), c * G::SPAN,
                       sr.y(qrow, hq), sr.z(qrow, hq));
         bulk_load(sb + D_OFF + g * 512, Dp + row, 512, bar(B_GF(g)));
         ++ng_issued;
@@ -244,10 +261,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       // descriptor low words: K, V and stage 0 of the Q and dO rings, K-major (LBO 16,
       // for S^T and dP^T) and MN-major (LBO = one 64-column chunk, for dK and dV); a
       // stage is TILE bytes on
-      constexpr uint32_t HI = sdesc_hi(1024, UMMA_SW128), STAGE_W = TILE >> 4;
+      constexpr uint32_t HI = G::HI, STAGE_W = TILE >> 4;
       const uint32_t k_lo = sdesc_lo(sb + K_OFF, 16), v_lo = sdesc_lo(sb + V_OFF, 16);
-      const uint32_t q_lo = sdesc_lo(sb + Q_OFF, 16), qm_lo = sdesc_lo(sb + Q_OFF, CHUNK);
-      const uint32_t o_lo = sdesc_lo(sb + DO_OFF, 16), om_lo = sdesc_lo(sb + DO_OFF, CHUNK);
+      const uint32_t q_lo = sdesc_lo(sb + Q_OFF, 16), qm_lo = sdesc_lo(sb + Q_OFF, G::CHUNK);
+      const uint32_t o_lo = sdesc_lo(sb + DO_OFF, 16), om_lo = sdesc_lo(sb + DO_OFF, G::CHUNK);
       bool ok = mbar_wait(bar(B_KV), 0, ctl) && mbar_wait(bar(B_QF(0)), 0, ctl);
       if (ok) {
         tc_fence_after();
@@ -278,7 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
           umma_ts_w(tmem + DV_COL, tmem + DP_COL + (kk / 4) * 64 + (kk % 4) * 8,
-                    dv_b + kk * (2048 >> 4), HI, idG, kk > 0 ? 1u : acc0);
+                    dv_b + kk * (G::KSTEP_MN >> 4), HI, idG, kk > 0 ? 1u : acc0);
         // dK += dS^T Q, dS^T from the second half
         if (!(ok = mbar_wait(bar(B_DR), it & 1, ctl))) break;
         tc_fence_after();
@@ -286,7 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
           umma_ts_w(tmem + DK_COL, tmem + DP_COL + (kk / 4) * 64 + 32 + (kk % 4) * 8,
-                    dk_b + kk * (2048 >> 4), HI, idG, kk > 0 ? 1u : acc0);
+                    dk_b + kk * (G::KSTEP_MN >> 4), HI, idG, kk > 0 ? 1u : acc0);
         umma_commit(bar(B_QE(s)));
         umma_commit(bar(B_GE(g)));
         if (next) {
@@ -430,9 +447,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       const bool valid = gkey < sr.n;
       const size_t roff = sr.off(gkey, hk, Hkv, N, HD) + 64 * h;
-      store_row64<BF16>(tmem + lane_off + DV_COL + 64 * h, 1.f, reinterpret_cast<T*>(dV) + roff,
+      constexpr int NC = HD < 64 ? HD : 64;
+      store_row<NC, BF16>(tmem + lane_off + DV_COL + 64 * h, 1.f, reinterpret_cast<T*>(dV) + roff,
                         valid);
-      store_row64<BF16>(tmem + lane_off + DK_COL + 64 * h, scale, reinterpret_cast<T*>(dK) + roff,
+      store_row<NC, BF16>(tmem + lane_off + DK_COL + 64 * h, scale, reinterpret_cast<T*>(dK) + roff,
                         valid);
     }
   }
@@ -476,6 +494,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                  int total, float scale, float c_log2, KernelCtl ctl) {
   using namespace qd;
   using SM = Smem<HD>;
+  using G = Geo<HD>;
   constexpr int TILE = SM::TILE, KV_STAGES = SM::KV_STAGES, DO_OFF = SM::DO_OFF;
   constexpr int K_OFF = SM::K_OFF, V_OFF = SM::V_OFF, BAR_OFF = SM::BAR_OFF, NBARS = SM::NBARS;
   constexpr int SLOT_OFF = SM::SLOT_OFF;
@@ -530,8 +549,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ producer (dO once, K/V ring)
     if (lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(bar(B_DOF), TILE);
-      for (int c = 0; c < HD / 64; ++c)
-        tma_load_3d(sb + DO_OFF + c * CHUNK, &tmdO, bar(B_DOF), c * 64, sr.y(qb * BT, hq),
+      for (int c = 0; c < G::NCH; ++c)
+        tma_load_3d(sb + DO_OFF + c * G::CHUNK, &tmdO, bar(B_DOF), c * G::SPAN, sr.y(qb * BT, hq),
                     sr.z(qb * BT, hq));
       bool ok = true;
       int j = 0;
@@ -539,10 +558,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int s = j % KV_STAGES;
         if (!(ok = mbar_wait(bar(B_KE(s)), ((j / KV_STAGES) & 1) ^ 1, ctl))) break;
         mbar_arrive_expect_tx(bar(B_KF(s)), 2 * TILE);
-        for (int c = 0; c < HD / 64; ++c) {
-          tma_load_3d(sb + K_OFF + s * TILE + c * CHUNK, &tmK, bar(B_KF(s)), c * 64,
+        for (int c = 0; c < G::NCH; ++c) {
+          tma_load_3d(sb + K_OFF + s * TILE + c * G::CHUNK, &tmK, bar(B_KF(s)), c * G::SPAN,
                       sr.y((j_lo + j) * BT, hk), sr.z((j_lo + j) * BT, hk));
-          tma_load_3d(sb + V_OFF + s * TILE + c * CHUNK, &tmV, bar(B_KF(s)), c * 64,
+          tma_load_3d(sb + V_OFF + s * TILE + c * G::CHUNK, &tmV, bar(B_KF(s)), c * G::SPAN,
                       sr.y((j_lo + j) * BT, hk), sr.z((j_lo + j) * BT, hk));
         }
       }
@@ -560,15 +579,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idQ = umma_idesc_f16(BT, HD, BF16, false, true);    // dQ
       // descriptor low words of dO and of stage 0 of the K and V rings, K-major (LBO 16)
       // and, for K as the B operand of dQ, MN-major (LBO = one 64-column chunk)
-      constexpr uint32_t HI = sdesc_hi(1024, UMMA_SW128), STAGE_W = TILE >> 4;
-      const uint32_t k_lo = sdesc_lo(sb + K_OFF, 16), km_lo = sdesc_lo(sb + K_OFF, CHUNK);
+      constexpr uint32_t HI = G::HI, STAGE_W = TILE >> 4;
+      const uint32_t k_lo = sdesc_lo(sb + K_OFF, 16), km_lo = sdesc_lo(sb + K_OFF, G::CHUNK);
       const uint32_t v_lo = sdesc_lo(sb + V_OFF, 16), o_lo = sdesc_lo(sb + DO_OFF, 16);
       auto issue_s = [&](int st) {                   // S = Q K^T, Q from TMEM
         const uint32_t b0 = k_lo + st * STAGE_W;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           umma_ts_w(tmem + S_COL, tmem + QT_COL + kk * 8,
-                    b0 + (((kk / 4) * CHUNK + (kk % 4) * 32) >> 4), HI, idS, kk > 0);
+                    b0 + (G::koff(kk) >> 4), HI, idS, kk > 0);
       };
       auto issue_dp = [&](int st) {                  // dP = dO V^T
         issue_ab_t_w<HD>(tmem + DP_COL, o_lo, v_lo + st * STAGE_W, idS);
@@ -605,7 +624,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
           umma_ts_w(tmem + DQ_COL, tmem + Z_COL + (kk / 4) * 32 + (kk % 4) * 8,
-                    kb0 + kk * (2048 >> 4), HI, idQ, kk > 0 ? 1u : acc0);
+                    kb0 + kk * (G::KSTEP_MN >> 4), HI, idQ, kk > 0 ? 1u : acc0);
         umma_commit(bar(B_ZFREE));
         umma_commit(bar(B_KE(s)));
       }
@@ -623,18 +642,31 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (h == 0) {
       // this row of Q into TMEM as 16-bit pairs (A operand of S = Q K^T); rows past N are zero
       const uint4* src = reinterpret_cast<const uint4*>(Q) + sr.off(grow, hq, H, N, HD) / 8;
-      uint32_t w[32];
+      if constexpr (HD >= 64) {
+        uint32_t w[32];
 #pragma unroll
-      for (int half = 0; half < HD / 64; ++half) {
+        for (int half = 0; half < HD / 64; ++half) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = grow < sr.n ? __ldg(src + 8 * half + i) : make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = grow < sr.n ? __ldg(src + 8 * half + i) : make_uint4(0, 0, 0, 0);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_off + QT_COL + 32 * half, w);
+        }
+      } else {
+        uint32_t w[16];                            // HD = 32: one row is 16 pairs
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = grow < sr.n ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
           w[4 * i] = v.x;
           w[4 * i + 1] = v.y;
           w[4 * i + 2] = v.z;
           w[4 * i + 3] = v.w;
         }
-        tmem_st32(tmem + lane_off + QT_COL + 32 * half, w);
+        tmem_st16(tmem + lane_off + QT_COL, w);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -714,7 +746,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       T* dst = reinterpret_cast<T*>(dQ) + sr.off(grow, hq, H, N, HD) + 64 * h;
-      store_row64<BF16>(tmem + lane_off + DQ_COL + 64 * h, scale, dst, grow < sr.n);
+      store_row<(HD < 64 ? HD : 64), BF16>(tmem + lane_off + DQ_COL + 64 * h, scale, dst,
+                                           grow < sr.n);
     }
   }
   tc_fence_before();
@@ -766,6 +799,10 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_bwd128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
+  if (d == 32) {
+    if (bf16) return causal ? launch_t<32, true, true>(a, st) : launch_t<32, true, false>(a, st);
+    return causal ? launch_t<32, false, true>(a, st) : launch_t<32, false, false>(a, st);
+  }
   if (d == 64) {
     if (bf16) return causal ? launch_t<64, true, true>(a, st) : launch_t<64, true, false>(a, st);
     return causal ? launch_t<64, false, true>(a, st) : launch_t<64, false, false>(a, st);

@@ -90,6 +90,7 @@ WINDOW_CASES = [
     (1, 4, 2, 517, 128, "bf16", 129),        # with shared K/V heads
     (1, 2, 2, 700, 128, "bf16", 333),
     (1, 2, 2, 300, 64, "bf16", 5000),        # window longer than N: plain causal
+    (1, 8, 2, 2048, 64, "bf16", 300),        # d = 64 with shared K/V heads, many tiles
 ]
 
 
@@ -129,3 +130,9 @@ def test_varlen_many_sequences():
     import numpy as np
     lens = tuple(int(x) for x in np.random.default_rng(5).integers(1, 2000, 32))
     print(compare_varlen(lens, 8, 128, "bf16", True, Hkv=2, seed=19))
+
+
+def test_d64_full_size_sampled():
+    # 1 x 16 x 8192 x 64 bf16 causal (the d = 64 backward on many query tiles per key
+    # block); heads 0 and 15 compared in full
+    print(compare(1, 16, 8192, 64, "bf16", True, heads=(0, 15)))
