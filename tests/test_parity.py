@@ -136,3 +136,9 @@ def test_d64_full_size_sampled():
     # 1 x 16 x 8192 x 64 bf16 causal (the d = 64 backward on many query tiles per key
     # block); heads 0 and 15 compared in full
     print(compare(1, 16, 8192, 64, "bf16", True, heads=(0, 15)))
+
+
+def test_d32_full_size_sampled():
+    # 2 x 8 x 4096 x 32 fp16 causal with shared K/V heads (4 query heads per K/V head);
+    # K/V heads 0 and 3 compared in full with their query heads
+    print(compare(2, 8, 4096, 32, "fp16", True, heads=(0, 3), Hkv=2))
