@@ -61,8 +61,12 @@ VARLEN_WORKLOADS = {
 # against K/V caches of lengths uniform in [Nmax/2, Nmax] from a fixed seed
 DECODE_WORKLOADS = {
     "decode_b16_gqa8_kv32k_d128_bf16": (16, 32, 8, 32768, 128, "bf16"),
+    # the same with E4M3 caches (per-tensor descale factors), bf16 q and O
+    "decode_fp8cache_b16_gqa8_kv32k_d128": (16, 32, 8, 32768, 128, "bf16", "e4m3"),
 }
 DECODE_METRIC = "split-KV decode KV-cache read GB/s (B=16,H=32,Hkv=8,cache<=32K,d=128,bf16)"
+DECODE8_METRIC = ("split-KV decode KV-cache read GB/s (B=16,H=32,Hkv=8,cache<=32K,d=128, "
+                  "E4M3 caches)")
 
 
 # forward on 8-bit E4M3 inputs: name: (B, H, Hkv, N, causal), d = 128
@@ -70,6 +74,35 @@ FP8_WORKLOADS = {
     "fp8_n8k_causal_d128": (1, 32, 32, 8192, True),
 }
 FP8_METRIC = "attention fwd TFLOP/s on E4M3 inputs (N=8K,d=128,causal); % of GB300 fp8 tensor peak"
+
+
+def decode_workload(name):
+    """(B, H, Hkv, Nmax, d, dtype, c8) of a decoding workload; c8: E4M3 caches."""
+    w = DECODE_WORKLOADS[name]
+    return (*w[:6], len(w) > 6 and w[6] == "e4m3")
+
+
+def make_decode_x(name, seed):
+    """Inputs of a decoding workload: q, k_cache, v_cache, cache_seqlens, and for E4M3
+    caches the codes with k_scale, v_scale."""
+    from exact_io_aware_22_gb300 import inputs
+    B, H, Hkv, Nmax, d, dtype, c8 = decode_workload(name)
+    lens = decode_lengths(name)
+    if not c8:
+        return inputs.make_decode_inputs(B, H, Hkv, Nmax, d, lens, dtype, seed=seed)
+    x = inputs.make_decode_fp8_inputs(B, H, Hkv, Nmax, d, lens, dtype, seed=seed)
+    return {"q": x["q"], "k_cache": x["k8"], "v_cache": x["v8"],
+            "cache_seqlens": x["cache_seqlens"], "k_scale": x["k_scale"], "v_scale": x["v_scale"]}
+
+
+def oracle_cache(x, name, sl, n):
+    """fp64 cache rows [0, n) of batch entries sl, decoded from E4M3 codes if need be."""
+    import oracle
+    kc, vc = x["k_cache"][sl, :, :n], x["v_cache"][sl, :, :n]
+    if "k_scale" in x:
+        return (oracle.e4m3_values(kc.numpy()) * x["k_scale"],
+                oracle.e4m3_values(vc.numpy()) * x["v_scale"])
+    return kc.double().numpy(), vc.double().numpy()
 
 
 def decode_lengths(name):
@@ -582,27 +615,27 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(out), flush=True)
 
 
-def decode_bytes(lens, H, Hkv, d):
+def decode_bytes(lens, H, Hkv, d, elem=2):
     """Algorithmic HBM bytes of one decoding step: every cached K and V row in use read
-    once (16-bit), q read, O written, L written."""
-    return sum(lens) * Hkv * d * 2 * 2 + len(lens) * H * (d * 2 * 2 + 4)
+    once (elem bytes per value), q read, O written (16-bit), L written."""
+    return sum(lens) * Hkv * d * elem * 2 + len(lens) * H * (d * 2 * 2 + 4)
 
 
-def decode_cpu_sample(x, lens, H, Hkv, d, scale, budget_s=10.0):
+def decode_cpu_sample(x, name, lens, H, Hkv, d, scale, budget_s=10.0):
     """Time the fp64 oracle's decode as it stands on the host cores, whole batch entries
     (all heads) at a time until ``budget_s`` is spent (at least one)."""
     import oracle
+    elem = 1 if "k_scale" in x else 2
     done, t_total, nbytes = 0, 0.0, 0
     B = len(lens)
     while done < B and (done == 0 or t_total < budget_s):
         sl = slice(done, done + 1)
         q = x["q"][sl].double().numpy()
-        kc = x["k_cache"][sl, :, :lens[done]].double().numpy()
-        vc = x["v_cache"][sl, :, :lens[done]].double().numpy()
+        kc, vc = oracle_cache(x, name, sl, lens[done])
         t0 = time.perf_counter()
         oracle.decode(q, kc, vc, [lens[done]], scale)
         t_total += time.perf_counter() - t0
-        nbytes += decode_bytes([lens[done]], H, Hkv, d)
+        nbytes += decode_bytes([lens[done]], H, Hkv, d, elem)
         done += 1
     return nbytes / t_total / 1e9, done, t_total
 
@@ -611,18 +644,17 @@ def run_decode_reference(args, rank, world):
     if rank != 0:
         return
     import oracle
-    from exact_io_aware_22_gb300 import inputs
-    B, H, Hkv, Nmax, d, dtype = DECODE_WORKLOADS[args.workload]
+    B, H, Hkv, Nmax, d, dtype, c8 = decode_workload(args.workload)
     lens = decode_lengths(args.workload)
     scale = 1.0 / math.sqrt(d)
-    x = inputs.make_decode_inputs(B, H, Hkv, Nmax, d, lens, dtype, seed=0)
+    x = make_decode_x(args.workload, 0)
+    elem = 1 if c8 else 2
 
     def step(i):
         b = i % B
-        oracle.decode(x["q"][b:b + 1].double().numpy(),
-                      x["k_cache"][b:b + 1, :, :lens[b]].double().numpy(),
-                      x["v_cache"][b:b + 1, :, :lens[b]].double().numpy(), [lens[b]], scale)
-        return decode_bytes([lens[b]], H, Hkv, d)
+        kc, vc = oracle_cache(x, args.workload, slice(b, b + 1), lens[b])
+        oracle.decode(x["q"][b:b + 1].double().numpy(), kc, vc, [lens[b]], scale)
+        return decode_bytes([lens[b]], H, Hkv, d, elem)
 
     for i in range(args.warmup):
         step(i)
@@ -631,12 +663,13 @@ def run_decode_reference(args, rank, world):
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9
     sample = f"one batch entry (all {H} heads, its whole cache) per step, fp64 oracle"
-    out = {"metric": DECODE_METRIC, "value": value, "unit": "GB/s", "impl": "reference",
+    out = {"metric": DECODE8_METRIC if c8 else DECODE_METRIC, "value": value, "unit": "GB/s",
+           "impl": "reference",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": args.workload, "B": B, "H": H, "Hkv": Hkv, "Nmax": Nmax,
-                      "d": d, "step_unit": "one batch entry"},
+                      "d": d, "cache": "e4m3" if c8 else dtype, "step_unit": "one batch entry"},
            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -654,20 +687,27 @@ def run_decode(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    B, H, Hkv, Nmax, d, dtype = DECODE_WORKLOADS[args.workload]
+    B, H, Hkv, Nmax, d, dtype, c8 = decode_workload(args.workload)
     lens = decode_lengths(args.workload)
     scale = 1.0 / math.sqrt(d)
-    x = inputs.make_decode_inputs(B, H, Hkv, Nmax, d, lens, dtype, seed=rank)
+    x = make_decode_x(args.workload, rank)
     q, kc, vc, cl = (x[n].to(dev) for n in ("q", "k_cache", "v_cache", "cache_seqlens"))
     o = torch.empty_like(q)
     lse = torch.empty((B, H), dtype=torch.float32, device=dev)
     ws = torch.empty(fa.decode_workspace_size(B, H, Hkv, Nmax, d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    alg_bytes = decode_bytes(lens, H, Hkv, d)
+    alg_bytes = decode_bytes(lens, H, Hkv, d, 1 if c8 else 2)
     flops = 4.0 * sum(lens) * H * d
 
+    def run(qq, kk, vv, ll, oo, lo):
+        if c8:
+            fa.decode_fp8(qq, kk, vv, ll, x["k_scale"], x["v_scale"], scale=scale, out=oo, lse=lo,
+                          workspace=ws)
+        else:
+            fa.decode(qq, kk, vv, ll, scale=scale, out=oo, lse=lo, workspace=ws)
+
     def step():
-        fa.decode(q, kc, vc, cl, scale=scale, out=o, lse=lse, workspace=ws)
+        run(q, kc, vc, cl, o, lse)
 
     def barrier():
         if world > 1:
@@ -724,8 +764,8 @@ def run_decode(args, rank, world, local_rank):
                       for _ in range(2)]
 
         def compute(dset):
-            fa.decode(dset["q"], dset["k_cache"], dset["v_cache"], dset["cache_seqlens"],
-                      scale=scale, out=dset["o"], lse=dset["lse"], workspace=ws)
+            run(dset["q"], dset["k_cache"], dset["v_cache"], dset["cache_seqlens"], dset["o"],
+                dset["lse"])
 
         ke = max(1, min(args.steps, 10))
         pms, sms = e2e_measure(torch, h_in, dev_sets, h_out_sets, compute, ke, barrier)
@@ -740,22 +780,24 @@ def run_decode(args, rank, world, local_rank):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
-        v_cpu, done, t_cpu = decode_cpu_sample(x, lens, H, Hkv, d, scale)
+        v_cpu, done, t_cpu = decode_cpu_sample(x, args.workload, lens, H, Hkv, d, scale)
         cpu = {"value": v_cpu, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{done} of {B} batch entries (all heads, whole caches), "
                          f"{t_cpu:.1f} s on host cores"}
     if rank == 0:
-        out = {"metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        out = {"metric": DECODE8_METRIC if c8 else DECODE_METRIC, "value": value, "unit": "GB/s",
+               "n_gpus": world,
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
                "data": "synthetic",
                "config": {"workload": args.workload, "B": B, "H": H, "Hkv": Hkv, "Nmax": Nmax,
-                          "d": d, "cached_keys": sum(lens),
+                          "d": d, "cache": "e4m3" if c8 else dtype, "cached_keys": sum(lens),
                           "lengths": f"uniform {Nmax // 2}..{Nmax}, seed 2027",
                           "parallelism": f"replicas x{world}",
                           "l2": f"inputs larger than L2 ({alg_bytes >> 20} MiB of K/V rows "
                                 "read per step), no flush"},
                "tflops": world * flops / (ms / 1e3) / 1e12,
+               "cached_rows_per_s": world * sum(lens) * Hkv / (ms / 1e3),
                "kernels_ms": per, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": launches, "clocks": clocks}
         print(json.dumps(out), flush=True)

@@ -81,6 +81,8 @@ def load_library(path: str | None = None):
     lib.fa_decode_workspace_size.restype = sz
     lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
     lib.fa_decode.restype = i
+    lib.fa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, f, f, i, vp]
+    lib.fa_decode_fp8.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, f, f, vp]
     lib.fa_fwd_fp8.restype = i
     lib.fa_quantize_fp8.argtypes = [vp, vp, ctypes.c_longlong, i, i, f, i, i, vp]
@@ -407,6 +409,41 @@ def decode(q, k_cache, v_cache, cache_seqlens, scale: float | None = None, out=N
     _check(load_library().fa_decode(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens), _ptr(out), _ptr(lse), ws,
         ws_bytes, B, H, Hkv, Nmax, d, float(scale), _dtype_code(q), _stream()), "fa_decode")
+    return out, lse
+
+
+def decode_fp8(q, k_cache8, v_cache8, cache_seqlens, k_scale: float, v_scale: float,
+               scale: float | None = None, out=None, lse=None, workspace=None):
+    """As ``decode``, with caches of 8-bit E4M3 codes (uint8 or float8_e4m3fn CUDA tensors,
+    (B, Hkv, Nmax, 128)) standing for k_scale * K and v_scale * V."""
+    import torch
+    _need_cuda(q, k_cache8, v_cache8, cache_seqlens)
+    if q.dim() != 3 or k_cache8.dim() != 4 or v_cache8.shape != k_cache8.shape:
+        raise ValueError("q must be (B, H, d) and the caches one (B, Hkv, Nmax, d) shape")
+    if k_cache8.element_size() != 1 or v_cache8.element_size() != 1:
+        raise ValueError("E4M3 caches must be 1-byte tensors")
+    B, H, d = q.shape
+    Bk, Hkv, Nmax, dk = k_cache8.shape
+    if Bk != B or dk != d or Hkv < 1 or H % Hkv:
+        raise ValueError("caches must be (B, Hkv, Nmax, d) with H a multiple of Hkv")
+    if cache_seqlens.dtype != torch.int32 or cache_seqlens.shape != (B,):
+        raise ValueError("cache_seqlens must be an int32 tensor of B lengths")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need_cuda(out, lse)
+    if out.shape != q.shape or out.dtype != q.dtype or lse.shape != (B, H) \
+            or lse.dtype != torch.float32:
+        raise ValueError("out must match q; lse must be (B, H) fp32")
+    ws, ws_bytes = None, 0
+    if workspace is not None:
+        _need_cuda(workspace)
+        ws, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    _check(load_library().fa_decode_fp8(
+        _ptr(q), _ptr(k_cache8), _ptr(v_cache8), _ptr(cache_seqlens), _ptr(out), _ptr(lse), ws,
+        ws_bytes, B, H, Hkv, Nmax, d, float(scale), float(k_scale), float(v_scale),
+        _dtype_code(q), _stream()), "fa_decode_fp8")
     return out, lse
 
 

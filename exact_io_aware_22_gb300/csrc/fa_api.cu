@@ -110,10 +110,11 @@ fa_status make_map_packed(CUtensorMap* m, const void* base, int d, int Hx, int t
   return FA_OK;
 }
 
-// 3-D map over bytes (inner, rows, depth), box 128 x 128 x 1 in the 128-byte
-// swizzle: the 8-bit tiles of the E4M3 forward.  Elements past the edges read as 0.
+// 3-D map over bytes (inner, rows, depth), box 128 bytes x box_rows x 1 in the
+// 128-byte swizzle: the 8-bit tiles of the E4M3 forward and of E4M3 caches.  Elements
+// past the edges read as 0.
 fa_status make_map_bytes(CUtensorMap* m, const void* base, long long inner, long long rows,
-                         long long depth) {
+                         long long depth, unsigned box_rows = 128) {
   EncodeTiledFn enc;
   fa_status st = get_encoder(&enc);
   if (st != FA_OK) return st;
@@ -121,7 +122,7 @@ fa_status make_map_bytes(CUtensorMap* m, const void* base, long long inner, long
                         static_cast<cuuint64_t>(depth)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner),
                            static_cast<cuuint64_t>(inner) * static_cast<cuuint64_t>(rows)};
-  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t box[3] = {128, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -581,9 +582,11 @@ size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nmax, int d) {
   return static_cast<size_t>(B) * H * splits * (d + 4) * sizeof(float);
 }
 
-fa_status fa_decode(const void* Q, const void* Kc, const void* Vc, const int* cache_seqlens,
-                    void* O, float* L, void* workspace, size_t workspace_bytes, int B, int H,
-                    int Hkv, int Nmax, int d, float scale, fa_dtype dtype, void* stream) {
+static fa_status decode_impl(const void* Q, const void* Kc, const void* Vc,
+                             const int* cache_seqlens, void* O, float* L, void* workspace,
+                             size_t workspace_bytes, int B, int H, int Hkv, int Nmax, int d,
+                             float scale, fa_dtype dtype, void* stream, bool c8, float k_scale,
+                             float v_scale) {
   fa_status st = check_common(B, H, Nmax, d, 0, scale, static_cast<int>(dtype));
   if (st != FA_OK) return st;
   if ((st = check_heads(H, Hkv)) != FA_OK) return st;
@@ -600,7 +603,7 @@ fa_status fa_decode(const void* Q, const void* Kc, const void* Vc, const int* ca
   const size_t need = fa_decode_workspace_size(B, H, Hkv, Nmax, d);
   if (workspace && workspace_bytes < need) return FA_ERR_INVALID_VALUE;
   const size_t qbytes = static_cast<size_t>(B) * H * d * 2, lbytes = static_cast<size_t>(B) * H * 4;
-  const size_t cbytes = static_cast<size_t>(B) * Hkv * Nmax * d * 2;
+  const size_t cbytes = static_cast<size_t>(B) * Hkv * Nmax * d * (c8 ? 1 : 2);
   const void* ins[4] = {Q, Kc, Vc, cache_seqlens};
   const size_t insz[4] = {qbytes, cbytes, cbytes, static_cast<size_t>(B) * 4};
   for (int i = 0; i < 4; ++i) {
@@ -616,9 +619,14 @@ fa_status fa_decode(const void* Q, const void* Kc, const void* Vc, const int* ca
   fa::DecodeArgs a;
   std::memset(&a, 0, sizeof(a));
   const long long BHkv = static_cast<long long>(B) * Hkv;
-  const int rows = fa::decode_key_rows(d);
-  if ((st = make_map(&a.tmK, Kc, d, Nmax, BHkv, bf16, rows)) != FA_OK) return st;
-  if ((st = make_map(&a.tmV, Vc, d, Nmax, BHkv, bf16, rows)) != FA_OK) return st;
+  const int rows = fa::decode_key_rows(d, c8);
+  if (c8) {
+    if ((st = make_map_bytes(&a.tmK, Kc, d, Nmax, BHkv, rows)) != FA_OK) return st;
+    if ((st = make_map_bytes(&a.tmV, Vc, d, Nmax, BHkv, rows)) != FA_OK) return st;
+  } else {
+    if ((st = make_map(&a.tmK, Kc, d, Nmax, BHkv, bf16, rows)) != FA_OK) return st;
+    if ((st = make_map(&a.tmV, Vc, d, Nmax, BHkv, bf16, rows)) != FA_OK) return st;
+  }
   if ((st = ctl_for_launch(&a.ctl)) != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = workspace;
@@ -639,14 +647,34 @@ fa_status fa_decode(const void* Q, const void* Kc, const void* Vc, const int* ca
   a.Nmax = Nmax;
   a.n_splits = splits;
   a.chunk = chunk;
-  a.c_log2 = scale * 1.4426950408889634f;
-  cudaError_t e = fa::launch_decode(a, d, bf16, s);
+  a.c_log2 = scale * (c8 ? k_scale : 1.f) * 1.4426950408889634f;
+  a.o_scale = c8 ? v_scale : 1.f;
+  cudaError_t e = fa::launch_decode(a, d, bf16, c8, s);
   if (owned) {
     cudaError_t e2 = cudaFreeAsync(ws, s);
     if (e == cudaSuccess) e = e2;
   }
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
+}
+
+fa_status fa_decode(const void* Q, const void* Kc, const void* Vc, const int* cache_seqlens,
+                    void* O, float* L, void* workspace, size_t workspace_bytes, int B, int H,
+                    int Hkv, int Nmax, int d, float scale, fa_dtype dtype, void* stream) {
+  return decode_impl(Q, Kc, Vc, cache_seqlens, O, L, workspace, workspace_bytes, B, H, Hkv, Nmax,
+                     d, scale, dtype, stream, false, 1.f, 1.f);
+}
+
+fa_status fa_decode_fp8(const void* Q, const void* Kc8, const void* Vc8, const int* cache_seqlens,
+                        void* O, float* L, void* workspace, size_t workspace_bytes, int B, int H,
+                        int Hkv, int Nmax, int d, float scale, float k_scale, float v_scale,
+                        fa_dtype dtype, void* stream) {
+  for (float x : {k_scale, v_scale})
+    if (!(std::isfinite(x) && x > 0.f)) return FA_ERR_INVALID_VALUE;
+  if (d != 128 && check_common(B, H, Nmax, d, 0, scale, static_cast<int>(dtype)) == FA_OK)
+    return FA_ERR_UNSUPPORTED;
+  return decode_impl(Q, Kc8, Vc8, cache_seqlens, O, L, workspace, workspace_bytes, B, H, Hkv,
+                     Nmax, d, scale, dtype, stream, true, k_scale, v_scale);
 }
 
 }  // extern "C"

@@ -33,6 +33,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 namespace fa {
 
@@ -41,23 +42,25 @@ namespace {
 constexpr int DEC_WARPS = 4;
 constexpr int DEC_STAGES = 2;
 
-// Geometry of one ring stage for head dim D.
-template <int D>
+// Geometry of one ring stage for head dim D, with 16-bit caches or (C8) E4M3 ones.
+template <int D, bool C8 = false>
 struct DecGeom {
-  static constexpr int BOXC = D == 32 ? 32 : 64;       // columns of one TMA box (one swizzle span)
-  static constexpr int SWM = D == 32 ? 3 : 7;          // 16-byte chunk bits ^= row bits (64/128 B)
+  static constexpr int ELEM = C8 ? 1 : 2;              // bytes per cached value
+  static constexpr int BOXC = C8 ? D : (D == 32 ? 32 : 64);   // columns of one TMA box
+  static constexpr int ROWB = BOXC * ELEM;             // bytes of one box row (one swizzle span)
+  static constexpr int SWM = ROWB == 128 ? 7 : 3;      // 16-byte chunk bits ^= row bits (128/64 B)
   static constexpr int HALVES = D / BOXC;              // lanes sharing one key in the score step
   static constexpr int KEYS = 32 / HALVES;             // keys per stage
-  static constexpr int BOXB = KEYS * BOXC * 2;         // bytes of one box (a multiple of 1 KiB)
+  static constexpr int BOXB = KEYS * ROWB;             // bytes of one box (a multiple of 1 KiB)
   static constexpr int TILEB = HALVES * BOXB;          // K (or V) rows of one stage
   static constexpr int STAGEB = 2 * TILEB;             // K then V
   static constexpr int QS = HALVES * (BOXC + 4);       // floats per q row (halves 16 B apart mod 128)
   static constexpr int VEC = D / 32;                   // output columns per lane
 };
 
-template <int D, int R>
+template <int D, int R, bool C8>
 constexpr int dec_smem_bytes() {
-  using G = DecGeom<D>;
+  using G = DecGeom<D, C8>;
   return 1024 + DEC_WARPS * DEC_STAGES * G::STAGEB + R * G::QS * 4 + DEC_WARPS * G::KEYS * R * 4 +
          DEC_WARPS * DEC_STAGES * 8;
 }
@@ -110,13 +113,23 @@ __device__ __forceinline__ float load_f(const void* p, size_t i) {
   return unpack2<BF16>(static_cast<uint32_t>(x)).x;
 }
 
-template <int D, bool BF16, int R>
+// Four E4M3 codes (a 32-bit word) as floats.
+__device__ __forceinline__ void e4m3x4_to_f(uint32_t w, float* out) {
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu),
+                                                     __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16),
+                                                     __NV_E4M3);
+  const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+  out[0] = a.x; out[1] = a.y; out[2] = b.x; out[3] = b.y;
+}
+
+template <int D, bool BF16, int R, bool C8>
 __global__ void __launch_bounds__(32 * DEC_WARPS, 3)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const void* __restrict__ Q,
                         const int* __restrict__ seqlens, float* __restrict__ part, int H, int Hkv,
                         int Nmax, int chunk, int n_splits, float c_log2, KernelCtl ctl) {
-  using G = DecGeom<D>;
+  using G = DecGeom<D, C8>;
   constexpr int KEYS = G::KEYS, VEC = G::VEC;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_rc = (H / Hkv) / R;               // row groups per K/V head
@@ -183,7 +196,7 @@ __global__ void __launch_bounds__(32 * DEC_WARPS, 3)
   const uint32_t q_lane = qs + half * (G::BOXC + 4) * 4;
   const int col0 = lane * VEC;
   const uint32_t v_lane = (col0 / G::BOXC) * G::BOXB;
-  const uint32_t v_col = (col0 % G::BOXC) * 2;
+  const uint32_t v_col = (col0 % G::BOXC) * G::ELEM;
 
   int c = 0;
   for (; c < nch; ++c) {
@@ -197,19 +210,41 @@ __global__ void __launch_bounds__(32 * DEC_WARPS, 3)
 #pragma unroll
     for (int r = 0; r < R; ++r) s2[r] = make_float2(0.f, 0.f);
     const uint32_t krow = kt + half * G::BOXB;
+    if constexpr (C8) {
+      // 16 E4M3 codes per 16-byte chunk of this lane's key row
 #pragma unroll
-    for (int cc = 0; cc < G::BOXC / 8; ++cc) {
-      const uint4 kw = lds128(krow + swz<G::SWM>(key * G::BOXC * 2 + cc * 16));
-      const float2 k0 = unpack2<BF16>(kw.x), k1 = unpack2<BF16>(kw.y);
-      const float2 k2 = unpack2<BF16>(kw.z), k3 = unpack2<BF16>(kw.w);
+      for (int cc = 0; cc < G::ROWB / 16; ++cc) {
+        const uint4 kw = lds128(krow + swz<G::SWM>(key * G::ROWB + cc * 16));
+        float k[16];
+        e4m3x4_to_f(kw.x, k);
+        e4m3x4_to_f(kw.y, k + 4);
+        e4m3x4_to_f(kw.z, k + 8);
+        e4m3x4_to_f(kw.w, k + 12);
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float4 qa = lds128f(q_lane + (r * G::QS + cc * 8) * 4);
-        const float4 qb = lds128f(q_lane + (r * G::QS + cc * 8 + 4) * 4);
-        s2[r] = fma2(make_float2(qa.x, qa.y), k0, s2[r]);
-        s2[r] = fma2(make_float2(qa.z, qa.w), k1, s2[r]);
-        s2[r] = fma2(make_float2(qb.x, qb.y), k2, s2[r]);
-        s2[r] = fma2(make_float2(qb.z, qb.w), k3, s2[r]);
+        for (int r = 0; r < R; ++r) {
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const float4 qv = lds128f(q_lane + (r * G::QS + cc * 16 + 4 * qq) * 4);
+            s2[r] = fma2(make_float2(qv.x, qv.y), make_float2(k[4 * qq], k[4 * qq + 1]), s2[r]);
+            s2[r] = fma2(make_float2(qv.z, qv.w), make_float2(k[4 * qq + 2], k[4 * qq + 3]), s2[r]);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int cc = 0; cc < G::BOXC / 8; ++cc) {
+        const uint4 kw = lds128(krow + swz<G::SWM>(key * G::ROWB + cc * 16));
+        const float2 k0 = unpack2<BF16>(kw.x), k1 = unpack2<BF16>(kw.y);
+        const float2 k2 = unpack2<BF16>(kw.z), k3 = unpack2<BF16>(kw.w);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float4 qa = lds128f(q_lane + (r * G::QS + cc * 8) * 4);
+          const float4 qb = lds128f(q_lane + (r * G::QS + cc * 8 + 4) * 4);
+          s2[r] = fma2(make_float2(qa.x, qa.y), k0, s2[r]);
+          s2[r] = fma2(make_float2(qa.z, qa.w), k1, s2[r]);
+          s2[r] = fma2(make_float2(qb.x, qb.y), k2, s2[r]);
+          s2[r] = fma2(make_float2(qb.z, qb.w), k3, s2[r]);
+        }
       }
     }
     const bool valid = key < nk;
@@ -262,7 +297,15 @@ __global__ void __launch_bounds__(32 * DEC_WARPS, 3)
           asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pv[r]) : "r"(ps + (kk * R + r) * 4));
       }
       float v[VEC];
-      lds_vec<VEC, BF16>(vt + v_lane + swz<G::SWM>(kk * G::BOXC * 2 + v_col), v);
+      if constexpr (C8) {                        // VEC = 4 codes, one 32-bit word
+        uint32_t x;
+        asm volatile("ld.shared.b32 %0, [%1];"
+                     : "=r"(x)
+                     : "r"(vt + v_lane + swz<G::SWM>(kk * G::ROWB + v_col)));
+        e4m3x4_to_f(x, v);
+      } else {
+        lds_vec<VEC, BF16>(vt + v_lane + swz<G::SWM>(kk * G::ROWB + v_col), v);
+      }
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -325,7 +368,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(D)
     decode_merge_kernel(const float* __restrict__ part, const int* __restrict__ seqlens,
                         void* __restrict__ O, float* __restrict__ L, int H, int Nmax, int chunk,
-                        int n_splits) {
+                        int n_splits, float o_scale) {
   const size_t row = blockIdx.x;                 // b * H + h
   const int b = static_cast<int>(row / H);
   const int n = min(max(__ldg(seqlens + b), 0), Nmax);
@@ -345,7 +388,7 @@ __global__ void __launch_bounds__(D)
       acc = fmaf(sp[4 + threadIdx.x], a, acc);
     }
   }
-  const float o = l > 0.f ? acc / l : 0.f;
+  const float o = l > 0.f ? acc / l * o_scale : 0.f;
   if constexpr (BF16)
     reinterpret_cast<__nv_bfloat16*>(O)[row * D + threadIdx.x] = __float2bfloat16_rn(o);
   else
@@ -353,10 +396,10 @@ __global__ void __launch_bounds__(D)
   if (threadIdx.x == 0) L[row] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
 }
 
-template <int D, bool BF16, int R>
+template <int D, bool BF16, int R, bool C8>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
-  constexpr int smem = dec_smem_bytes<D, R>();
-  auto kern = decode_split_kernel<D, BF16, R>;
+  constexpr int smem = dec_smem_bytes<D, R, C8>();
+  auto kern = decode_split_kernel<D, BF16, R, C8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long ctas =
@@ -382,18 +425,18 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, BF16>, static_cast<const float*>(a.part),
-                         a.seqlens, a.O, a.L, a.H, a.Nmax, a.chunk, a.n_splits);
+                         a.seqlens, a.O, a.L, a.H, a.Nmax, a.chunk, a.n_splits, a.o_scale);
   trace_end(TR_DEC_MERGE, st);
   return e;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool C8 = false>
 cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t st) {
   switch (decode_rows(a.H, a.Hkv)) {
-    case 8: return launch_decode_t<D, BF16, 8>(a, st);
-    case 4: return launch_decode_t<D, BF16, 4>(a, st);
-    case 2: return launch_decode_t<D, BF16, 2>(a, st);
-    default: return launch_decode_t<D, BF16, 1>(a, st);
+    case 8: return launch_decode_t<D, BF16, 8, C8>(a, st);
+    case 4: return launch_decode_t<D, BF16, 4, C8>(a, st);
+    case 2: return launch_decode_t<D, BF16, 2, C8>(a, st);
+    default: return launch_decode_t<D, BF16, 1, C8>(a, st);
   }
 }
 
@@ -419,9 +462,13 @@ int decode_parts(int B, int H, int Hkv, int Nmax, int* chunk) {
   return static_cast<int>((Nmax + c - 1) / c);
 }
 
-int decode_key_rows(int d) { return d == 128 ? 16 : 32; }
+int decode_key_rows(int d, bool c8) { return (d == 128 && !c8) ? 16 : 32; }
 
-cudaError_t launch_decode(const DecodeArgs& a, int d, bool bf16, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeArgs& a, int d, bool bf16, bool c8, cudaStream_t st) {
+  if (c8) {                                      // E4M3 caches: d = 128
+    if (d != 128) return cudaErrorInvalidValue;
+    return bf16 ? launch_decode_d<128, true, true>(a, st) : launch_decode_d<128, false, true>(a, st);
+  }
   if (d == 32) return bf16 ? launch_decode_d<32, true>(a, st) : launch_decode_d<32, false>(a, st);
   if (d == 64) return bf16 ? launch_decode_d<64, true>(a, st) : launch_decode_d<64, false>(a, st);
   if (d == 128)

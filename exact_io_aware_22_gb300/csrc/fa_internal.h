@@ -83,16 +83,17 @@ struct DecodeArgs {
   float* part;                 // workspace: (B*H, n_splits, d+4) partial states
   int B, H, Hkv, Nmax;
   int n_splits, chunk;         // splits of the cache and keys per split
-  float c_log2;                // scale * log2(e)
+  float c_log2;                // scale * log2(e) (E4M3 caches: times k_scale)
+  float o_scale;               // 1 (E4M3 caches: v_scale)
   KernelCtl ctl;
 };
 // Query rows that one decode CTA serves from each K/V row (a power of two dividing H/Hkv).
 int decode_rows(int H, int Hkv);
-// Keys per ring stage of the decode kernel (the TMA box height).
-int decode_key_rows(int d);
+// Keys per ring stage of the decode kernel (the TMA box height); c8: E4M3 caches.
+int decode_key_rows(int d, bool c8);
 // Splits and keys per split (written to *chunk) for caches of Nmax keys.
 int decode_parts(int B, int H, int Hkv, int Nmax, int* chunk);
-cudaError_t launch_decode(const DecodeArgs& a, int d, bool bf16, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, int d, bool bf16, bool c8, cudaStream_t st);
 
 // Forward on 8-bit E4M3 inputs, d = 128, dense (B, H, N, 128) layout.
 struct Fwd8Args {

@@ -81,6 +81,32 @@ def make_decode_inputs(B: int, H: int, Hkv: int, Nmax: int, d: int, lens, dtype:
             "cache_seqlens": torch.tensor([int(n) for n in lens], dtype=torch.int32)}
 
 
+def make_decode_fp8_inputs(B: int, H: int, Hkv: int, Nmax: int, d: int, lens,
+                           dtype: str = "bf16", seed: int = 0, fill_code: int | None = None):
+    """Decoding inputs with E4M3 caches: q drawn and rounded as in make_decode_inputs, then
+    K and V caches drawn in fp32 N(0, 1), each divided by its scale amax / 448 and rounded
+    to E4M3 by torch's float8_e4m3fn conversion.  Returns dict(q, k8, v8 (uint8 codes,
+    (B, Hkv, Nmax, d)), cache_seqlens, k_scale, v_scale).  With ``fill_code`` every cache
+    row at or past its sequence's length holds that code (0x7F: NaN)."""
+    if len(lens) != B:
+        raise ValueError("lens must hold B lengths")
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((B, H, d), generator=g, dtype=torch.float32).to(DTYPES[dtype])
+    out = {"q": q}
+    for name in ("k", "v"):
+        x = torch.randn((B, Hkv, Nmax, d), generator=g, dtype=torch.float32)
+        sc = torch.tensor(float(x.abs().max()) / 448.0, dtype=torch.float32)
+        codes = (x / sc).to(torch.float8_e4m3fn).view(torch.uint8).clone()
+        if fill_code is not None:
+            for b, n in enumerate(lens):
+                codes[b, :, int(n):] = int(fill_code)
+        out[name + "8"] = codes
+        out[name + "_scale"] = float(sc)
+    out["cache_seqlens"] = torch.tensor([int(n) for n in lens], dtype=torch.int32)
+    return out
+
+
 def make_fp8_inputs(B: int, H: int, N: int, d: int, seed: int = 0, Hkv: int | None = None):
     """8-bit E4M3 inputs with per-tensor scales: Q, K, V drawn like make_inputs (fp32
     N(0, 1), in that order), each divided by its scale amax / 448 (so the largest

@@ -210,6 +210,20 @@ fa_status fa_decode(const void* Q, const void* Kc, const void* Vc, const int* ca
                     void* O, float* L, void* workspace, size_t workspace_bytes, int B, int H,
                     int Hkv, int Nmax, int d, float scale, fa_dtype dtype, void* stream);
 
+/* Split-KV decoding from 8-bit E4M3 caches with per-tensor descale factors: as
+ * fa_decode, with Kc8 and Vc8 (B, Hkv, Nmax, d) holding one E4M3 code per value,
+ * standing for k_scale * K and v_scale * V (the FP8 precision of the FlashAttention
+ * note's FlashAttention-3 entry, "Versions and Evolution", applied to a decoding
+ * cache).  The scores are formed in fp32 from the decoded codes and P stays fp32,
+ * so only the cache is in 8 bits.  Q, O in fp16/bf16 (dtype), L fp32 as in
+ * fa_decode; the workspace is fa_decode_workspace_size(B, H, Hkv, Nmax, d) bytes or
+ * NULL.  d must be 128 (FA_ERR_UNSUPPORTED otherwise); k_scale and v_scale must be
+ * positive and finite (FA_ERR_INVALID_VALUE); the other errors are fa_decode's. */
+fa_status fa_decode_fp8(const void* Q, const void* Kc8, const void* Vc8, const int* cache_seqlens,
+                        void* O, float* L, void* workspace, size_t workspace_bytes, int B, int H,
+                        int Hkv, int Nmax, int d, float scale, float k_scale, float v_scale,
+                        fa_dtype dtype, void* stream);
+
 /* Static description of a status code. */
 const char* fa_status_string(fa_status s);
 

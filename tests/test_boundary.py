@@ -258,3 +258,16 @@ def test_quantize_rejects(lib, args, code):
                                0, 1, None) == INVALID
     assert lib.fa_quantize_fp8(ctypes.c_void_p(M1), ctypes.c_void_p(8 * M1), 1, 4, 4, 1.0,
                                0, 7, None) == UNSUPPORTED
+
+
+def test_decode_fp8_rejects(lib):
+    a = [ctypes.c_void_p(M1 * i) for i in (1, 2, 3, 4, 5, 6)]
+    ws = ctypes.c_void_p(0)
+    # d = 64: unsupported for E4M3 caches; non-positive descale factors; bad heads
+    assert lib.fa_decode_fp8(*a, ws, 0, 2, 8, 2, 300, 64, 0.125, 0.01, 0.01, 1, None) == UNSUPPORTED
+    assert lib.fa_decode_fp8(*a, ws, 0, 2, 8, 2, 300, 128, 0.125, 0.0, 0.01, 1, None) == INVALID
+    assert lib.fa_decode_fp8(*a, ws, 0, 2, 8, 2, 300, 128, 0.125, 0.01, -1.0, 1, None) == INVALID
+    assert lib.fa_decode_fp8(*a, ws, 0, 2, 8, 3, 300, 128, 0.125, 0.01, 0.01, 1, None) == INVALID
+    b = list(a)
+    b[1] = ctypes.c_void_p(2 * M1 + 8)
+    assert lib.fa_decode_fp8(*b, ws, 0, 2, 8, 2, 300, 128, 0.125, 0.01, 0.01, 1, None) == MISALIGNED

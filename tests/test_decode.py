@@ -99,3 +99,53 @@ def test_decode_caller_workspace_matches_library_allocation():
     o2, l2 = fa.decode(q, kc, vc, cl, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def run_decode_fp8(B, H, Hkv, Nmax, lens, dtype, seed=0, rows=None):
+    """E4M3 caches: the oracle's decode of the dequantized caches (codes times their
+    descale factors).  Only the cache is in 8 bits (the scores and P stay fp32), so the
+    16-bit decode tolerances hold."""
+    import exact_io_aware_22_gb300 as fa
+    d = 128
+    x = inputs.make_decode_fp8_inputs(B, H, Hkv, Nmax, d, lens, dtype, seed=seed, fill_code=0x7F)
+    scale = 1.0 / math.sqrt(d)
+    q, k8, v8, cl = (x[n].cuda() for n in ("q", "k8", "v8", "cache_seqlens"))
+    o, lse = fa.decode_fp8(q, k8, v8, cl, x["k_scale"], x["v_scale"], scale=scale)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0, "a kernel reported a bounded-wait timeout"
+    o, lse = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    sel = list(range(B)) if rows is None else list(rows)
+    kd = oracle.e4m3_values(x["k8"].numpy()[sel]) * x["k_scale"]
+    vd = oracle.e4m3_values(x["v8"].numpy()[sel]) * x["v_scale"]
+    o_ref, l_ref = oracle.decode(x["q"].double().numpy()[sel], kd, vd,
+                                 x["cache_seqlens"].numpy()[sel], scale)
+    o, lse = o[sel], lse[sel]
+    assert np.isfinite(o).all(), "non-finite O: a row past a sequence's length was read"
+    empty = l_ref == -np.inf
+    assert (lse[empty] == -np.inf).all() and (o[empty] == 0).all()
+    rep = {"o": float(np.max(np.abs(o - o_ref), initial=0.0)),
+           "lse": float(np.max(np.abs(lse[~empty] - l_ref[~empty]), initial=0.0))}
+    assert rep["o"] <= TOL_O[dtype], rep
+    assert rep["lse"] <= TOL_L, rep
+    return rep
+
+
+FP8_CASES = [
+    (4, 32, 8, 1000, "bf16", (1000, 1, 517, 64)),
+    (3, 16, 2, 777, "fp16", (0, 777, 300)),
+    (2, 16, 1, 2000, "bf16", (1999, 1234)),
+    (2, 8, 8, 513, "fp16", (513, 17)),
+    (2, 12, 2, 300, "bf16", (300, 31)),
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=[str(c[:5]) for c in FP8_CASES])
+def test_decode_fp8_cache(case):
+    B, H, Hkv, Nmax, dt, lens = case
+    print(case[:5], run_decode_fp8(B, H, Hkv, Nmax, lens, dt, seed=Nmax))
+
+
+def test_decode_fp8_full_size_sampled():
+    B, H, Hkv, Nmax = 16, 32, 8, 32768
+    lens = tuple(int(n) for n in np.random.default_rng(2027).integers(Nmax // 2, Nmax + 1, B))
+    print(run_decode_fp8(B, H, Hkv, Nmax, lens, "bf16", seed=1, rows=(0, 7, 15)))
