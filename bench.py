@@ -241,6 +241,14 @@ def e2e_measure(torch, h_in, dev_sets, h_out_sets, compute, steps, barrier):
 E2E_NOTE = ("pipelined: step k's inputs copied host->device while step k-1 computes and step "
             "k-2's results are copied device->host (three streams, device tensors "
             "double-buffered); every step moves its own inputs and results")
+E2E_SEQ_NOTE = "sequential: copy in, compute, copy out, one step after another on one stream"
+
+
+def e2e_pick(pms, sms):
+    """(ms per step, mode, other mode's ms) of the faster of the two end-to-end modes."""
+    if pms <= sms:
+        return pms, E2E_NOTE, ("sequential", sms)
+    return sms, E2E_SEQ_NOTE, ("pipelined", pms)
 
 
 def parse():
@@ -578,12 +586,12 @@ def run_ours(args, rank, world, local_rank):
         ke = max(1, min(args.steps, 20))
         pms, sms = e2e_measure(torch, h_in, dev_sets, h_out_sets, compute, ke, barrier)
         pms, sms = max_over_ranks(pms, world, dev), max_over_ranks(sms, world, dev)
-        e2e = {"value": whole_job_tflops(fwd_f + bwd_f, world, pms), "unit": "TFLOP/s",
+        ems, mode, (other, oms) = e2e_pick(pms, sms)
+        e2e = {"value": whole_job_tflops(fwd_f + bwd_f, world, ems), "unit": "TFLOP/s",
                "h2d_bytes_per_step": in_bytes,
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs.values()),
-               "ms_per_step": pms, "steps": ke, "mode": E2E_NOTE,
-               "sequential": {"value": whole_job_tflops(fwd_f + bwd_f, world, sms),
-                              "ms_per_step": sms}}
+               "ms_per_step": ems, "steps": ke, "mode": mode,
+               other: {"value": whole_job_tflops(fwd_f + bwd_f, world, oms), "ms_per_step": oms}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -770,11 +778,12 @@ def run_decode(args, rank, world, local_rank):
         ke = max(1, min(args.steps, 10))
         pms, sms = e2e_measure(torch, h_in, dev_sets, h_out_sets, compute, ke, barrier)
         pms, sms = max_over_ranks(pms, world, dev), max_over_ranks(sms, world, dev)
-        e2e = {"value": world * alg_bytes / (pms / 1e3) / 1e9, "unit": "GB/s",
+        ems, mode, (other, oms) = e2e_pick(pms, sms)
+        e2e = {"value": world * alg_bytes / (ems / 1e3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in.values()),
                "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * 4,
-               "ms_per_step": pms, "steps": ke, "mode": E2E_NOTE,
-               "sequential": {"value": world * alg_bytes / (sms / 1e3) / 1e9, "ms_per_step": sms},
+               "ms_per_step": ems, "steps": ke, "mode": mode,
+               other: {"value": world * alg_bytes / (oms / 1e3) / 1e9, "ms_per_step": oms},
                "note": "the whole K/V cache is copied host to device every step"}
 
     cpu = None
@@ -931,11 +940,12 @@ def run_fp8(args, rank, world, local_rank):
         ke = max(1, min(args.steps, 20))
         pms, sms = e2e_measure(torch, h_in, dev_sets, h_out_sets, compute, ke, barrier)
         pms, sms = max_over_ranks(pms, world, dev), max_over_ranks(sms, world, dev)
-        e2e = {"value": world * fwd_f / (pms / 1e3) / 1e12, "unit": "TFLOP/s",
+        ems, mode, (other, oms) = e2e_pick(pms, sms)
+        e2e = {"value": world * fwd_f / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": sum(t.numel() for t in h_in.values()),
                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
-               "ms_per_step": pms, "steps": ke, "mode": E2E_NOTE,
-               "sequential": {"value": world * fwd_f / (sms / 1e3) / 1e12, "ms_per_step": sms}}
+               "ms_per_step": ems, "steps": ke, "mode": mode,
+               other: {"value": world * fwd_f / (oms / 1e3) / 1e12, "ms_per_step": oms}}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
