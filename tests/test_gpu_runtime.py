@@ -125,3 +125,74 @@ def test_gqa_entry_points_with_equal_heads_match_mha():
     assert fa.device_status() == 0
     for a, b in ((o, o2), (lse, lse2), (dq, dq2), (dk, dk2), (dv, dv2)):
         assert torch.equal(a, b)
+
+
+def _guarded(count, dtype, pad=4096, canary=-12345.0):
+    buf = torch.full((count + pad,), float("nan"), dtype=dtype, device="cuda")
+    buf[count:] = canary
+    return buf
+
+
+def _check_guard(buf, count, canary=-12345.0):
+    stored = torch.tensor(canary, dtype=buf.dtype).float().item()
+    head, tail = buf[:count].float(), buf[count:].float()
+    return bool(torch.isfinite(head).all()) and bool((tail == stored).all())
+
+
+@pytest.mark.parametrize("fp8_cache", [False, True])
+def test_decode_outputs_guarded_and_deterministic(fp8_cache):
+    """Split-KV decoding overwrites every O and L element (pre-filled with NaN; an empty
+    cache gives O = 0, L = -inf), writes nothing past them, and repeats bit for bit."""
+    fa = _fa()
+    B, H, Hkv, Nmax, d = 3, 16, 4, 1500, 128
+    lens = (1500, 0, 333)
+    if fp8_cache:
+        x = inputs.make_decode_fp8_inputs(B, H, Hkv, Nmax, d, lens, "bf16", seed=8)
+        kc, vc = x["k8"].cuda(), x["v8"].cuda()
+    else:
+        x = inputs.make_decode_inputs(B, H, Hkv, Nmax, d, lens, "bf16", seed=8)
+        kc, vc = x["k_cache"].cuda(), x["v_cache"].cuda()
+    q, cl = x["q"].cuda(), x["cache_seqlens"].cuda()
+
+    def run():
+        ob, lb = _guarded(B * H * d, torch.bfloat16), _guarded(B * H, torch.float32)
+        o, lse = ob[:B * H * d].view(B, H, d), lb[:B * H].view(B, H)
+        if fp8_cache:
+            fa.decode_fp8(q, kc, vc, cl, x["k_scale"], x["v_scale"], out=o, lse=lse)
+        else:
+            fa.decode(q, kc, vc, cl, out=o, lse=lse)
+        torch.cuda.synchronize()
+        return ob, lb, o.clone(), lse.clone()
+
+    ob, lb, o1, l1 = run()
+    assert fa.device_status() == 0
+    assert _check_guard(ob, B * H * d)
+    assert bool((lb[B * H:] == -12345.0).all())
+    assert bool(torch.isfinite(lb[:B * H].view(B, H)[[0, 2]]).all())
+    assert bool((lb[:B * H].view(B, H)[1] == -float("inf")).all())
+    _, _, o2, l2 = run()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_fwd_fp8_outputs_guarded_and_deterministic():
+    """The FP8 forward overwrites every O and L element, writes nothing past them, and
+    repeats bit for bit."""
+    fa = _fa()
+    B, H, N, d = 1, 4, 400, 128
+    x = inputs.make_fp8_inputs(B, H, N - N % 16, d, seed=9, Hkv=2)
+    N = N - N % 16
+    q8, k8, vt8 = (x[n].cuda() for n in ("q8", "k8", "vt8"))
+
+    def run():
+        ob, lb = _guarded(B * H * N * d, torch.bfloat16), _guarded(B * H * N, torch.float32)
+        o, lse = ob[:B * H * N * d].view(B, H, N, d), lb[:B * H * N].view(B, H, N)
+        fa.fwd_fp8(q8, k8, vt8, x["q_scale"], x["k_scale"], x["v_scale"], causal=True, out=o,
+                   lse=lse)
+        torch.cuda.synchronize()
+        return ob, lb, o.clone(), lse.clone()
+
+    ob, lb, o1, l1 = run()
+    assert fa.device_status() == 0
+    assert _check_guard(ob, B * H * N * d) and _check_guard(lb, B * H * N)
+    _, _, o2, l2 = run()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
