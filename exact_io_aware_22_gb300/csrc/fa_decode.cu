@@ -306,10 +306,23 @@ __global__ void __launch_bounds__(32 * DEC_WARPS, 3)
       } else {
         lds_vec<VEC, BF16>(vt + v_lane + swz<G::SWM>(kk * G::ROWB + v_col), v);
       }
+      if constexpr (VEC % 2 == 0) {               // pairs of columns: packed fp32x2 FMAs
 #pragma unroll
-      for (int r = 0; r < R; ++r)
+        for (int r = 0; r < R; ++r) {
+          const float2 p2 = make_float2(pv[r], pv[r]);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[r][e] = fmaf(pv[r], v[e], acc[r][e]);
+          for (int e = 0; e < VEC; e += 2) {
+            const float2 a = fma2(p2, make_float2(v[e], v[e + 1]), make_float2(acc[r][e], acc[r][e + 1]));
+            acc[r][e] = a.x;
+            acc[r][e + 1] = a.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[r][e] = fmaf(pv[r], v[e], acc[r][e]);
+      }
     }
     __syncwarp();                                 // stage and P read by every lane
     if (lane == 0 && c + DEC_STAGES < nch) issue(c + DEC_STAGES, st);
