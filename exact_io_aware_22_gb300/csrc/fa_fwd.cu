@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sg + C::SLOT_OFF);
 
   if (warp == 0) {
+    regs_dec<kRegsLow>();                          // warpgroup 0 (TMA, MMA issue): few registers
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_stream > 0) {
       bool ok = true;
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
+    regs_dec<kRegsLow>();
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_stream > 0) {
       constexpr uint32_t idS = umma_idesc_f16(BM, BN, BF16, false, false);
@@ -253,6 +255,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
+    regs_inc<kRegsHigh>();                         // the compute warpgroups take what it gives back
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;
     const int rit = (warp & 3) * 32 + lane;              // row within the tile (= TMEM lane)
@@ -372,6 +375,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                        : static_cast<size_t>(bh) * N + grow] =
             (m_run + log2f(l_run)) * 0.69314718055994531f;
     }
+  } else {
+    regs_dec<kRegsLow>();                          // warps 2 and 3: idle
   }
   // ------------------------------------------------------------ teardown
   tc_fence_before();
@@ -386,8 +391,9 @@ template <int D, bool BF16, bool CAUSAL, bool WINDOW, bool PACKED>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   using C = Cfg<D>;
   auto kern = fwd_kernel<D, BF16, CAUSAL, WINDOW, PACKED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  cudaError_t e = check_split_regs(reinterpret_cast<const void*>(kern));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int n_qblk = (a.N + NT * BM - 1) / (NT * BM);
   const long long grid = static_cast<long long>(n_qblk) * a.BH;

@@ -97,6 +97,39 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl));
 }
 
+// Register split between warpgroups (setmaxnreg): the launch gives every thread the
+// kernel's register count; a warpgroup that gives some back (dec) lets another take
+// them (inc, which waits until they are free).  Every warp of a warpgroup executes the
+// same call.  For a 384-thread CTA launched at 168 registers per thread (64,512 in
+// all), one warpgroup at 40 and two at 232 use exactly that total.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+constexpr uint32_t kRegsLaunch = 168, kRegsLow = 72, kRegsHigh = 216;
+static_assert(128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch,
+              "register split must use exactly the launch allocation");
+// Host check before launching a kernel that splits its registers: it must have been
+// compiled to exactly kRegsLaunch registers per thread, or the split would not add up
+// (an inc would wait for registers that no warpgroup gives back).  Results are kept
+// per kernel.
+inline cudaError_t check_split_regs(const void* kern) {
+  static const void* seen[256];
+  static int n_seen = 0;
+  for (int i = 0; i < n_seen; ++i)
+    if (seen[i] == kern) return cudaSuccess;
+  cudaFuncAttributes fa;
+  const cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorInvalidConfiguration;
+  if (n_seen < 256) seen[n_seen++] = kern;
+  return cudaSuccess;
+}
+
 // Named barrier among a subset of warps (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
