@@ -209,7 +209,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sg + SLOT_OFF);
 
   if (warp == 0) {
-    regs_dec<kRegsLow>();                          // warpgroup 0 (TMA, MMA issue): few registers
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(bar(B_KV), 2 * TILE);
@@ -255,7 +254,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    regs_dec<kRegsLow>();
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_iter > 0) {
       constexpr uint32_t idS = umma_idesc_f16(BT, BT, BF16, false, false);   // S^T, dP^T
@@ -323,7 +321,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    regs_inc<kRegsHigh>();                         // the compute warpgroups take what it gives back
     // ------------------------------------------------------------ compute
     const int h = (warp - 4) >> 2;                 // query columns [64h, 64h + 64)
     const int kr = (warp & 3) * 32 + lane;         // key row (= TMEM lane)
@@ -456,8 +453,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       store_row<NC, BF16>(tmem + lane_off + DK_COL + 64 * h, scale, reinterpret_cast<T*>(dK) + roff,
                         valid);
     }
-  } else {
-    regs_dec<kRegsLow>();                          // warps 2 and 3: idle
   }
   tc_fence_before();
   __syncthreads();
@@ -777,9 +772,7 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
   {
     auto kern = dkdv128_kernel<HD, BF16, CAUSAL>;
     constexpr int smem = kv::Smem<HD>::SMEM_BYTES;
-    cudaError_t e = check_split_regs(reinterpret_cast<const void*>(kern));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DKDV, st);
     kern<<<static_cast<unsigned>(nblk_kv), THREADS, smem, st>>>(

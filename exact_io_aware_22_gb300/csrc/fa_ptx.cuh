@@ -101,7 +101,9 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
 // kernel's register count; a warpgroup that gives some back (dec) lets another take
 // them (inc, which waits until they are free).  Every warp of a warpgroup executes the
 // same call.  For a 384-thread CTA launched at 168 registers per thread (64,512 in
-// all), one warpgroup at 40 and two at 232 use exactly that total.
+// all), one warpgroup at 88 and two at 208 use exactly that total.  Values that live
+// across the call must fit the new count, or they go to local memory: with fewer
+// than 88, the loaders of the forward and dQ kernels spilled.
 template <uint32_t N>
 __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
@@ -110,7 +112,7 @@ template <uint32_t N>
 __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
-constexpr uint32_t kRegsLaunch = 168, kRegsLow = 72, kRegsHigh = 216;
+constexpr uint32_t kRegsLaunch = 168, kRegsLow = 88, kRegsHigh = 208;
 static_assert(128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch,
               "register split must use exactly the launch allocation");
 // Host check before launching a kernel that splits its registers: it must have been
