@@ -12,17 +12,19 @@
 // Both products run as tcgen05.mma kind::f8f6f4 with both operands K-major in
 // shared memory, fp32 accumulators in TMEM:
 //   S   = Q K^T     A = Q tile (128 rows x 128 bytes of d), B = K tile (same shape)
-//   O  += P V       A = P tile (128 query rows x 128 bytes of keys), written by the
-//                   softmax threads as E4M3; B = V^T tile (128 rows of d x 128 bytes
-//                   of keys), V^T being the caller's transposed copy of V.
-// At d = 128 every tile is 128 rows of 128 bytes, one 128-byte swizzle span, so
-// each product is four MMAs of K = 32 bytes.
+//   O  += P V       A = P (128 query rows x 128 keys as E4M3), written by the softmax
+//                   threads into TMEM over the first 32 columns of their S tile (four
+//                   codes per 32-bit column, the lowest key in the lowest byte); B =
+//                   V^T tile (128 rows of d x 128 bytes of keys), V^T being the
+//                   caller's transposed copy of V.
+// At d = 128 every shared-memory tile is 128 rows of 128 bytes, one 128-byte swizzle
+// span, so each product is four MMAs of K = 32 bytes.
 //
 // Warp roles and TMEM are those of the 16-bit forward (one CTA per SM, 384
 // threads): warp 0 TMA, warp 1 TMEM and MMA issue, warps 4-7 / 8-11 softmax for
-// query tiles 0 / 1; TMEM S0 | S1 | O0 | O1.  P goes through shared memory instead
-// of TMEM: its tile is rewritten only after the S MMA of the next KV tile has
-// completed, which the MMA thread issues after the P.V MMA that reads it.
+// query tiles 0 / 1; TMEM S0 | S1 | O0 | O1, P over the start of S as in the 16-bit
+// forward: the S MMA of the next KV tile, which overwrites it, is issued after the
+// P.V MMA that reads it, and the tensor pipe runs them in order.
 // The probabilities p = 2^(s - m) lie in (0, 2^8] (lazy running max, as in the
 // 16-bit forward), inside the E4M3 range (largest finite value 448); l sums the
 // unrounded p.
@@ -51,8 +53,7 @@ constexpr int TILE = 128 * 128;                 // one 128-row tile of 128 bytes
 constexpr int Q_OFF = 0;
 constexpr int K_OFF = Q_OFF + NT * TILE;
 constexpr int V_OFF = K_OFF + STAGES * TILE;
-constexpr int P_OFF = V_OFF + STAGES * TILE;
-constexpr int BAR_OFF = P_OFF + NT * TILE;
+constexpr int BAR_OFF = V_OFF + STAGES * TILE;
 // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_full[2], done
 constexpr int NBARS = 1 + 4 * STAGES + 7;
 constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
@@ -75,6 +76,18 @@ __device__ __forceinline__ void umma8_ss_w(uint32_t d_tmem, uint32_t alo, uint32
       "setp.ne.b32 p, %5, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %4, p;\n\t}" ::"r"(d_tmem),
       "r"(alo), "r"(blo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], 8-bit operands (A: one row per lane, four codes per
+// 32-bit column), B's descriptor given as words.
+__device__ __forceinline__ void umma8_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo,
+                                           uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\tmov.b64 b, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(blo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -180,7 +193,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // k-step of 32 bytes is +2 in the descriptor's low word
       constexpr uint32_t HI = sdesc_hi(1024, UMMA_SW128), TILE_W = TILE >> 4;
       const uint32_t q_lo = sdesc_lo(sb + Q_OFF, 16), k_lo = sdesc_lo(sb + K_OFF, 16);
-      const uint32_t v_lo = sdesc_lo(sb + V_OFF, 16), p_lo = sdesc_lo(sb + P_OFF, 16);
+      const uint32_t v_lo = sdesc_lo(sb + V_OFF, 16);
       auto issue_S = [&](int t, int s) {
         const uint32_t qa = q_lo + t * TILE_W, ka = k_lo + s * TILE_W;
 #pragma unroll
@@ -188,10 +201,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           umma8_ss_w(tmem + S_COL + t * BN, qa + 2 * kk, ka + 2 * kk, HI, idS, kk > 0);
       };
       auto issue_PV = [&](int t, int s, bool acc) {
-        const uint32_t pa = p_lo + t * TILE_W, va = v_lo + s * TILE_W, acc0 = acc ? 1u : 0u;
+        const uint32_t va = v_lo + s * TILE_W, acc0 = acc ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BN / 32; ++kk)
-          umma8_ss_w(tmem + O_COL + t * HD, pa + 2 * kk, va + 2 * kk, HI, idO,
+          umma8_ts_w(tmem + O_COL + t * HD, tmem + S_COL + t * BN + 8 * kk, va + 2 * kk, HI, idO,
                      kk > 0 ? 1u : acc0);
       };
       bool ok = mbar_wait(bar(B_QF), 0, ctl) && mbar_wait(bar(B_KF(0)), 0, ctl);
@@ -246,9 +259,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + S_COL + t * BN;
     const uint32_t tO = tmem + lane_off + O_COL + t * HD;
-    // this row of the P tile: 128 bytes, 16-byte chunk c at (c ^ (row & 7)) * 16
-    const uint32_t prow = sb + P_OFF + t * TILE + rit * 128;
-    const uint32_t pswz = static_cast<uint32_t>(rit & 7);
     const int nt = n_t[t];
     const int tile_row0 = row0 + t * BM;
     float m_run = -INFINITY, l_run = 0.f;
@@ -289,9 +299,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
       const float2 c2 = make_float2(c_log2, c_log2), nm2 = make_float2(-m_sub, -m_sub);
       float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t w[32];                            // the row of P: keys 4i .. 4i+3 in word i
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        uint32_t w[8];                           // 32 probabilities of columns 32h .. 32h+31
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
           const int c = 32 * h + 2 * i;
@@ -301,16 +311,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float2 p1 = make_float2(ex2(t1.x), ex2(t1.y));
           rs2[0] = add2(rs2[0], p0);
           rs2[1] = add2(rs2[1], p1);
-          w[i / 2] = e4m3x2(p0.x, p0.y) | (e4m3x2(p1.x, p1.y) << 16);
+          w[8 * h + i / 2] = e4m3x2(p0.x, p0.y) | (e4m3x2(p1.x, p1.y) << 16);
         }
-        const uint32_t c0 = 2 * h, c1 = 2 * h + 1;
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((c0 ^ pswz) << 4)),
-                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                     : "memory");
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((c1 ^ pswz) << 4)),
-                     "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                     : "memory");
       }
+      tmem_st32(tS, w);                          // P over the first 32 columns of S
       const float rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
       l_run = l_run * alpha + rs;
       if (j > 0 && __any_sync(0xffffffffu, grow_m)) {
@@ -333,7 +337,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       m_run = m_use;
       tmem_st_wait();
-      fence_proxy_async_smem();                  // P stores visible to the tensor cores
       tc_fence_before();
       mbar_arrive(bar(B_PF(t)));
     }
