@@ -3,6 +3,7 @@
 // (kind::f16, fp32 accumulation in TMEM), commits, TMEM loads/stores, and the
 // UMMA shared-memory / instruction descriptors.
 #pragma once
+#include <mutex>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -118,10 +119,12 @@ static_assert(128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch,
 // Host check before launching a kernel that splits its registers: it must have been
 // compiled to exactly kRegsLaunch registers per thread, or the split would not add up
 // (an inc would wait for registers that no warpgroup gives back).  Results are kept
-// per kernel.
+// per kernel; launches from several host threads share the record under a lock.
 inline cudaError_t check_split_regs(const void* kern) {
+  static std::mutex mu;
   static const void* seen[256];
   static int n_seen = 0;
+  std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_seen; ++i)
     if (seen[i] == kern) return cudaSuccess;
   cudaFuncAttributes fa;
