@@ -251,7 +251,19 @@ def e2e_pick(pms, sms):
     return sms, E2E_SEQ_NOTE, ("pipelined", pms)
 
 
-def parse():
+def emit(out: dict, args) -> None:
+    """Print the result as one JSON line; with --json-out also write it to that file."""
+    line = json.dumps(out)
+    print(line, flush=True)
+    path = getattr(args, "json_out", None)
+    if path:
+        d = os.path.dirname(os.path.abspath(path))
+        os.makedirs(d, exist_ok=True)
+        with open(path, "w") as f:
+            f.write(line + "\n")
+
+
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
@@ -263,7 +275,9 @@ def parse():
                     default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--json-out", default=None,
+                    help="also write the JSON line to this file (rank 0)")
+    return ap.parse_args(argv)
 
 
 def load_peaks():
@@ -415,7 +429,7 @@ def run_reference(args, rank, world):
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
-    print(json.dumps(out), flush=True)
+    emit(out, args)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -620,7 +634,7 @@ def run_ours(args, rank, world, local_rank):
                "kernels_ms": {kk: per[kk][0] for kk in per},
                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": launches, "clocks": clocks}
-        print(json.dumps(out), flush=True)
+        emit(out, args)
 
 
 def decode_bytes(lens, H, Hkv, d, elem=2):
@@ -682,7 +696,7 @@ def run_decode_reference(args, rank, world):
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
-    print(json.dumps(out), flush=True)
+    emit(out, args)
 
 
 def run_decode(args, rank, world, local_rank):
@@ -809,7 +823,7 @@ def run_decode(args, rank, world, local_rank):
                "cached_rows_per_s": world * sum(lens) * Hkv / (ms / 1e3),
                "kernels_ms": per, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": launches, "clocks": clocks}
-        print(json.dumps(out), flush=True)
+        emit(out, args)
 
 
 def run_fp8_reference(args, rank, world):
@@ -848,7 +862,7 @@ def run_fp8_reference(args, rank, world):
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
-    print(json.dumps(out), flush=True)
+    emit(out, args)
 
 
 def run_fp8(args, rank, world, local_rank):
@@ -977,7 +991,7 @@ def run_fp8(args, rank, world, local_rank):
                "kernels_ms": {kk: v[0] / v[1] for kk, v in traced.items()},
                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": launches, "clocks": clocks}
-        print(json.dumps(out), flush=True)
+        emit(out, args)
 
 
 def main():

@@ -74,3 +74,14 @@ def test_committed_profiles_have_the_fields_the_bench_reads():
         assert re.search(r"source_sha256:\s*[0-9a-f]{64}", text), n
         assert re.search(r"dram_bytes_per_launch:\s*[0-9]+", text), n
         assert "--clock-control none" in text, n
+
+
+def test_emit_prints_one_line_and_writes_it_with_json_out(tmp_path, capsys):
+    out = {"metric": "m", "value": 1.5, "unit": "TFLOP/s"}
+    bench.emit(out, bench.parse([]))
+    lines = capsys.readouterr().out.splitlines()
+    assert len(lines) == 1 and lines[0].startswith("{")
+    path = tmp_path / "sub" / "line.json"
+    bench.emit(out, bench.parse(["--json-out", str(path)]))
+    printed = capsys.readouterr().out.strip()
+    assert path.read_text().strip() == printed
