@@ -271,3 +271,22 @@ def test_decode_fp8_rejects(lib):
     b = list(a)
     b[1] = ctypes.c_void_p(2 * M1 + 8)
     assert lib.fa_decode_fp8(*b, ws, 0, 2, 8, 2, 300, 128, 0.125, 0.01, 0.01, 1, None) == MISALIGNED
+
+
+def test_trace_kind_names_and_read_rejects(lib):
+    # the per-kernel trace kinds of include/fa.h, in order; none past the last
+    names = [lib.fa_trace_kind_name(k) for k in range(7)]
+    assert names == [b"fwd_kernel", b"bwd_pre_kernel", b"bwd_dkdv_kernel", b"bwd_dq_kernel",
+                     b"decode_split_kernel", b"decode_merge_kernel", b"fwd_fp8_kernel"]
+    assert lib.fa_trace_kind_name(7) is None and lib.fa_trace_kind_name(-1) is None
+    t, n = ctypes.c_double(), ctypes.c_longlong()
+    assert lib.fa_trace_read(7, ctypes.byref(t), ctypes.byref(n)) == INVALID
+    assert lib.fa_trace_read(-1, ctypes.byref(t), ctypes.byref(n)) == INVALID
+    assert lib.fa_trace_read(0, None, ctypes.byref(n)) == INVALID
+    assert lib.fa_trace_read(0, ctypes.byref(t), None) == INVALID
+
+
+def test_wait_limit_setter(lib):
+    # any value is accepted (0 restores the default); no CUDA call is made
+    assert lib.fa_set_wait_limit_ns(1_000_000) == OK
+    assert lib.fa_set_wait_limit_ns(0) == OK
