@@ -291,20 +291,53 @@ def load_peaks():
             "source": "fallback"}
 
 
-def traffic_from_profiles(kernel: str, workload: str):
-    """dram bytes per launch recorded in profiles/<kernel>__<workload>.txt, or None when
-    the file is missing or the kernel's source changed since the capture."""
+def profile_record(kernel: str, workload: str):
+    """(dram bytes per launch, tensor-pipe active % of elapsed cycles) recorded by ncu in
+    profiles/<kernel>__<workload>.txt; (None, None) when the file is missing or the
+    kernel's source changed since the capture, and None for a figure it lacks."""
     path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.txt")
     src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
     if not os.path.exists(path) or not os.path.exists(src):
-        return None
+        return None, None
     text = open(path).read()
     m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_b:
-        return None
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return float(m_b.group(1)) if sha == m_sha.group(1) else None
+    if not m_sha or sha != m_sha.group(1):
+        return None, None
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_t = re.search(r"sm__pipe_tensor_cycles_active[^\n]*?([0-9.]+) %", text)
+    return (float(m_b.group(1)) if m_b else None), (float(m_t.group(1)) if m_t else None)
+
+
+def traffic_from_profiles(kernel: str, workload: str):
+    """dram bytes per launch recorded in profiles/<kernel>__<workload>.txt, or None when
+    the file is missing or the kernel's source changed since the capture."""
+    return profile_record(kernel, workload)[0]
+
+
+# Dense 16-bit tcgen05.mma rate of one SM per clock (M = 128, N >= 128, back-to-back
+# MMAs on one SM: 64 cycles per 128 x 128 x 16 product); the 8-bit kind runs at twice it.
+TENSOR_FLOP_PER_CLK_SM = 8192
+
+
+def tensor_rate_at_clock(sm_count: int, sm_mhz: float, bits: int = 16) -> float:
+    """TFLOP/s the tensor pipes of sm_count SMs deliver at sm_mhz when never idle."""
+    return TENSOR_FLOP_PER_CLK_SM * (2 if bits == 8 else 1) * sm_count * sm_mhz * 1e6 / 1e12
+
+
+def memory_report(lens, H, d, elem, device_bytes, peak_bytes):
+    """The footprint arithmetic of the pages' calculator for sequences of the given
+    lengths (B equal lengths N for a dense batch): the H*N*N score matrix per sequence
+    that ordinary attention materialises against everything the tiled kernel keeps (Q,
+    K, V, O in the input type plus L in fp32), their ratio, the N at which the score
+    matrix of len(lens) sequences of N alone no longer fits the device, and the peak
+    device bytes one step of this library held (inputs, outputs, workspace)."""
+    score = sum(H * n * n * elem for n in lens)
+    linear = sum(4 * H * n * d * elem + 4 * H * n for n in lens)
+    oom_n = math.isqrt(device_bytes // (len(lens) * H * elem))
+    return {"peak_device_bytes_step": peak_bytes, "score_matrix_bytes": score,
+            "linear_footprint_bytes": linear, "score_over_linear": score / linear,
+            "ordinary_attention_runs_out_at_N": oom_n, "device_bytes": device_bytes}
 
 
 class ClockSampler:
@@ -461,6 +494,9 @@ def run_ours(args, rank, world, local_rank):
         lse_shape = (B, H, N)
         ws_bytes = fa.bwd_workspace_size(B, H, N, d, causal)
     scale = 1.0 / math.sqrt(d)
+    torch.cuda.synchronize(dev)
+    mem_base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
     lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
@@ -487,6 +523,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if fa.device_status() != 0:
         raise RuntimeError("a kernel reported a bounded-wait timeout during warm-up")
+    peak_step_bytes = torch.cuda.max_memory_allocated(dev) - mem_base
 
     try:   # the UUID names this process's GPU whatever CUDA_VISIBLE_DEVICES says
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -566,11 +603,23 @@ def run_ours(args, rank, world, local_rank):
     else:
         achieved = work / (per[top][0] / 1e3) / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
+    traffic, tensor_active = profile_record(top, args.workload)
     roofline = {"bound": bound, "kernel": top, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": traffic_from_profiles(top, args.workload),
+                "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peaks['source']} (burst)",
                 "algorithmic_work_per_launch": work,
                 "avg_launch_ms": per[top][0]}
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    if bound == "tensor":
+        # the measured peak is cuBLAS at the clock it ran at (power-capped, below this
+        # run's); beside it, the fraction of the tensor pipes' rate at this run's median
+        # SM clock, and the tensor-pipe activity ncu recorded for this kernel
+        run_mhz = clocks["sm_mhz"] if clocks else None
+        roofline["ncu_tensor_active_pct"] = tensor_active
+        if run_mhz:
+            at_clock = tensor_rate_at_clock(sm_count, run_mhz)
+            roofline["tensor_rate_at_run_clock"] = at_clock
+            roofline["frac_of_tensor_rate_at_run_clock"] = achieved / at_clock
 
     e2e = None
     if not args.no_e2e:
@@ -631,6 +680,14 @@ def run_ours(args, rank, world, local_rank):
                "fwd_tflops": fwd_f / (fwd_ms / 1e3) / 1e12 if fwd_ms else None,
                "bwd_tflops": bwd_f / (bwd_ms / 1e3) / 1e12 if bwd_ms else None,
                "frac_of_peak": value / world / peaks["bf16_tflops"],
+               "frac_of_peak_basis": "measured cuBLAS bf16 burst rate (MEASURED_PEAKS.json "
+                                     "bf16_tflops) at the clock it ran at",
+               "frac_of_tensor_rate_at_run_clock": (
+                   value / world / tensor_rate_at_clock(sm_count, clocks["sm_mhz"])
+                   if clocks else None),
+               "memory": memory_report(
+                   lens if varlen else [N] * B, H, d, 2,
+                   torch.cuda.get_device_properties(dev).total_memory, peak_step_bytes),
                "kernels_ms": {kk: per[kk][0] for kk in per},
                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": launches, "clocks": clocks}

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
@@ -16,8 +17,6 @@ namespace {
 // Sticky status word written by kernels whose bounded wait ran out.
 __device__ uint32_t g_status_word;
 
-constexpr int kMaxDevices = 64;
-uint32_t* g_status_ptr[kMaxDevices] = {};
 unsigned long long g_wait_limit_ns = 2000000000ull;
 thread_local int g_last_cuda_error = 0;
 
@@ -26,19 +25,86 @@ fa_status cuda_fail(cudaError_t e) {
   return FA_ERR_CUDA;
 }
 
-// Device address of the status word on the current device (resolved once).
-fa_status status_ptr(uint32_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+// ---- device addresses of this library's file-scope __device__ variables
+// On the host a __device__ variable's name is only a stand-in; its device address
+// belongs to one CUDA context (the module is loaded anew into every context, and a
+// context that is destroyed and recreated, e.g. by cudaDeviceReset, may place it
+// elsewhere).  Addresses are therefore cached per context, keyed on the driver's
+// unique context ID (never reused within a process), and looked up again in a new
+// context.  One lock guards the table, so first calls from several host threads do
+// not race.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+fa_status driver_fn(const char* name, void** fn) {
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion(name, fn, 12000, cudaEnableDefault, &q);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
-  if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_status_word);
-    if (e != cudaSuccess) return cuda_fail(e);
-    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  if (q != cudaDriverEntryPointSuccess || !*fn) return cuda_fail(cudaErrorSymbolNotFound);
+  return FA_OK;
+}
+
+// ID of the context current on this thread (0: none yet).
+fa_status current_ctx_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  static fa_status init_st = FA_OK;
+  std::call_once(once, [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    init_st = driver_fn("cuCtxGetCurrent", &a);
+    if (init_st == FA_OK) init_st = driver_fn("cuCtxGetId", &b);
+    get_cur = reinterpret_cast<CtxGetCurrentFn>(a);
+    get_id = reinterpret_cast<CtxGetIdFn>(b);
+  });
+  if (init_st != FA_OK) return init_st;
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS) return cuda_fail(cudaErrorContextIsDestroyed);
+  *id = 0;
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return cuda_fail(cudaErrorContextIsDestroyed);
+  return FA_OK;
+}
+
+// Device address of the __device__ variable `sym` in the current context.
+fa_status symbol_address(const void* sym, void** out) {
+  struct Entry {
+    unsigned long long ctx;
+    const void* sym;
+    void* ptr;
+  };
+  constexpr int kEntries = 64;
+  static Entry table[kEntries] = {};
+  static int next = 0;
+  static std::mutex mu;
+  unsigned long long id = 0;
+  fa_status st = current_ctx_id(&id);
+  if (st != FA_OK) return st;
+  std::lock_guard<std::mutex> lock(mu);
+  if (id != 0)
+    for (const Entry& en : table)
+      if (en.ctx == id && en.sym == sym) {
+        *out = en.ptr;
+        return FA_OK;
+      }
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, sym);   // also creates the context if needed
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (id == 0 && (st = current_ctx_id(&id)) != FA_OK) return st;
+  if (id != 0) {
+    table[next] = {id, sym, p};
+    next = (next + 1) % kEntries;
   }
-  *out = g_status_ptr[dev];
+  *out = p;
+  return FA_OK;
+}
+
+// Device address of the status word in the current context.
+fa_status status_ptr(uint32_t** out) {
+  void* p = nullptr;
+  fa_status st = symbol_address(reinterpret_cast<const void*>(&g_status_word), &p);
+  if (st != FA_OK) return st;
+  *out = static_cast<uint32_t*>(p);
   return FA_OK;
 }
 
@@ -687,24 +753,16 @@ fa_status fa_decode_fp8(const void* Q, const void* Kc8, const void* Vc8, const i
 // workspace: every GPU that loads the library holds it until the process exits.
 static constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
-static float* g_noalloc_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device.  On the host the
-// array's name is only a stand-in, never a device address, so it is looked up
-// once per device, with that device current, and the looked-up pointer is what
-// the kernels receive.
+// Device address of the scratch array in the current context.  On the host the
+// array's name is only a stand-in, never a device address, so it is looked up in the
+// current context (once per context) and the looked-up pointer is what the kernels
+// receive.
 static fa_status noalloc_scratch(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e);
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  fa_status st = symbol_address(reinterpret_cast<const void*>(&g_noalloc_scratch), &p);
+  if (st != FA_OK) return st;
+  *out = static_cast<float*>(p);
   return FA_OK;
 }
 

@@ -275,11 +275,14 @@ fa_status fa_trace_read(int kind, double* total_ms, long long* launches);
  * scratch is a 16 MiB device array inside the library, held by every GPU that
  * loads the library until the process exits; sizes whose scratch need
  * (fa_bwd_workspace_size) exceeds 16 MiB are rejected with FA_ERR_UNSUPPORTED
- * before anything is launched.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current; make
- * that first call before any stream capture.  All calls share the one array and
- * it keeps the last call's contents: calls that overlap on the GPU (other
- * streams, other host threads) race on it, so serialise them.  Nothing in it
+ * before anything is launched.  The first call in a CUDA context looks up the
+ * array's device address there (cudaGetSymbolAddress, with the caller's device and
+ * context current; a context destroyed and recreated, e.g. by cudaDeviceReset, is
+ * looked up again); make that first call before any stream capture.  The lookup is
+ * guarded by a lock, so first calls from several host threads are safe.  All
+ * calls share the one array and it keeps the last call's contents: calls that
+ * overlap on the GPU (other streams, other host threads) race on it, so
+ * serialise them.  Nothing in it
  * needs to start at zero: each call writes every scratch value before reading
  * it.  Capacity: 8 bytes per row, B*H*ceil(N/128)*128 up to 2,097,152 rows. */
 fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,

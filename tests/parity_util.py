@@ -6,8 +6,9 @@ Tolerances (max over every compared element):
   dQ, dK, dV:   max|err| / max|ref| <= 1e-2 (fp16), 3e-2 (bf16)
 Two cases fall outside what those bounds were stated for:
   * Q, K ~ N(0, 4^2) (the stress inputs): rows are nearly one-hot, so |O| reaches
-    max|V| (about 4.5) and the 16-bit rounding of P and of O grows with it.  The O
-    bound is then multiplied by max(1, max|O_ref|).
+    max|V| (about 4.5) and the 16-bit rounding of P and of O grows with it.  O is then
+    checked element by element against a bound derived from the kernel's arithmetic
+    (``o_bound_elementwise``) instead of the constant stated for N(0,1) inputs.
   * N = 1: one key gives P = 1 and dS = dP - D = 0, so the reference dQ and dK are
     identically zero and the relative error is undefined.  Where max|ref| is below
     1e-6 of the size of a single term scale * |dP| * |k| (exact cancellation), the
@@ -49,6 +50,59 @@ def _sel(t: torch.Tensor, heads):
     return flat[list(heads)].unsqueeze(0)
 
 
+def allowed_keys(N: int, causal: bool, window: int = 0) -> np.ndarray:
+    """(N, N) boolean: query i may attend to key j."""
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    ok = np.ones((N, N), dtype=bool)
+    if causal:
+        ok &= j <= i
+    if window:
+        ok &= i - j < window
+    return ok
+
+
+def o_bound_elementwise(q, k, v, o_ref, l_ref, causal, scale, dtype, window=0):
+    """Bound on |O_gpu - O_ref| for every element, from the arithmetic the forward
+    kernel does (reading of the pages: fp32 scores and accumulation, P rounded to the
+    16-bit input type before P.V, O rounded to it at the end; the pages fix none of
+    this).  Arrays are (1, heads, N, d) fp64; l_ref is the natural-log L.
+
+    With P_ij = exp(S_ij - L_i) the exact probabilities, A_ic = sum_j P_ij |v_jc|,
+    u the unit round-off of the 16-bit type (2^-11 fp16, 2^-8 bf16) and n the keys
+    of the row:
+      output rounding              u |O_ic|            (+ 2^-25 below fp16's normals)
+      P rounded to 16 bits         u A_ic              (+ 2^-25 sum_j |v_jc| max_j P_ij
+                                                         for fp16 subnormal p)
+      a score off by dx_j (natural log units) moves O_ic by at most
+                                   max_j |dx_j| (A_ic + |O_ic|)
+        fp32 dot product over d:   dx_j <= d 2^-24 scale sum_k |q_ik k_jk|
+        ex2.approx and the fp32 exponent argument: 2^-21
+      fp32 sums of l and of P.V over n keys and the alpha rescales:
+                                   (n + d) 2^-23 (A_ic + |O_ic|)
+    """
+    fp16 = dtype == "fp16"
+    u = 2.0 ** -11 if fp16 else 2.0 ** -8
+    sub = 2.0 ** -25 if fp16 else 0.0
+    _, nh, N, d = q.shape
+    ok = allowed_keys(N, causal, window)
+    n_keys = ok.sum(axis=1)[:, None].astype(np.float64)
+    out = np.empty_like(o_ref)
+    for h in range(nh):
+        qh, kh, vh = q[0, h], k[0, h], v[0, h]
+        S = scale * (qh @ kh.T)
+        P = np.where(ok, np.exp(np.where(ok, S, 0.0) - l_ref[0, h][:, None]), 0.0)
+        A = P @ np.abs(vh)
+        O = np.abs(o_ref[0, h])
+        dS = d * 2.0 ** -24 * scale * (np.abs(qh) @ np.abs(kh).T)
+        dx = np.max(np.where(ok, dS, 0.0), axis=1)[:, None] + 2.0 ** -21
+        b = u * O + sub + u * A + dx * (A + O) + (n_keys + d) * 2.0 ** -23 * (A + O)
+        if fp16:
+            b += sub * (ok.astype(np.float64) @ np.abs(vh)) * np.max(P, axis=1)[:, None]
+        out[0, h] = b
+    return out
+
+
 def compare(B, H, N, d, dtype, causal, qk_std=1.0, heads=None, seed=0, scale=None, Hkv=None,
             window=0):
     """Run the CUDA path on the whole problem and the oracle on ``heads`` (flat b*H+h
@@ -88,9 +142,16 @@ def compare(B, H, N, d, dtype, causal, qk_std=1.0, heads=None, seed=0, scale=Non
             mref = float(np.max(np.abs(ref)))
             err /= mref if mref >= 1e-6 * term else term
         rep[name] = err
-    o_scale = 1.0 if qk_std == 1.0 else max(1.0, float(np.max(np.abs(o_ref))))
-    rep["o_bound"] = TOL_O[dtype] * o_scale
-    assert rep["o"] <= rep["o_bound"], rep
+    if qk_std == 1.0:
+        rep["o_bound"] = TOL_O[dtype]
+        assert rep["o"] <= rep["o_bound"], rep
+    else:
+        assert Hkv is None, "the element-wise O bound is written for H == Hkv"
+        got = _sel(g["o"], qheads).double().numpy().reshape(o_ref.shape)
+        bound = o_bound_elementwise(q, k, v, o_ref, l_ref, causal, scale, dtype, window)
+        ratio = np.abs(got - o_ref) / (1.25 * bound + 1e-6)
+        rep["o_vs_bound"] = float(np.max(ratio))
+        assert rep["o_vs_bound"] <= 1.0, rep
     assert rep["lse"] <= TOL_L, rep
     for n in ("dq", "dk", "dv"):
         assert rep[n] <= TOL_G[dtype], rep

@@ -85,3 +85,41 @@ def test_emit_prints_one_line_and_writes_it_with_json_out(tmp_path, capsys):
     bench.emit(out, bench.parse(["--json-out", str(path)]))
     printed = capsys.readouterr().out.strip()
     assert path.read_text().strip() == printed
+
+
+def test_memory_report_matches_the_pages_sizes():
+    # one head at 8K fp16: the 128 MiB score matrix the docs page prints (Fig. 2 and the
+    # hero panel), against Q, K, V, O and L of that head
+    r = bench.memory_report([8192], 1, 128, 2, 280 << 30, 0)
+    assert r["score_matrix_bytes"] == 128 << 20
+    assert r["linear_footprint_bytes"] == 4 * 8192 * 128 * 2 + 4 * 8192
+    assert abs(r["score_over_linear"] - (128 << 20) / (8 << 20 | 32768)) < 1e-9
+    # the score matrix alone fills the device at the N where B*H*N^2*2 reaches its size
+    n = r["ordinary_attention_runs_out_at_N"]
+    assert n * n * 2 <= 280 << 30 < (n + 1) * (n + 1) * 2
+    # packed sequences add their own squares
+    r2 = bench.memory_report([100, 300], 4, 64, 2, 1 << 30, 7)
+    assert r2["score_matrix_bytes"] == 4 * 2 * (100 ** 2 + 300 ** 2)
+    assert r2["peak_device_bytes_step"] == 7
+
+
+def test_tensor_rate_at_clock():
+    # 8192 FLOP per clock per SM: 152 SMs at 1807 MHz give the nominal 2.25 PFLOP/s
+    assert abs(bench.tensor_rate_at_clock(152, 1807.0) - 2250.0) < 1.0
+    assert bench.tensor_rate_at_clock(152, 1807.0, bits=8) == 2 * bench.tensor_rate_at_clock(152, 1807.0)
+
+
+def test_profile_record_reads_tensor_activity(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_text("kernel source")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "fwd_kernel__w.txt").write_text(
+        f"source_sha256: {sha}\ndram_bytes_per_launch: 1234\n"
+        "tensor pipeline (sm__pipe_tensor_cycles_active, elapsed)      66.2 %\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setitem(bench.KERNEL_SOURCES, "fwd_kernel", "k.cu")
+    assert bench.profile_record("fwd_kernel", "w") == (1234.0, 66.2)
+    src.write_text("changed")
+    assert bench.profile_record("fwd_kernel", "w") == (None, None)
