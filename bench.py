@@ -542,26 +542,36 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.2)
     barrier()
     torch.cuda.synchronize()
+
+    def timed_steps():
+        if flush is None:
+            # one event per step boundary: back-to-back steps, per-step times for the median
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+            evs[0].record(stream)
+            for i in range(args.steps):
+                step()
+                evs[i + 1].record(stream)
+            sp = list(zip(evs[:-1], evs[1:]))
+        else:
+            sp = []
+            for _ in range(args.steps):
+                flush.zero_()
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(stream)
+                step()
+                t1.record(stream)
+                sp.append((t0, t1))
+        torch.cuda.synchronize()
+        barrier()
+        return sp
+
+    # The step time comes from a pass without per-kernel events: an event recorded
+    # between two kernels stops the second from starting while the first drains (the
+    # kernels are launched as programmatic dependents).  A second pass of the same
+    # steps records an event pair around every kernel for the per-kernel times.
+    spans = timed_steps()
     fa.trace_enable(True)
-    if flush is None:
-        # one event per step boundary: back-to-back steps, per-step times for the median
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-        evs[0].record(stream)
-        for i in range(args.steps):
-            step()
-            evs[i + 1].record(stream)
-        spans = list(zip(evs[:-1], evs[1:]))
-    else:
-        spans = []
-        for _ in range(args.steps):
-            flush.zero_()
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0.record(stream)
-            step()
-            t1.record(stream)
-            spans.append((t0, t1))
-    torch.cuda.synchronize()
-    barrier()
+    timed_steps()
     fa.trace_enable(False)
     clocks = sampler.stop()
     if fa.device_status() != 0:
@@ -805,14 +815,22 @@ def run_decode(args, rank, world, local_rank):
     time.sleep(0.2)
     barrier()
     torch.cuda.synchronize()
+
+    def timed_steps():
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return t0, t1
+
+    # step time without per-kernel events (they would stand between the split kernel and
+    # the merge kernel, its programmatic dependent); per-kernel times from a second pass
+    t0, t1 = timed_steps()
     fa.trace_enable(True)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
+    timed_steps()
     fa.trace_enable(False)
     clocks = sampler.stop()
     if fa.device_status() != 0:

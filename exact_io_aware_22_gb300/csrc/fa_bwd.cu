@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(256) pre_kernel(const void* __restrict__ O,
                                                   const int* __restrict__ cu_seqlens, int H,
                                                   int total) {
   constexpr int TPR = D / 8;   // threads per row, 16 bytes each
+  grid_dep_launch();
+  grid_dep_wait();             // O and L come from the forward
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long rp = gt / TPR;
   const int part = static_cast<int>(gt % TPR);
@@ -87,10 +89,11 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     trace_begin(TR_BWD_PRE, st);
-    pre_kernel<D, BF16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        a.O, a.dO, a.L, a.Dvec, Lp, a.N, Np, rows_p, a.cu_seqlens, a.H, a.total);
+    cudaError_t e = launch_dependent(pre_kernel<D, BF16>, static_cast<unsigned>(blocks), 256, 0,
+                                     st, a.O, a.dO, a.L, a.Dvec, Lp, a.N, Np, rows_p,
+                                     a.cu_seqlens, a.H, a.total);
     trace_end(TR_BWD_PRE, st);
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   // dK/dV and dQ: the TMEM-resident kernels of fa_bwd128.cu

@@ -161,10 +161,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int SLOT_OFF = SM::SLOT_OFF;
   extern __shared__ __align__(1024) uint8_t sg[];
   const uint32_t sb = smem_u32(sg);
+  grid_dep_launch();
   if (sb & 1023u) {                                // see FA_DEV_SMEM_ALIGN
+    grid_dep_wait();
     if (threadIdx.x == 0) atomicOr(ctl.status, FA_DEV_SMEM_ALIGN);
     return;
   }
+  if (cu_seqlens) grid_dep_wait();                 // the offsets may come from earlier work
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + BT - 1) / BT;
   const BlockPos bp = block_pos(nkb);
@@ -207,6 +210,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sg + SLOT_OFF);
+  grid_dep_wait();                                 // D and L*log2e from the pre-pass
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -500,10 +504,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int SLOT_OFF = SM::SLOT_OFF;
   extern __shared__ __align__(1024) uint8_t sg[];
   const uint32_t sb = smem_u32(sg);
+  grid_dep_launch();
   if (sb & 1023u) {                                // see FA_DEV_SMEM_ALIGN
+    grid_dep_wait();
     if (threadIdx.x == 0) atomicOr(ctl.status, FA_DEV_SMEM_ALIGN);
     return;
   }
+  if constexpr (PACKED) grid_dep_wait();           // the offsets may come from earlier work
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = Np / BT;
   const BlockPos bp = block_pos(nqb);
@@ -544,6 +551,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sg + SLOT_OFF);
+  grid_dep_wait();                                 // D and L*log2e from the pre-pass
 
   if (warp == 0) {
     regs_dec<kRegsLow>();                          // warpgroup 0 (TMA, MMA issue): few registers
@@ -772,14 +780,15 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
   {
     auto kern = dkdv128_kernel<HD, BF16, CAUSAL>;
     constexpr int smem = kv::Smem<HD>::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DKDV, st);
-    kern<<<static_cast<unsigned>(nblk_kv), THREADS, smem, st>>>(
-        a.tmQ, a.tmK, a.tmV, a.tmdO, a.Dvec, Lp, a.dK, a.dV, a.N, Np, a.group, a.window,
-        a.cu_seqlens, a.H, a.total, a.scale, a.c_log2, a.ctl);
+    e = launch_dependent(kern, static_cast<unsigned>(nblk_kv), THREADS, smem, st, a.tmQ, a.tmK,
+                         a.tmV, a.tmdO, static_cast<const float*>(a.Dvec), Lp, a.dK, a.dV, a.N,
+                         Np, a.group, a.window, a.cu_seqlens, a.H, a.total, a.scale, a.c_log2,
+                         a.ctl);
     trace_end(TR_BWD_DKDV, st);
-    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   {
@@ -792,14 +801,14 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
     constexpr int smem = qd::Smem<HD>::SMEM_BYTES;
     cudaError_t e = check_split_regs(reinterpret_cast<const void*>(kern));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     trace_begin(TR_BWD_DQ, st);
-    kern<<<static_cast<unsigned>(nblk), THREADS, smem, st>>>(
-        a.tmK, a.tmV, a.tmdO, a.Q, a.Dvec, Lp, a.dQ, a.N, Np, a.group, a.window, a.cu_seqlens,
-        a.H, a.total, a.scale, a.c_log2, a.ctl);
+    e = launch_dependent(kern, static_cast<unsigned>(nblk), THREADS, smem, st, a.tmK, a.tmV,
+                         a.tmdO, a.Q, static_cast<const float*>(a.Dvec), Lp, a.dQ, a.N, Np,
+                         a.group, a.window, a.cu_seqlens, a.H, a.total, a.scale, a.c_log2, a.ctl);
     trace_end(TR_BWD_DQ, st);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
   }
 }
 

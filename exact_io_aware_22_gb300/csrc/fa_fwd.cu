@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* sg = smem_raw + (sb - raw);
 
+  grid_dep_launch();                            // the next kernel may start setting up
+  if constexpr (PACKED) grid_dep_wait();        // the offsets may come from earlier work
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BlockPos bp = block_pos(n_qblk);
   const int bh = bp.bh;
@@ -139,6 +141,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sg + C::SLOT_OFF);
+  grid_dep_wait();                              // inputs written, outputs free to overwrite
 
   if (warp == 0) {
     regs_dec<kRegsLow>();                          // warpgroup 0 (TMA, MMA issue): few registers
@@ -393,17 +396,17 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   auto kern = fwd_kernel<D, BF16, CAUSAL, WINDOW, PACKED>;
   cudaError_t e = check_split_regs(reinterpret_cast<const void*>(kern));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  e = ensure_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int n_qblk = (a.N + NT * BM - 1) / (NT * BM);
   const long long grid = static_cast<long long>(n_qblk) * a.BH;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   trace_begin(TR_FWD, st);
-  kern<<<static_cast<unsigned>(grid), THREADS, C::SMEM_BYTES, st>>>(
-      a.tmQ, a.tmK, a.tmV, a.O, a.L, a.N, n_qblk, a.group, a.window, a.cu_seqlens, a.H, a.total,
-      a.c_log2, a.ctl);
+  e = launch_dependent(kern, static_cast<unsigned>(grid), THREADS, C::SMEM_BYTES, st, a.tmQ,
+                       a.tmK, a.tmV, a.O, a.L, a.N, n_qblk, a.group, a.window, a.cu_seqlens, a.H,
+                       a.total, a.c_log2, a.ctl);
   trace_end(TR_FWD, st);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

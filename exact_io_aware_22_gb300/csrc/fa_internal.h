@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "fa_ptx.cuh"
 
@@ -25,6 +26,42 @@ enum TraceKind {
 // Record an event before / after one kernel launch on `st` (no-op unless tracing).
 void trace_begin(int kind, cudaStream_t st);
 void trace_end(int kind, cudaStream_t st);
+
+// Launch `kern` with programmatic stream serialisation: its CTAs may be scheduled
+// while the previous kernel in `st` finishes its last wave, so launch latency and the
+// kernel's set-up overlap that kernel's tail.  The kernel must call grid_dep_wait()
+// before its first access to global memory that earlier work in the stream writes or
+// reads (fa_ptx.cuh).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block,
+                                    size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes`, once per kernel (later
+// calls only look it up; launches from several host threads share the record).
+inline cudaError_t ensure_smem(const void* kern, int bytes) {
+  static std::mutex mu;
+  static const void* seen[512];
+  static int n_seen = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_seen; ++i)
+    if (seen[i] == kern) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && n_seen < 512) seen[n_seen++] = kern;
+  return e;
+}
 
 // TMA box of one 128-row tile: box_cols elements (one swizzle width) per row.
 struct FwdTileInfo {

@@ -135,6 +135,19 @@ inline cudaError_t check_split_regs(const void* kern) {
   return cudaSuccess;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation (launch_dependent in fa_internal.h) may start while the kernel before
+// it in the stream is still running: it sets up (barriers, TMEM) and then waits in
+// grid_dep_wait() until that kernel has completed and its writes are visible, before
+// touching any global memory that earlier work writes or reads.  grid_dep_launch()
+// lets the next kernel in the stream start once every CTA of this grid has called it
+// (or exited); it promises nothing about this grid's writes.  Both are no-ops for a
+// kernel launched without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier among a subset of warps (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
