@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfa_gb300.so")
-UNITS = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd128.cu", "fa_decode.cu", "fa_fwd8.cu"]
+UNITS = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd128.cu", "fa_bwd64.cu", "fa_decode.cu",
+         "fa_fwd8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v", "-I", os.path.join(ROOT, "include")]

@@ -96,8 +96,11 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // dK/dV and dQ: the TMEM-resident kernels of fa_bwd128.cu
-  return launch_bwd128(a, D, BF16, CAUSAL, st);
+  // dK/dV: the persistent kernel of fa_bwd64.cu at d <= 64, else fa_bwd128.cu's; dQ
+  cudaError_t e = D <= 64 ? launch_dkdv64(a, D, BF16, CAUSAL, st)
+                          : launch_dkdv128(a, D, BF16, CAUSAL, st);
+  if (e != cudaSuccess) return e;
+  return launch_dq128(a, D, BF16, CAUSAL, st);
 }
 
 }  // namespace

@@ -45,6 +45,7 @@
 //   warps 4-11   two compute warpgroups, one thread per TMEM lane (a key row
 //                in dkdv, a query row in dq), 64 columns each; in the epilogue
 //                warpgroup h stores head-dim columns [64h, 64h + 64).
+#include "fa_bwd_tiles.cuh"
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -54,49 +55,11 @@ namespace fa {
 
 namespace {
 
-constexpr int BT = 128;          // rows of every tile (keys or queries)
+using bwdt::BT;
+using bwdt::Geo;
+using bwdt::bulk_load;
+using bwdt::issue_ab_t_w;
 constexpr int THREADS = 384;
-
-// Shared-memory geometry of a 128-row tile of head dim HD as TMA writes it: chunks of
-// SPAN columns (64, or all 32 at HD = 32) side by side, each in the 128-byte swizzle
-// (64-byte at HD = 32), so that UMMA reads it as a K-major operand (k-steps of 16
-// columns) or as an MN-major one (k-steps of 16 rows).
-template <int HD>
-struct Geo {
-  static constexpr int SPAN = HD < 64 ? HD : 64;             // columns per chunk
-  static constexpr int NCH = HD / SPAN;                      // chunks per tile
-  static constexpr int ROWB = SPAN * 2;                      // bytes per chunk row
-  static constexpr int CHUNK = BT * ROWB;                    // bytes per chunk
-  static constexpr int KPC = SPAN / 16;                      // K-major k-steps per chunk
-  static constexpr uint32_t HI = sdesc_hi(8 * ROWB, ROWB == 128 ? UMMA_SW128 : UMMA_SW64);
-  static constexpr int KSTEP_MN = 16 * ROWB;                 // MN-major k-step: 16 rows
-  // byte offset of K-major k-step kk
-  static constexpr uint32_t koff(int kk) { return (kk / KPC) * CHUNK + (kk % KPC) * 32; }
-};
-
-// 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// X^T = A B^T over the head dim HD into TMEM columns d_tmem: A and B are 128-row
-// K-major tiles (HD/64 chunks of 64 columns each), given by their descriptor low
-// words (sdesc_lo with LBO 16).
-template <int HD>
-__device__ __forceinline__ void issue_ab_t_w(uint32_t d_tmem, uint32_t alo, uint32_t blo,
-                                             uint32_t idesc) {
-  using G = Geo<HD>;
-#pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t o = G::koff(kk) >> 4;
-    umma_ss_w(d_tmem, alo + o, blo + o, G::HI, idesc, kk > 0);
-  }
-}
 
 // Epilogue: NC (32 or 64) fp32 TMEM columns of this thread's lane, times mul,
 // rounded to the 16-bit type and stored as one contiguous run of 2 NC bytes (when
@@ -772,59 +735,68 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int HD, bool BF16, bool CAUSAL>
-cudaError_t launch_t(const BwdArgs& a, cudaStream_t st) {
+cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t st) {
   const int Np = (a.N + 127) / 128 * 128;
   const float* Lp = a.Dvec + static_cast<size_t>(a.BH) * Np;
-  const long long nblk = static_cast<long long>(Np / BT) * a.BH;           // dQ: per query head
   const long long nblk_kv = static_cast<long long>(Np / BT) * (a.BH / a.group);   // per K/V head
-  {
-    auto kern = dkdv128_kernel<HD, BF16, CAUSAL>;
-    constexpr int smem = kv::Smem<HD>::SMEM_BYTES;
-    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
-    if (e != cudaSuccess) return e;
-    trace_begin(TR_BWD_DKDV, st);
-    e = launch_dependent(kern, static_cast<unsigned>(nblk_kv), THREADS, smem, st, a.tmQ, a.tmK,
-                         a.tmV, a.tmdO, static_cast<const float*>(a.Dvec), Lp, a.dK, a.dV, a.N,
-                         Np, a.group, a.window, a.cu_seqlens, a.H, a.total, a.scale, a.c_log2,
-                         a.ctl);
-    trace_end(TR_BWD_DKDV, st);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  {
-    // windowed and packed-sequence dQ kernels are separate instantiations
-    auto kern = CAUSAL && a.window > 0
-        ? (a.cu_seqlens ? dq128_kernel<HD, BF16, CAUSAL, CAUSAL, true>
-                        : dq128_kernel<HD, BF16, CAUSAL, CAUSAL, false>)
-        : (a.cu_seqlens ? dq128_kernel<HD, BF16, CAUSAL, false, true>
-                        : dq128_kernel<HD, BF16, CAUSAL, false, false>);
-    constexpr int smem = qd::Smem<HD>::SMEM_BYTES;
-    cudaError_t e = check_split_regs(reinterpret_cast<const void*>(kern));
-    if (e != cudaSuccess) return e;
-    e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
-    if (e != cudaSuccess) return e;
-    trace_begin(TR_BWD_DQ, st);
-    e = launch_dependent(kern, static_cast<unsigned>(nblk), THREADS, smem, st, a.tmK, a.tmV,
-                         a.tmdO, a.Q, static_cast<const float*>(a.Dvec), Lp, a.dQ, a.N, Np,
-                         a.group, a.window, a.cu_seqlens, a.H, a.total, a.scale, a.c_log2, a.ctl);
-    trace_end(TR_BWD_DQ, st);
-    return e != cudaSuccess ? e : cudaGetLastError();
-  }
+  auto kern = dkdv128_kernel<HD, BF16, CAUSAL>;
+  constexpr int smem = kv::Smem<HD>::SMEM_BYTES;
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  trace_begin(TR_BWD_DKDV, st);
+  e = launch_dependent(kern, static_cast<unsigned>(nblk_kv), THREADS, smem, st, a.tmQ, a.tmK,
+                       a.tmV, a.tmdO, static_cast<const float*>(a.Dvec), Lp, a.dK, a.dV, a.N,
+                       Np, a.group, a.window, a.cu_seqlens, a.H, a.total, a.scale, a.c_log2,
+                       a.ctl);
+  trace_end(TR_BWD_DKDV, st);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int HD, bool BF16, bool CAUSAL>
+cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t st) {
+  const int Np = (a.N + 127) / 128 * 128;
+  const float* Lp = a.Dvec + static_cast<size_t>(a.BH) * Np;
+  const long long nblk = static_cast<long long>(Np / BT) * a.BH;           // per query head
+  // windowed and packed-sequence dQ kernels are separate instantiations
+  auto kern = CAUSAL && a.window > 0
+      ? (a.cu_seqlens ? dq128_kernel<HD, BF16, CAUSAL, CAUSAL, true>
+                      : dq128_kernel<HD, BF16, CAUSAL, CAUSAL, false>)
+      : (a.cu_seqlens ? dq128_kernel<HD, BF16, CAUSAL, false, true>
+                      : dq128_kernel<HD, BF16, CAUSAL, false, false>);
+  constexpr int smem = qd::Smem<HD>::SMEM_BYTES;
+  cudaError_t e = check_split_regs(reinterpret_cast<const void*>(kern));
+  if (e != cudaSuccess) return e;
+  e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  trace_begin(TR_BWD_DQ, st);
+  e = launch_dependent(kern, static_cast<unsigned>(nblk), THREADS, smem, st, a.tmK, a.tmV,
+                       a.tmdO, a.Q, static_cast<const float*>(a.Dvec), Lp, a.dQ, a.N, Np,
+                       a.group, a.window, a.cu_seqlens, a.H, a.total, a.scale, a.c_log2, a.ctl);
+  trace_end(TR_BWD_DQ, st);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
-  if (d == 32) {
-    if (bf16) return causal ? launch_t<32, true, true>(a, st) : launch_t<32, true, false>(a, st);
-    return causal ? launch_t<32, false, true>(a, st) : launch_t<32, false, false>(a, st);
-  }
-  if (d == 64) {
-    if (bf16) return causal ? launch_t<64, true, true>(a, st) : launch_t<64, true, false>(a, st);
-    return causal ? launch_t<64, false, true>(a, st) : launch_t<64, false, false>(a, st);
-  }
-  if (bf16) return causal ? launch_t<128, true, true>(a, st) : launch_t<128, true, false>(a, st);
-  return causal ? launch_t<128, false, true>(a, st) : launch_t<128, false, false>(a, st);
+#define FA_BWD_DISPATCH(FN)                                                              \
+  if (d == 32) {                                                                         \
+    if (bf16) return causal ? FN<32, true, true>(a, st) : FN<32, true, false>(a, st);    \
+    return causal ? FN<32, false, true>(a, st) : FN<32, false, false>(a, st);            \
+  }                                                                                      \
+  if (d == 64) {                                                                         \
+    if (bf16) return causal ? FN<64, true, true>(a, st) : FN<64, true, false>(a, st);    \
+    return causal ? FN<64, false, true>(a, st) : FN<64, false, false>(a, st);            \
+  }                                                                                      \
+  if (bf16) return causal ? FN<128, true, true>(a, st) : FN<128, true, false>(a, st);    \
+  return causal ? FN<128, false, true>(a, st) : FN<128, false, false>(a, st);
+
+cudaError_t launch_dkdv128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
+  FA_BWD_DISPATCH(launch_dkdv_t)
 }
+
+cudaError_t launch_dq128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
+  FA_BWD_DISPATCH(launch_dq_t)
+}
+#undef FA_BWD_DISPATCH
 
 }  // namespace fa

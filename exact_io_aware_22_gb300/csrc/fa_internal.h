@@ -48,6 +48,17 @@ inline cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsig
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Heads per ordering group (block_pos) of a persistent kernel whose work items stream
+// `bytes_per_head` bytes of one head's tiles: all heads (the whole grid longest-first)
+// when they fit in about half of L2 together, else as many as do, at least 8.
+inline int order_group(long long heads, long long bytes_per_head) {
+  const long long budget = 64ll << 20;
+  long long g = bytes_per_head > 0 ? budget / bytes_per_head : heads;
+  if (g < 8) g = 8;
+  if (g > heads) g = heads;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
 // Raise a kernel's dynamic shared-memory limit to `bytes`, once per kernel (later
 // calls only look it up; launches from several host threads share the record).
 inline cudaError_t ensure_smem(const void* kern, int bytes) {
@@ -107,7 +118,11 @@ struct BwdArgs {
   KernelCtl ctl;
 };
 cudaError_t launch_bwd(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
-cudaError_t launch_bwd128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
+// dK/dV and dQ kernels after the pre-pass: the TMEM-resident kernels of fa_bwd128.cu
+// (every head dim) and the persistent ones of fa_bwd64.cu (head dims 32 and 64)
+cudaError_t launch_dkdv128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
+cudaError_t launch_dq128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
+cudaError_t launch_dkdv64(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
 // Workspace: D and L*log2(e) per padded row.
 size_t bwd_workspace_bytes(long long BH, int N, int d);
 

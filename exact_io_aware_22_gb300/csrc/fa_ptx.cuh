@@ -117,10 +117,11 @@ constexpr uint32_t kRegsLaunch = 168, kRegsLow = 88, kRegsHigh = 208;
 static_assert(128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch,
               "register split must use exactly the launch allocation");
 // Host check before launching a kernel that splits its registers: it must have been
-// compiled to exactly kRegsLaunch registers per thread, or the split would not add up
-// (an inc would wait for registers that no warpgroup gives back).  Results are kept
-// per kernel; launches from several host threads share the record under a lock.
-inline cudaError_t check_split_regs(const void* kern) {
+// compiled to exactly `launch_regs` registers per thread (kRegsLaunch unless the kernel
+// states its own), or the split would not add up (an inc would wait for registers that
+// no warpgroup gives back).  Results are kept per kernel; launches from several host
+// threads share the record under a lock.
+inline cudaError_t check_split_regs(const void* kern, int launch_regs = kRegsLaunch) {
   static std::mutex mu;
   static const void* seen[256];
   static int n_seen = 0;
@@ -130,7 +131,7 @@ inline cudaError_t check_split_regs(const void* kern) {
   cudaFuncAttributes fa;
   const cudaError_t e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorInvalidConfiguration;
+  if (fa.numRegs != launch_regs) return cudaErrorInvalidConfiguration;
   if (n_seen < 256) seen[n_seen++] = kern;
   return cudaSuccess;
 }
@@ -146,6 +147,34 @@ inline cudaError_t check_split_regs(const void* kern) {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Cluster launch control (dynamic tile scheduling for persistent CTAs).  A running
+// CTA asks the hardware to cancel the launch of a CTA that has not started yet and
+// takes over its work: try_cancel writes a 16-byte response to shared memory and
+// completes 16 transaction bytes on `bar` (the caller has armed it with
+// mbar_arrive_expect_tx(bar, 16)); clc_result reads the response and returns the
+// x index of the cancelled CTA, or -1 when none was left to cancel.  Once a request
+// has come back empty no further request may be made.  The hardware launches (and
+// so cancels) CTAs in index order, so a grid ordered longest-first stays so.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp_smem, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(resp_smem),
+      "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ int clc_result(uint32_t resp_smem) {
+  uint32_t x, ok;
+  asm volatile(
+      "{\n\t.reg .b128 resp;\n\t.reg .pred p;\n\tld.shared.b128 resp, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, resp;\n\t"
+      "selp.u32 %1, 1, 0, p;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, resp;\n\t}"
+      : "=r"(x), "=r"(ok)
+      : "r"(resp_smem)
+      : "memory");
+  return ok ? static_cast<int>(x) : -1;
 }
 
 // Named barrier among a subset of warps (ids 1..15; 0 is __syncthreads).
@@ -353,16 +382,17 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool bf16, b
 
 // ---------------------------------------------------------------- block order
 // Which (batch*head, tile rank) a CTA of a grid of nblk tiles per head takes.
-// Heads go in groups of 8; inside a group every head's rank-0 tile comes first,
-// then every head's rank-1 tile, and so on.  Rank 0 is the tile with the most
-// work under the causal mask, so the grid runs close to longest-first (the short
-// tiles fill the tail), while the CTAs running at one time stream the K/V or
-// Q/dO of at most a few heads, which stay in L2.
+// Heads go in groups of G (8 unless the caller chooses); inside a group every head's
+// rank-0 tile comes first, then every head's rank-1 tile, and so on.  Rank 0 is the
+// tile with the most work under the causal mask, so the grid runs close to
+// longest-first (the short tiles fill the tail), while the CTAs running at one time
+// stream the K/V or Q/dO of at most a few heads, which stay in L2.  A G as large as
+// the head count orders the whole grid longest-first, which the persistent kernels
+// take when every head's streamed tiles fit in L2 together.
 struct BlockPos {
   int bh, rank;
 };
-__device__ __forceinline__ BlockPos block_pos(int nblk, int bid) {
-  constexpr int G = 8;
+__device__ __forceinline__ BlockPos block_pos(int nblk, int bid, int G = 8) {
   const int BH = static_cast<int>(gridDim.x) / nblk;
   const int g0 = bid / (G * nblk) * G;
   const int gsz = min(G, BH - g0);
@@ -453,6 +483,23 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// Maximum of a row of 128 fp32 values held as bits, as a tree of 3-input maxima
+// (depth 5), so the 64 max operations do not form a few long dependent chains.
+__device__ __forceinline__ float row_max128(const uint32_t (&s)[128]) {
+  float a[43], b[15], c[5];
+#pragma unroll
+  for (int i = 0; i < 42; ++i)
+    a[i] = fmax3(__uint_as_float(s[3 * i]), __uint_as_float(s[3 * i + 1]),
+                 __uint_as_float(s[3 * i + 2]));
+  a[42] = fmaxf(__uint_as_float(s[126]), __uint_as_float(s[127]));
+#pragma unroll
+  for (int i = 0; i < 14; ++i) b[i] = fmax3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  b[14] = a[42];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) c[i] = fmax3(b[3 * i], b[3 * i + 1], b[3 * i + 2]);
+  return fmaxf(fmax3(c[0], c[1], c[2]), fmaxf(c[3], c[4]));
 }
 
 template <bool BF16>
