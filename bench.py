@@ -125,6 +125,11 @@ def workload(name):
             (w[7] if len(w) > 7 else 0))
 DEFAULT_WORKLOAD = "n8k_causal_d128_bf16"
 L2_BYTES = 129 * 1000 * 1000        # GB300 L2 (126 MiB)
+# at head dims 32 and 64 the backward runs the persistent kernels of fa_bwd64.cu
+SMALL_D_SOURCES = {
+    "bwd_dkdv_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd64.cu",
+    "bwd_dq_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd64.cu",
+}
 KERNEL_SOURCES = {
     "fwd_kernel": "exact_io_aware_22_gb300/csrc/fa_fwd.cu",
     "bwd_pre_kernel": "exact_io_aware_22_gb300/csrc/fa_bwd.cu",
@@ -291,12 +296,19 @@ def load_peaks():
             "source": "fallback"}
 
 
+def kernel_source(kernel: str, workload: str) -> str:
+    """Source file of the kernel that the trace kind `kernel` times on `workload`."""
+    if workload in WORKLOADS and WORKLOADS[workload][3] <= 64 and kernel in SMALL_D_SOURCES:
+        return SMALL_D_SOURCES[kernel]
+    return KERNEL_SOURCES[kernel]
+
+
 def profile_record(kernel: str, workload: str):
     """(dram bytes per launch, tensor-pipe active % of elapsed cycles) recorded by ncu in
     profiles/<kernel>__<workload>.txt; (None, None) when the file is missing or the
     kernel's source changed since the capture, and None for a figure it lacks."""
     path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.txt")
-    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
+    src = os.path.join(ROOT, kernel_source(kernel, workload))
     if not os.path.exists(path) or not os.path.exists(src):
         return None, None
     text = open(path).read()

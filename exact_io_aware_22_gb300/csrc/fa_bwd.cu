@@ -96,11 +96,11 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st) {
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // dK/dV: the persistent kernel of fa_bwd64.cu at d <= 64, else fa_bwd128.cu's; dQ
+  // dK/dV and dQ: the persistent kernels of fa_bwd64.cu at d <= 64, else fa_bwd128.cu's
   cudaError_t e = D <= 64 ? launch_dkdv64(a, D, BF16, CAUSAL, st)
                           : launch_dkdv128(a, D, BF16, CAUSAL, st);
   if (e != cudaSuccess) return e;
-  return launch_dq128(a, D, BF16, CAUSAL, st);
+  return D <= 64 ? launch_dq64(a, D, BF16, CAUSAL, st) : launch_dq128(a, D, BF16, CAUSAL, st);
 }
 
 }  // namespace

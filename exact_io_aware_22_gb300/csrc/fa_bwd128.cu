@@ -778,25 +778,18 @@ cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-#define FA_BWD_DISPATCH(FN)                                                              \
-  if (d == 32) {                                                                         \
-    if (bf16) return causal ? FN<32, true, true>(a, st) : FN<32, true, false>(a, st);    \
-    return causal ? FN<32, false, true>(a, st) : FN<32, false, false>(a, st);            \
-  }                                                                                      \
-  if (d == 64) {                                                                         \
-    if (bf16) return causal ? FN<64, true, true>(a, st) : FN<64, true, false>(a, st);    \
-    return causal ? FN<64, false, true>(a, st) : FN<64, false, false>(a, st);            \
-  }                                                                                      \
-  if (bf16) return causal ? FN<128, true, true>(a, st) : FN<128, true, false>(a, st);    \
-  return causal ? FN<128, false, true>(a, st) : FN<128, false, false>(a, st);
-
+// The kernels here serve d = 128 (head dims 32 and 64 run the persistent kernels of
+// fa_bwd64.cu).
 cudaError_t launch_dkdv128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
-  FA_BWD_DISPATCH(launch_dkdv_t)
+  if (d != 128) return cudaErrorInvalidValue;
+  if (bf16) return causal ? launch_dkdv_t<128, true, true>(a, st) : launch_dkdv_t<128, true, false>(a, st);
+  return causal ? launch_dkdv_t<128, false, true>(a, st) : launch_dkdv_t<128, false, false>(a, st);
 }
 
 cudaError_t launch_dq128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
-  FA_BWD_DISPATCH(launch_dq_t)
+  if (d != 128) return cudaErrorInvalidValue;
+  if (bf16) return causal ? launch_dq_t<128, true, true>(a, st) : launch_dq_t<128, true, false>(a, st);
+  return causal ? launch_dq_t<128, false, true>(a, st) : launch_dq_t<128, false, false>(a, st);
 }
-#undef FA_BWD_DISPATCH
 
 }  // namespace fa

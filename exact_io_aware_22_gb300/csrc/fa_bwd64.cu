@@ -532,6 +532,398 @@ cudaError_t launch_dkdv64_t(const BwdArgs& a, cudaStream_t st) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// ============================================================== dQ
+namespace q64 {
+// Q and dO (with the tile's L*log2e and D) of two work items; K and V in a 3-stage ring
+// that runs on across items; dQ rows staged for the store.
+template <int HD>
+struct Smem {
+  static constexpr int TILE = BT * HD * 2;
+  static constexpr int KV_STAGES = 3;
+  static constexpr int Q_OFF = 0;                           // Q of two items
+  static constexpr int DO_OFF = 2 * TILE;                   // dO of two items
+  static constexpr int LD_OFF = 4 * TILE;                   // per item: 128 L*log2e, 128 D
+  static constexpr int K_OFF = LD_OFF + 2 * 1024;
+  static constexpr int V_OFF = K_OFF + KV_STAGES * TILE;
+  static constexpr int ST_OFF = V_OFF + KV_STAGES * TILE;   // 32-column row slices, 8 KiB
+  static constexpr int BAR_OFF = ST_OFF + 4 * 8192;          // per compute warpgroup
+  // qd_full[2], qd_empty[2], kv_full[3], kv_empty[3], s_full, s_free, dp_full, dp_free,
+  // ds_full, z_free, out_full[2], acc_free[2], done[2], tile_full[2], tile_empty[2], clc
+  static constexpr int NBARS = 4 + 2 * KV_STAGES + 6 + 4 + 2 + 4 + 1;
+  static constexpr int CLC_OFF = (BAR_OFF + NBARS * 8 + 15) / 16 * 16;
+  static constexpr int SLOT_OFF = CLC_OFF + 16;
+  static constexpr int SMEM_BYTES = SLOT_OFF + 16;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
+};
+// TMEM: dQ of accumulator buffer a at columns 64a (HD of its 64 in use) | S (128) |
+// dP (128) | Z (64: dS as 16-bit pairs).  Compute warpgroup q owns key columns
+// [32q, 32q + 32) of S and dP and pair columns [16q, 16q + 16) of Z.
+constexpr uint32_t S_COL = 128, DP_COL = 256, Z_COL = 384;
+
+// One 128-query tile of one query head and the key blocks it sees.
+struct Item {
+  int bh, qb, hq, hk, j_lo, n_iter;
+  SeqRows sr;
+};
+template <bool CAUSAL, bool WINDOW, bool PACKED>
+__device__ __forceinline__ Item item(int id, int nqb, int ord_g, int N, int group, int window,
+                                     const int* __restrict__ cu_seqlens, int H, int total) {
+  Item t;
+  const BlockPos bp = block_pos(nqb, id, ord_g);
+  t.bh = bp.bh;
+  t.qb = nqb - 1 - bp.rank;                       // causal: the last query tiles have the most work
+  t.j_lo = WINDOW ? max(0, t.qb * BT - window + 1) / BT : 0;
+  t.sr = seq_rows_t<PACKED>(cu_seqlens, t.bh / H, N, total);
+  t.hq = t.sr.packed ? t.bh % H : t.bh;
+  t.hk = t.sr.packed ? (t.bh % H) / group : t.bh / group;
+  const int nk_r = (t.sr.n + BT - 1) / BT;        // key blocks of this sequence
+  t.n_iter = t.qb * BT >= t.sr.n ? 0 : (CAUSAL ? min(t.qb + 1, nk_r) : nk_r) - t.j_lo;
+  if (t.n_iter < 0) t.n_iter = 0;
+  return t;
+}
+}  // namespace q64
+
+template <int HD, bool BF16, bool CAUSAL, bool WINDOW, bool PACKED>
+__global__ void __launch_bounds__(THREADS, 1)
+    dq64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const float* __restrict__ Dp, const float* __restrict__ Lp, void* __restrict__ dQ,
+                int N, int Np, int group, int window, const int* __restrict__ cu_seqlens, int H,
+                int total, float scale, float c_log2, int ord_g, KernelCtl ctl) {
+  using namespace q64;
+  using SM = Smem<HD>;
+  using G = Geo<HD>;
+  constexpr int TILE = SM::TILE, KV_STAGES = SM::KV_STAGES;
+  extern __shared__ __align__(1024) uint8_t sg[];
+  const uint32_t sb = smem_u32(sg);
+  grid_dep_launch();
+  if (sb & 1023u) {                                // see FA_DEV_SMEM_ALIGN
+    grid_dep_wait();
+    if (threadIdx.x == 0) atomicOr(ctl.status, FA_DEV_SMEM_ALIGN);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nqb = Np / BT;
+  auto item_of = [&](int id) {
+    return item<CAUSAL, WINDOW, PACKED>(id, nqb, ord_g, N, group, window, cu_seqlens, H, total);
+  };
+
+  auto bar = [&](int i) -> uint32_t { return sb + SM::BAR_OFF + 8 * i; };
+  auto B_QDF = [&](int b) { return b; };
+  auto B_QDE = [&](int b) { return 2 + b; };
+  auto B_KF = [&](int s) { return 4 + s; };
+  auto B_KE = [&](int s) { return 4 + KV_STAGES + s; };
+  const int B_SF = 4 + 2 * KV_STAGES, B_SFREE = B_SF + 1, B_DPF = B_SF + 2, B_DPFREE = B_SF + 3,
+            B_DSF = B_SF + 4, B_ZFREE = B_SF + 5;
+  auto B_OF = [&](int a) { return B_SF + 6 + a; };
+  auto B_AF = [&](int a) { return B_SF + 8 + a; };
+  auto B_DONE = [&](int i) { return B_SF + 10 + i; };
+  auto B_TF = [&](int b) { return B_SF + 12 + b; };
+  auto B_TE = [&](int b) { return B_SF + 14 + b; };
+  const int B_CLC = B_SF + 16;
+  volatile int* slot = reinterpret_cast<volatile int*>(sg + SM::SLOT_OFF + 4);
+  const uint32_t clc_resp = sb + SM::CLC_OFF;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SM::NBARS; ++i) mbar_init(bar(i), 1);
+    mbar_init(bar(B_SFREE), 512);
+    mbar_init(bar(B_DPFREE), 512);
+    mbar_init(bar(B_DSF), 512);
+    mbar_init(bar(B_AF(0)), 512);
+    mbar_init(bar(B_AF(1)), 512);
+    for (int i = 0; i < KV_STAGES; ++i) mbar_init(bar(B_KE(i)), 2);   // both MMA issuers
+    mbar_init(bar(B_QDE(0)), 1);
+    mbar_init(bar(B_QDE(1)), 1);
+    mbar_init(bar(B_TE(0)), 18);                   // the MMA issuers and one lane per compute warp
+    mbar_init(bar(B_TE(1)), 18);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + SM::SLOT_OFF, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sg + SM::SLOT_OFF);
+  grid_dep_wait();                                 // D and L*log2e from the pre-pass
+
+  auto next_item = [&](int k, bool& ok) -> int {
+    if (!(ok = mbar_wait(bar(B_TF(k & 1)), (k >> 1) & 1, ctl))) return -1;
+    return slot[k & 1];
+  };
+
+  if (warp == 0) {
+    regs_dec<kRegs64Low>();                        // warpgroup 0 (TMA, MMA issue): few registers
+    // ------------------------------------------------------------ producer, scheduler
+    if (lane == 0) {
+      bool ok = true, pending = false;
+      int id = static_cast<int>(blockIdx.x);
+      int gj = 0, kq = 0, nkv = 0, n_req = 0;     // K/V tiles, items, K/V loads issued, requests
+      for (int k = 0; ok; ++k) {
+        if (!(ok = mbar_wait(bar(B_TE(k & 1)), ((k >> 1) & 1) ^ 1, ctl))) break;
+        slot[k & 1] = id;
+        mbar_arrive(bar(B_TF(k & 1)));
+        if (id < 0) break;
+        // ask for the next item now, so that it is known once this item's loads are out
+        mbar_arrive_expect_tx(bar(B_CLC), 16);
+        clc_try_cancel(clc_resp, bar(B_CLC));
+        pending = true;
+        ++n_req;
+        const Item t = item_of(id);
+        if (t.n_iter > 0) {
+          const int b = kq & 1;
+          const int qrow = t.qb * BT;
+          if (!(ok = mbar_wait(bar(B_QDE(b)), ((kq >> 1) & 1) ^ 1, ctl))) break;
+          mbar_arrive_expect_tx(bar(B_QDF(b)), 2 * TILE + 1024);
+          for (int c = 0; c < G::NCH; ++c) {
+            tma_load_3d(sb + SM::Q_OFF + b * TILE + c * G::CHUNK, &tmQ, bar(B_QDF(b)),
+                        c * G::SPAN, t.sr.y(qrow, t.hq), t.sr.z(qrow, t.hq));
+            tma_load_3d(sb + SM::DO_OFF + b * TILE + c * G::CHUNK, &tmdO, bar(B_QDF(b)),
+                        c * G::SPAN, t.sr.y(qrow, t.hq), t.sr.z(qrow, t.hq));
+          }
+          const size_t row = static_cast<size_t>(t.bh) * Np + qrow;
+          bulk_load(sb + SM::LD_OFF + b * 1024, Lp + row, 512, bar(B_QDF(b)));
+          bulk_load(sb + SM::LD_OFF + b * 1024 + 512, Dp + row, 512, bar(B_QDF(b)));
+          ++kq;
+          for (int j = 0; j < t.n_iter; ++j, ++gj) {
+            const int s = gj % KV_STAGES;
+            const int krow = (t.j_lo + j) * BT;
+            if (!(ok = mbar_wait(bar(B_KE(s)), ((gj / KV_STAGES) & 1) ^ 1, ctl))) break;
+            mbar_arrive_expect_tx(bar(B_KF(s)), 2 * TILE);
+            for (int c = 0; c < G::NCH; ++c) {
+              tma_load_3d(sb + SM::K_OFF + s * TILE + c * G::CHUNK, &tmK, bar(B_KF(s)),
+                          c * G::SPAN, t.sr.y(krow, t.hk), t.sr.z(krow, t.hk));
+              tma_load_3d(sb + SM::V_OFF + s * TILE + c * G::CHUNK, &tmV, bar(B_KF(s)),
+                          c * G::SPAN, t.sr.y(krow, t.hk), t.sr.z(krow, t.hk));
+            }
+            ++nkv;
+          }
+          if (!ok) break;
+        }
+        // the next item: a CTA that had not started, if any was left
+        if (!(ok = mbar_wait(bar(B_CLC), k & 1, ctl))) break;
+        pending = false;
+        id = clc_result(clc_resp);
+      }
+      if (!ok) {
+        // drain: wait (bounded) for the copies this thread may still have in flight
+        if (pending) mbar_wait(bar(B_CLC), (n_req - 1) & 1, ctl);   // the response lands in smem
+        for (int i = max(0, kq - 2); i < kq; ++i) mbar_wait(bar(B_QDF(i & 1)), (i >> 1) & 1, ctl);
+        for (int i = max(0, nkv - KV_STAGES); i < nkv; ++i)
+          mbar_wait(bar(B_KF(i % KV_STAGES)), (i / KV_STAGES) & 1, ctl);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1 || warp == 2) {
+    regs_dec<kRegs64Low>();
+    // ------------------------------------------------------------ MMA issuers
+    // warp 1: the score products S = Q K^T and dP = dO V^T; warp 2: dQ += dS K.  A K/V
+    // stage is free once both threads' products that read it have completed.
+    if (lane == 0) {
+      const bool scores = warp == 1;
+      constexpr uint32_t idS = umma_idesc_f16(BT, BT, BF16, false, false);   // S, dP
+      constexpr uint32_t idQ = umma_idesc_f16(BT, HD, BF16, false, true);    // dQ
+      constexpr uint32_t HI = G::HI, STAGE_W = TILE >> 4;
+      const uint32_t q_lo = sdesc_lo(sb + SM::Q_OFF, 16), o_lo = sdesc_lo(sb + SM::DO_OFF, 16);
+      const uint32_t k_lo = sdesc_lo(sb + SM::K_OFF, 16), km_lo = sdesc_lo(sb + SM::K_OFF, G::CHUNK);
+      const uint32_t v_lo = sdesc_lo(sb + SM::V_OFF, 16);
+      bool ok = true;
+      int gj = 0, kq = 0;
+      for (int k = 0; ok; ++k) {
+        const int id = next_item(k, ok);
+        if (!ok) break;
+        mbar_arrive(bar(B_TE(k & 1)));
+        if (id < 0) break;
+        const Item t = item_of(id);
+        if (t.n_iter <= 0) continue;
+        const int b = kq & 1, a = kq & 1;
+        if (scores) {
+          if (!(ok = mbar_wait(bar(B_QDF(b)), (kq >> 1) & 1, ctl))) break;
+          const uint32_t qa = q_lo + b * STAGE_W, oa = o_lo + b * STAGE_W;
+          for (int j = 0; ok && j < t.n_iter; ++j, ++gj) {
+            const int s = gj % KV_STAGES;
+            if (!(ok = mbar_wait(bar(B_KF(s)), (gj / KV_STAGES) & 1, ctl))) break;
+            // S once the compute warps have read the previous one, then dP likewise
+            if (gj > 0 && !(ok = mbar_wait(bar(B_SFREE), (gj - 1) & 1, ctl))) break;
+            tc_fence_after();
+            issue_ab_t_w<HD>(tmem + S_COL, qa, k_lo + s * STAGE_W, idS);
+            umma_commit(bar(B_SF));
+            if (gj > 0 && !(ok = mbar_wait(bar(B_DPFREE), (gj - 1) & 1, ctl))) break;
+            tc_fence_after();
+            issue_ab_t_w<HD>(tmem + DP_COL, oa, v_lo + s * STAGE_W, idS);
+            umma_commit(bar(B_DPF));
+            umma_commit(bar(B_KE(s)));
+          }
+          if (!ok) break;
+          umma_commit(bar(B_QDE(b)));              // this item's Q and dO no longer read
+        } else {
+          const uint32_t dq_col = tmem + 64 * a;
+          for (int j = 0; ok && j < t.n_iter; ++j, ++gj) {
+            const int s = gj % KV_STAGES;
+            // dQ += dS K: dS from Z (k-step kk, keys [16kk, 16kk + 16), is warpgroup kk / 2's),
+            // K as an MN-major B; the item's first one overwrites this dQ buffer, whose
+            // previous item the epilogue must have read
+            if (!(ok = mbar_wait(bar(B_DSF), gj & 1, ctl))) break;
+            if (j == 0 && !(ok = mbar_wait(bar(B_AF(a)), ((kq >> 1) & 1) ^ 1, ctl))) break;
+            tc_fence_after();
+            const uint32_t kb0 = km_lo + s * STAGE_W, acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < BT / 16; ++kk)
+              umma_ts_w(dq_col, tmem + Z_COL + (kk / 2) * 16 + (kk % 2) * 8,
+                        kb0 + kk * (G::KSTEP_MN >> 4), HI, idQ, kk > 0 ? 1u : acc0);
+            umma_commit(bar(B_ZFREE));
+            umma_commit(bar(B_KE(s)));
+          }
+          if (!ok) break;
+          umma_commit(bar(B_OF(a)));               // this item's dQ is complete
+        }
+        ++kq;
+      }
+      // every MMA this thread issued has completed before TMEM is released
+      umma_commit(bar(B_DONE(scores ? 0 : 1)));
+      mbar_wait(bar(B_DONE(scores ? 0 : 1)), 0, ctl);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    regs_inc<kRegs64High>();                       // the compute warpgroups take what it gives back
+    // ------------------------------------------------------------ compute, epilogue
+    const int q = (warp - 4) >> 2;                 // key columns [32q, 32q + 32)
+    const int r = (warp & 3) * 32 + lane;          // query row within the tile (= TMEM lane)
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + S_COL + 32 * q;
+    const uint32_t tP = tmem + lane_off + DP_COL + 32 * q;
+    const uint32_t tZ = tmem + lane_off + Z_COL + 16 * q;
+    uint4* stage = reinterpret_cast<uint4*>(sg + SM::ST_OFF + q * 8192) + (warp & 3) * 32 * 4;
+    using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    const float2 c2 = make_float2(c_log2, c_log2);
+    bool ok = true;
+    int gj = 0, kq = 0;
+    for (int k = 0; ok; ++k) {
+      const int id = next_item(k, ok);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_TE(k & 1)));
+      if (id < 0) break;
+      const Item t = item_of(id);
+      if (t.n_iter <= 0) continue;
+      const int b = kq & 1, a = kq & 1;
+      const int grow = t.qb * BT + r;
+      // this row's L*log2e and D (padded rows: +inf and 0, never stored)
+      if (!(ok = mbar_wait_warp(bar(B_QDF(b)), (kq >> 1) & 1, ctl))) break;
+      const float lr = reinterpret_cast<const float*>(sg + SM::LD_OFF + b * 1024)[r];
+      const float dr = reinterpret_cast<const float*>(sg + SM::LD_OFF + b * 1024 + 512)[r];
+      const float lsub = lr == INFINITY ? 0.f : lr;
+      const float2 nl2 = make_float2(-lsub, -lsub), nd2 = make_float2(-dr, -dr);
+      for (int j = 0; j < t.n_iter; ++j, ++gj) {
+        const int k0 = (t.j_lo + j) * BT + 32 * q;  // first key of this thread's columns
+        if (!(ok = mbar_wait_warp(bar(B_SF), gj & 1, ctl))) break;
+        tc_fence_after();
+        uint32_t x[32];
+        tmem_ld32(tS, x);
+        tmem_ld_wait_regs(x);
+        tc_fence_before();
+        mbar_arrive(bar(B_SFREE));                 // S may now receive the next block
+        // P = exp2(S c - L log2e); on the diagonal block, zero where the key follows the query
+        float p[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 tt = fma2(make_float2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])),
+                                 c2, nl2);
+          p[2 * i] = ex2(tt.x);
+          p[2 * i + 1] = ex2(tt.y);
+        }
+        if (CAUSAL && t.j_lo + j == t.qb) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (k0 + c > grow) p[c] = 0.f;
+        }
+        if (WINDOW && t.qb * BT + BT - 1 - (t.j_lo + j) * BT >= window) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (grow - (k0 + c) >= window) p[c] = 0.f;
+        }
+        if (PACKED && k0 + 32 > t.sr.n) {
+          // keys past the end of a packed sequence are the next sequence's keys
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (k0 + c >= t.sr.n) p[c] = 0.f;
+        }
+        if (!(ok = mbar_wait_warp(bar(B_DPF), gj & 1, ctl))) break;
+        tc_fence_after();
+        tmem_ld32(tP, x);
+        tmem_ld_wait_regs(x);
+        tc_fence_before();
+        mbar_arrive(bar(B_DPFREE));                // dP may now receive the next block
+        // dS = P o (dP - D) as 16-bit pairs into Z once the previous block's dQ read it
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 ds = mul2(make_float2(p[2 * i], p[2 * i + 1]),
+                                 add2(make_float2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])),
+                                      nd2));
+          w[i] = pack2<BF16>(ds.x, ds.y);
+        }
+        if (gj > 0 && !(ok = mbar_wait_warp(bar(B_ZFREE), (gj - 1) & 1, ctl))) break;
+        tc_fence_after();
+        tmem_st16(tZ, w);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(B_DSF));
+      }
+      if (!ok) break;
+      // epilogue: warpgroup q stores dQ columns [32q, 32q + 32) (scaled) from buffer a
+      if (!(ok = mbar_wait_warp(bar(B_OF(a)), (kq >> 1) & 1, ctl))) break;
+      tc_fence_after();
+      if (32 * q < HD) {
+        const int row0 = t.qb * BT + (warp & 3) * 32;
+        T* base = reinterpret_cast<T*>(dQ) + 32 * q;
+        store_rows_staged<BF16>(
+            tmem + lane_off + 64 * a + 32 * q, scale, stage, lane,
+            [&](int rr) { return base + t.sr.off(row0 + rr, t.hq, H, N, HD); }, t.sr.n - row0);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_AF(a)));                   // buffer a may take the item after next
+      ++kq;
+    }
+  } else {
+    regs_dec<kRegs64Low>();                        // warp 3: idle
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int HD, bool BF16, bool CAUSAL>
+cudaError_t launch_dq64_t(const BwdArgs& a, cudaStream_t st) {
+  const int Np = (a.N + 127) / 128 * 128;
+  const float* Lp = a.Dvec + static_cast<size_t>(a.BH) * Np;
+  const long long nblk = static_cast<long long>(Np / BT) * a.BH;           // per query head
+  // windowed and packed-sequence kernels are separate instantiations
+  auto kern = CAUSAL && a.window > 0
+      ? (a.cu_seqlens ? dq64_kernel<HD, BF16, CAUSAL, CAUSAL, true>
+                      : dq64_kernel<HD, BF16, CAUSAL, CAUSAL, false>)
+      : (a.cu_seqlens ? dq64_kernel<HD, BF16, CAUSAL, false, true>
+                      : dq64_kernel<HD, BF16, CAUSAL, false, false>);
+  constexpr int smem = q64::Smem<HD>::SMEM_BYTES;
+  cudaError_t e = check_split_regs(reinterpret_cast<const void*>(kern), kRegs64Launch);
+  if (e != cudaSuccess) return e;
+  e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  // an item streams the K and V tiles of its query head's K/V head
+  const int ord_g = order_group(a.BH, 2ll * Np * HD * 2);
+  trace_begin(TR_BWD_DQ, st);
+  e = launch_dependent(kern, static_cast<unsigned>(nblk), THREADS, smem, st, a.tmQ, a.tmK, a.tmV,
+                       a.tmdO, static_cast<const float*>(a.Dvec), Lp, a.dQ, a.N, Np, a.group,
+                       a.window, a.cu_seqlens, a.H, a.total, a.scale, a.c_log2, ord_g, a.ctl);
+  trace_end(TR_BWD_DQ, st);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_dkdv64(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
@@ -542,6 +934,18 @@ cudaError_t launch_dkdv64(const BwdArgs& a, int d, bool bf16, bool causal, cudaS
   if (d == 64) {
     if (bf16) return causal ? launch_dkdv64_t<64, true, true>(a, st) : launch_dkdv64_t<64, true, false>(a, st);
     return causal ? launch_dkdv64_t<64, false, true>(a, st) : launch_dkdv64_t<64, false, false>(a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dq64(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st) {
+  if (d == 32) {
+    if (bf16) return causal ? launch_dq64_t<32, true, true>(a, st) : launch_dq64_t<32, true, false>(a, st);
+    return causal ? launch_dq64_t<32, false, true>(a, st) : launch_dq64_t<32, false, false>(a, st);
+  }
+  if (d == 64) {
+    if (bf16) return causal ? launch_dq64_t<64, true, true>(a, st) : launch_dq64_t<64, true, false>(a, st);
+    return causal ? launch_dq64_t<64, false, true>(a, st) : launch_dq64_t<64, false, false>(a, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -123,6 +123,7 @@ cudaError_t launch_bwd(const BwdArgs& a, int d, bool bf16, bool causal, cudaStre
 cudaError_t launch_dkdv128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
 cudaError_t launch_dq128(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
 cudaError_t launch_dkdv64(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
+cudaError_t launch_dq64(const BwdArgs& a, int d, bool bf16, bool causal, cudaStream_t st);
 // Workspace: D and L*log2(e) per padded row.
 size_t bwd_workspace_bytes(long long BH, int N, int d);
 

@@ -66,11 +66,11 @@ def test_committed_profiles_have_the_fields_the_bench_reads():
     names = [n for n in os.listdir(os.path.join(ROOT, "profiles")) if n.endswith(".txt")]
     assert names
     for n in names:
-        kernel = n.split("__")[0]
+        kernel, workload = n[:-4].split("__")
         assert kernel in bench.KERNEL_SOURCES, n
         text = open(os.path.join(ROOT, "profiles", n)).read()
         src = re.search(r"^source:\s*(\S+)", text, re.M)
-        assert src and src.group(1) == bench.KERNEL_SOURCES[kernel], n
+        assert src and src.group(1) == bench.kernel_source(kernel, workload), n
         assert re.search(r"source_sha256:\s*[0-9a-f]{64}", text), n
         assert re.search(r"dram_bytes_per_launch:\s*[0-9]+", text), n
         assert "--clock-control none" in text, n
@@ -123,3 +123,10 @@ def test_profile_record_reads_tensor_activity(tmp_path, monkeypatch):
     assert bench.profile_record("fwd_kernel", "w") == (1234.0, 66.2)
     src.write_text("changed")
     assert bench.profile_record("fwd_kernel", "w") == (None, None)
+
+
+def test_kernel_source_follows_the_head_dim():
+    assert bench.kernel_source("bwd_dkdv_kernel", "n8k_causal_d128_bf16").endswith("fa_bwd128.cu")
+    assert bench.kernel_source("bwd_dkdv_kernel", "gpt2m_causal_d64_fp16").endswith("fa_bwd64.cu")
+    assert bench.kernel_source("bwd_dq_kernel", "ragged_causal_d32_fp16").endswith("fa_bwd64.cu")
+    assert bench.kernel_source("fwd_kernel", "ragged_causal_d32_fp16").endswith("fa_fwd.cu")
