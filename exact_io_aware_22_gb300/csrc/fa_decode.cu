@@ -377,6 +377,248 @@ __global__ void __launch_bounds__(32 * DEC_WARPS, 3)
   }
 }
 
+// ---------------------------------------------------------------- E4M3 caches
+// The split kernel for E4M3 caches (d = 128) forms scores and P.V with warp-level
+// tensor-core products (mma.sync m16n8k16, f16 operands, fp32 accumulation) instead
+// of per-key FMAs, so each key costs a code conversion and a share of 64 MMAs per
+// 32-key stage rather than 2 x 128 FMAs per query row: the cache read, not the issue
+// slots, then sets the pace.  E4M3 codes convert to f16 exactly (cvt of two codes per
+// instruction); q is taken as f16 (exact for fp16 input, and for bf16 values inside
+// f16's range) and the scale is applied to the fp32 scores; P is rounded to f16 for
+// the P.V product (the row sums use the fp32 values).
+//   rows     query row g = lane / 4 of the group (rows >= R are zero padding)
+//   scores   the head dim is visited in an order of its own, the same for q and K:
+//            k-step ks, fragment column 2c + e (e = 0, 1) and 2c + 8 + e stand for
+//            dims 32c + 4ks + e and 32c + 4ks + 2 + e (c = lane % 4), so lane (g, c)
+//            reads 32 contiguous bytes of its key row per 8-key tile.
+//   P.V      the score fragments of two key tiles are the A fragment of one 16-key
+//            k-step (P never leaves registers); output fragment column n of tile jn
+//            stands for dim 16n + jn, so lane (g, c) reads 16 contiguous bytes of each
+//            of its four V rows, and holds dims 32c + jn and 32c + 16 + jn.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t codes16) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(r)
+      : "r"(codes16));
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                         uint32_t b1) {
+  // rows g + 8 of A are zero (a1 = a3 = 0)
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <bool BF16, int R>
+__global__ void __launch_bounds__(32 * DEC_WARPS, 3)
+    decode8_split_kernel(const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const void* __restrict__ Q,
+                         const int* __restrict__ seqlens, float* __restrict__ part, int H, int Hkv,
+                         int Nmax, int chunk, int n_splits, float c_log2, KernelCtl ctl) {
+  constexpr int D = 128;
+  using G = DecGeom<D, true>;
+  constexpr int KEYS = G::KEYS;                 // 32 keys per stage, one 128-byte row each
+  static_assert(KEYS == 32 && G::ROWB == 128 && G::HALVES == 1, "E4M3 stage geometry");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, cq = lane & 3;      // fragment row, column pair
+  const int n_rc = (H / Hkv) / R;               // row groups per K/V head
+  long long t = blockIdx.x;
+  const int rc = static_cast<int>(t % n_rc);
+  t /= n_rc;
+  const int split = static_cast<int>(t % n_splits);
+  const int bkv = static_cast<int>(t / n_splits);           // b * Hkv + hk
+  const int b = bkv / Hkv, hk = bkv % Hkv;
+  const int n = min(max(__ldg(seqlens + b), 0), Nmax);       // cached keys of this sequence
+  const int s0 = split * chunk;
+  if (s0 >= n) return;                          // no keys here; the merge skips this split
+  const int s1 = min(s0 + chunk, n);
+  const int per = ((s1 - s0 + DEC_WARPS * KEYS - 1) / (DEC_WARPS * KEYS)) * KEYS;
+  const int j0 = min(s0 + warp * per, s1), j1 = min(j0 + per, s1);
+  const int nch = (j1 - j0 + KEYS - 1) / KEYS;
+  const int h0 = (hk * (H / Hkv)) + rc * R;      // first query head of the group
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  const uint32_t ring = sb + warp * DEC_STAGES * G::STAGEB;
+  const uint32_t bars = sb + DEC_WARPS * DEC_STAGES * G::STAGEB + warp * DEC_STAGES * 8;
+  if (lane == 0) {
+    for (int st = 0; st < DEC_STAGES; ++st) mbar_init(bars + st * 8, 1);
+    fence_mbar_init();
+  }
+  // q of row gq as the A fragments of the score products, in f16 (rows >= R: zero)
+  uint32_t qa[8][2];
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (gq < R) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        v[e] = load_f<BF16>(Q, (static_cast<size_t>(b) * H + h0 + gq) * D + 32 * cq + 4 * ks + e);
+    }
+    qa[ks][0] = f2_to_h2(v[0], v[1]);
+    qa[ks][1] = f2_to_h2(v[2], v[3]);
+  }
+  __syncwarp();
+
+  auto issue = [&](int c, int st) {
+    const uint32_t bar = bars + st * 8, dst = ring + st * G::STAGEB;
+    mbar_arrive_expect_tx(bar, G::STAGEB);
+    const int y = j0 + c * KEYS;
+    tma_load_3d(dst, &tmK, bar, 0, y, bkv);
+    tma_load_3d(dst + G::TILEB, &tmV, bar, 0, y, bkv);
+  };
+  if (lane == 0)
+    for (int c = 0; c < DEC_STAGES && c < nch; ++c) issue(c, c);
+
+  float m_row = -INFINITY, l_part = 0.f;        // row gq: running max, this lane's part of l
+  float acc[16][4];                             // P.V fragments of 16 output tiles
+#pragma unroll
+  for (int jn = 0; jn < 16; ++jn)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[jn][e] = 0.f;
+
+  int c = 0;
+  for (; c < nch; ++c) {
+    const int st = c % DEC_STAGES;
+    if (!mbar_wait_warp(bars + st * 8, (c / DEC_STAGES) & 1, ctl)) break;
+    const uint32_t kt = ring + st * G::STAGEB, vt = kt + G::TILEB;
+    const int nk = min(KEYS, j1 - j0 - c * KEYS);
+
+    // scores of row gq with keys 8j + 2cq + e (e = 0, 1), j = 0..3
+    float s[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[j][e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int key = 8 * j + gq;
+      const uint4 wa = lds128(kt + swz<G::SWM>(key * G::ROWB + 32 * cq));
+      const uint4 wb = lds128(kt + swz<G::SWM>(key * G::ROWB + 32 * cq + 16));
+      const uint32_t w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma16816(s[j], qa[ks][0], qa[ks][1], cvt_e4m3x2_f16x2(w[ks] & 0xffffu),
+                 cvt_e4m3x2_f16x2(w[ks] >> 16));
+    }
+    // online update of row gq over this stage's keys (keys past nk: -inf)
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = 8 * j + 2 * cq + e;
+        s[j][e] = key < nk ? s[j][e] * c_log2 : -INFINITY;
+        mx = fmaxf(mx, s[j][e]);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_row, mx);       // finite: the stage holds a key
+    const float alpha = ex2(m_row - m_new);     // 0 at the first stage
+    m_row = m_new;
+    float p[4][2];
+    float ps = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        p[j][e] = ex2(s[j][e] - m_new);         // 0 for keys past nk
+        ps += p[j][e];
+      }
+    l_part = fmaf(l_part, alpha, ps);
+#pragma unroll
+    for (int jn = 0; jn < 16; ++jn) {
+      acc[jn][0] *= alpha;
+      acc[jn][1] *= alpha;
+    }
+    // P.V: k-step kk covers keys 16kk .. 16kk + 15; V rows past nk read as zero
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint32_t pa0 = f2_to_h2(p[2 * kk][0], p[2 * kk][1]);
+      const uint32_t pa2 = f2_to_h2(p[2 * kk + 1][0], p[2 * kk + 1][1]);
+      const int r0 = 16 * kk + 2 * cq;          // rows r0, r0 + 1 (b0) and r0 + 8, r0 + 9 (b1)
+      uint4 v4[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int vr = r0 + (q4 & 1) + 8 * (q4 >> 1);
+        v4[q4] = lds128(vt + swz<G::SWM>(vr * G::ROWB + 16 * gq));
+        if (vr >= nk) v4[q4] = make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd) {
+        const uint32_t A0 = (&v4[0].x)[wd], A1 = (&v4[1].x)[wd];   // rows r0, r0 + 1
+        const uint32_t B0 = (&v4[2].x)[wd], B1 = (&v4[3].x)[wd];   // rows r0 + 8, r0 + 9
+        const uint32_t lo0 = prmt(A0, A1, 0x5140u), hi0 = prmt(A0, A1, 0x7362u);
+        const uint32_t lo1 = prmt(B0, B1, 0x5140u), hi1 = prmt(B0, B1, 0x7362u);
+        mma16816(acc[4 * wd + 0], pa0, pa2, cvt_e4m3x2_f16x2(lo0 & 0xffffu), cvt_e4m3x2_f16x2(lo1 & 0xffffu));
+        mma16816(acc[4 * wd + 1], pa0, pa2, cvt_e4m3x2_f16x2(lo0 >> 16), cvt_e4m3x2_f16x2(lo1 >> 16));
+        mma16816(acc[4 * wd + 2], pa0, pa2, cvt_e4m3x2_f16x2(hi0 & 0xffffu), cvt_e4m3x2_f16x2(hi1 & 0xffffu));
+        mma16816(acc[4 * wd + 3], pa0, pa2, cvt_e4m3x2_f16x2(hi0 >> 16), cvt_e4m3x2_f16x2(hi1 >> 16));
+      }
+    }
+    __syncwarp();                                 // stage read by every lane
+    if (lane == 0 && c + DEC_STAGES < nch) issue(c + DEC_STAGES, st);
+  }
+  if (c < nch) {
+    // a wait ran out (recorded in the status word): let the copies already issued
+    // land (bounded) before the CTA's shared memory is released
+    for (int k = c; k < nch && k < c + DEC_STAGES; ++k)
+      mbar_wait_warp(bars + (k % DEC_STAGES) * 8, (k / DEC_STAGES) & 1, ctl);
+  }
+
+  // row sums over the four lanes of a row; the warps' states merged per row in shared
+  // memory (staged in the ring once every warp is done with it); one record per row and split
+  l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
+  l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
+  __syncthreads();
+  float* red = reinterpret_cast<float*>(smem_raw + (sb - raw));   // [W][R] (m, l), [W][R][D] acc
+  float* racc = red + 2 * DEC_WARPS * R;
+  if (gq < R) {
+    if (cq == 0) {
+      red[(warp * R + gq) * 2] = m_row;
+      red[(warp * R + gq) * 2 + 1] = l_part;
+    }
+#pragma unroll
+    for (int jn = 0; jn < 16; ++jn) {
+      racc[(warp * R + gq) * D + 32 * cq + jn] = acc[jn][0];
+      racc[(warp * R + gq) * D + 32 * cq + 16 + jn] = acc[jn][1];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < R * D; i += 32 * DEC_WARPS) {
+    const int r = i / D, col = i % D;
+    float mm = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < DEC_WARPS; ++w) mm = fmaxf(mm, red[(w * R + r) * 2]);   // finite: warp 0 has keys
+    float ll = 0.f, aa = 0.f;
+#pragma unroll
+    for (int w = 0; w < DEC_WARPS; ++w) {
+      const float a = ex2(red[(w * R + r) * 2] - mm);   // an empty warp (m = -inf) weighs 0
+      ll = fmaf(red[(w * R + r) * 2 + 1], a, ll);
+      aa = fmaf(racc[(w * R + r) * D + col], a, aa);
+    }
+    float* dst = part + ((static_cast<size_t>(b) * H + h0 + r) * n_splits + split) * (D + 4);
+    dst[4 + col] = aa;
+    if (col == 0) {
+      dst[0] = mm;
+      dst[1] = ll;
+    }
+  }
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(D)
     decode_merge_kernel(const float* __restrict__ part, const int* __restrict__ seqlens,
@@ -412,7 +654,10 @@ __global__ void __launch_bounds__(D)
 template <int D, bool BF16, int R, bool C8>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   constexpr int smem = dec_smem_bytes<D, R, C8>();
-  auto kern = decode_split_kernel<D, BF16, R, C8>;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const void*, const int*, float*, int, int,
+               int, int, int, float, KernelCtl);
+  if constexpr (C8) kern = decode8_split_kernel<BF16, R>;
+  else kern = decode_split_kernel<D, BF16, R, C8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long ctas =

@@ -103,8 +103,9 @@ def test_decode_caller_workspace_matches_library_allocation():
 
 def run_decode_fp8(B, H, Hkv, Nmax, lens, dtype, seed=0, rows=None):
     """E4M3 caches: the oracle's decode of the dequantized caches (codes times their
-    descale factors).  Only the cache is in 8 bits (the scores and P stay fp32), so the
-    16-bit decode tolerances hold."""
+    descale factors).  Only the cache is in 8 bits: the scores are exact products summed
+    in fp32 and P is rounded to f16 for the tensor-core P.V product (half the 16-bit
+    input's rounding or less), so the 16-bit decode tolerances hold."""
     import exact_io_aware_22_gb300 as fa
     d = 128
     x = inputs.make_decode_fp8_inputs(B, H, Hkv, Nmax, d, lens, dtype, seed=seed, fill_code=0x7F)
