@@ -1,5 +1,6 @@
-// fa_bwd128.cu -- attention backward (dK/dV and dQ) on sm_103a, templated on the
-// head dim HD = 32, 64, 128 (the pre-pass is in fa_bwd.cu).
+// fa_bwd128.cu -- attention backward (dK/dV and dQ) on sm_103a at head dim 128
+// (the pre-pass is in fa_bwd.cu, the persistent kernels for head dims 32 and 64
+// in fa_bwd64.cu).  The kernels are templated on HD but instantiated at 128 only.
 //
 // Method: "flash-attn-triton" docs page, section "Scope" (backward kernels for
 // dQ, dK, dV that rebuild P from the saved L; causal mask only on diagonal
