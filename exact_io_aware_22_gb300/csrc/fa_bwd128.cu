@@ -42,7 +42,8 @@
 // and the split form is deterministic.
 //
 // Roles in both kernels (384 threads, one CTA per SM):
-//   warp 0       TMA producer.   warp 1  TMEM allocator; lane 0 issues MMAs.
+//   warp 0       TMA producer.   warp 1  TMEM allocator; lane 0 issues MMAs
+//                (in dq: S and dP; lane 0 of warp 2 issues dQ).
 //   warps 4-11   two compute warpgroups, one thread per TMEM lane (a key row
 //                in dkdv, a query row in dq), 64 columns each; in the epilogue
 //                warpgroup h stores head-dim columns [64h, 64h + 64).
@@ -505,6 +506,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(bar(B_SFREE), 256);
     mbar_init(bar(B_DPFREE), 256);
     mbar_init(bar(B_DSF), 256);
+    for (int st = 0; st < KV_STAGES; ++st) mbar_init(bar(B_KE(st)), 2);   // S/dP and dQ issuers
+    mbar_init(bar(B_DONE), 2);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -550,11 +553,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_iter > 0) {
       constexpr uint32_t idS = umma_idesc_f16(BT, BT, BF16, false, false);   // S, dP
-      constexpr uint32_t idQ = umma_idesc_f16(BT, HD, BF16, false, true);    // dQ
       // descriptor low words of dO and of stage 0 of the K and V rings, K-major (LBO 16)
-      // and, for K as the B operand of dQ, MN-major (LBO = one 64-column chunk)
       constexpr uint32_t HI = G::HI, STAGE_W = TILE >> 4;
-      const uint32_t k_lo = sdesc_lo(sb + K_OFF, 16), km_lo = sdesc_lo(sb + K_OFF, G::CHUNK);
+      const uint32_t k_lo = sdesc_lo(sb + K_OFF, 16);
       const uint32_t v_lo = sdesc_lo(sb + V_OFF, 16), o_lo = sdesc_lo(sb + DO_OFF, 16);
       auto issue_s = [&](int st) {                   // S = Q K^T, Q from TMEM
         const uint32_t b0 = k_lo + st * STAGE_W;
@@ -574,23 +575,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         umma_commit(bar(B_SF));
         issue_dp(0);
         umma_commit(bar(B_DPF));
+        umma_commit(bar(B_KE(0)));
       }
+      for (int j = 0; ok && j + 1 < n_iter; ++j) {
+        // the next block's S and dP as soon as the compute warps hold this block's
+        const int s1 = (j + 1) % KV_STAGES;
+        if (!(ok = mbar_wait(bar(B_KF(s1)), ((j + 1) / KV_STAGES) & 1, ctl))) break;
+        if (!(ok = mbar_wait(bar(B_SFREE), j & 1, ctl))) break;
+        tc_fence_after();
+        issue_s(s1);
+        umma_commit(bar(B_SF));
+        if (!(ok = mbar_wait(bar(B_DPFREE), j & 1, ctl))) break;
+        tc_fence_after();
+        issue_dp(s1);
+        umma_commit(bar(B_DPF));
+        umma_commit(bar(B_KE(s1)));
+      }
+      umma_commit(bar(B_DONE));
+      mbar_wait(bar(B_DONE), 0, ctl);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    regs_dec<kRegsLow>();
+    // ------------------------------------------------------------ MMA issuer for dQ: a
+    // thread of its own, so that dQ(j) is not queued behind the issue of S(j+1) and
+    // dP(j+1), nor they behind the wait for dS(j)
+    if (lane == 0 && n_iter > 0) {
+      constexpr uint32_t idQ = umma_idesc_f16(BT, HD, BF16, false, true);
+      // K as the B operand of dQ: MN-major, LBO = one 64-column chunk
+      constexpr uint32_t HI = G::HI, STAGE_W = TILE >> 4;
+      const uint32_t km_lo = sdesc_lo(sb + K_OFF, G::CHUNK);
+      bool ok = true;
       for (int j = 0; ok && j < n_iter; ++j) {
         const int s = j % KV_STAGES;
-        if (j + 1 < n_iter) {
-          // the next block's S and dP as soon as the compute warps hold this block's
-          const int s1 = (j + 1) % KV_STAGES;
-          if (!(ok = mbar_wait(bar(B_KF(s1)), ((j + 1) / KV_STAGES) & 1, ctl))) break;
-          if (!(ok = mbar_wait(bar(B_SFREE), j & 1, ctl))) break;
-          tc_fence_after();
-          issue_s(s1);
-          umma_commit(bar(B_SF));
-          if (!(ok = mbar_wait(bar(B_DPFREE), j & 1, ctl))) break;
-          tc_fence_after();
-          issue_dp(s1);
-          umma_commit(bar(B_DPF));
-        }
         // dQ += dS K: dS from Z, K as an MN-major B
+        if (!(ok = mbar_wait(bar(B_KF(s)), (j / KV_STAGES) & 1, ctl))) break;
         if (!(ok = mbar_wait(bar(B_DSF), j & 1, ctl))) break;
         tc_fence_after();
         const uint32_t kb0 = km_lo + s * STAGE_W;
@@ -725,7 +744,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                            grow < sr.n);
     }
   } else {
-    regs_dec<kRegsLow>();                          // warps 2 and 3: idle
+    regs_dec<kRegsLow>();                          // warp 3: idle
   }
   tc_fence_before();
   __syncthreads();
