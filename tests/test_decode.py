@@ -137,6 +137,9 @@ FP8_CASES = [
     (2, 16, 1, 2000, "bf16", (1999, 1234)),
     (2, 8, 8, 513, "fp16", (513, 17)),
     (2, 12, 2, 300, "bf16", (300, 31)),
+    (2, 4, 1, 16, "bf16", (16, 15)),                          # shorter than one ring stage
+    (5, 8, 4, 64, "fp16", (0, 0, 0, 0, 0)),                   # every cache empty
+    (3, 24, 8, 2049, "fp16", (2049, 2048, 33)),               # G = 3, a 32-key stage plus one
 ]
 
 

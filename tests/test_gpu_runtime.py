@@ -46,9 +46,13 @@ def test_nan_prefill_and_canaries(N, causal):
         assert (buf[count:].float() == stored).all()
 
 
-def test_deterministic():
+@pytest.mark.parametrize("B,H,N,d", [(2, 4, 777, 128), (4, 16, 1500, 64), (8, 8, 1000, 32)])
+def test_deterministic(B, H, N, d):
+    """Twice the same inputs, bit-identical results.  At d <= 64 the kernels are
+    persistent and take tiles in whatever order the hardware hands them out; every
+    tile still writes its outputs alone, with no atomics, so the order cannot show."""
     fa = _fa()
-    x = inputs.make_inputs(2, 4, 777, 128, "bf16", seed=2)
+    x = inputs.make_inputs(B, H, N, d, "bf16", seed=2)
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
     outs = []
     for _ in range(2):
