@@ -26,7 +26,11 @@
  *   Alignment  16-bit arrays and the workspace: 16-byte aligned; L: 4-byte aligned.
  *   Streams    `stream` is a cudaStream_t (NULL = the legacy default stream).
  *              Calls only enqueue work: they return before the GPU finishes and
- *              never synchronise, except fa_device_status.
+ *              never synchronise, except fa_device_status.  So a sequence of calls
+ *              can be captured into a CUDA graph once each call has run eagerly
+ *              (the first call of a kind sets kernel attributes) and, for the
+ *              backward, with a caller workspace; the replay gives the eager
+ *              results bit for bit.
  *   Errors     arguments are validated before anything is launched; a call that
  *              returns an error has enqueued nothing (launch failures excepted:
  *              FA_ERR_CUDA, with the CUDA error code from fa_last_cuda_error()).
