@@ -232,13 +232,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         slot[k & 1] = id;
         mbar_arrive(bar(B_TF(k & 1)));
         if (id < 0) break;
-        // ask for the next item now, so that it is known (and its K/V can be loaded)
-        // as soon as this item's last loads are issued
-        mbar_arrive_expect_tx(bar(B_CLC), 16);
-        clc_try_cancel(clc_resp, bar(B_CLC));
-        pending = true;
-        ++n_req;
+        // ask for the next item together with this item's last loads: early enough that
+        // the answer is there when they complete, late enough that a CTA takes an item
+        // only when it is nearly free
+        auto request = [&]() {
+          mbar_arrive_expect_tx(bar(B_CLC), 16);
+          clc_try_cancel(clc_resp, bar(B_CLC));
+          pending = true;
+          ++n_req;
+        };
         const Item t = item_of(id);
+        if (t.n_iter <= 0) request();
         if (t.n_iter > 0) {
           const int kvb = kq & 1;
           if (!(ok = mbar_wait(bar(B_KVE(kvb)), ((kq >> 1) & 1) ^ 1, ctl))) break;
@@ -270,6 +274,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                           c * G::SPAN, t.sr.y(qrow, hq), t.sr.z(qrow, hq));
             bulk_load(sb + SM::D_OFF + g * 512, Dp + row, 512, bar(B_GF(g)));
             ++ng;
+            if (it + 1 == t.n_iter) request();
           }
           if (!ok) break;
         }
@@ -665,12 +670,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         slot[k & 1] = id;
         mbar_arrive(bar(B_TF(k & 1)));
         if (id < 0) break;
-        // ask for the next item now, so that it is known once this item's loads are out
-        mbar_arrive_expect_tx(bar(B_CLC), 16);
-        clc_try_cancel(clc_resp, bar(B_CLC));
-        pending = true;
-        ++n_req;
+        // ask for the next item together with this item's last loads (as in dK/dV)
+        auto request = [&]() {
+          mbar_arrive_expect_tx(bar(B_CLC), 16);
+          clc_try_cancel(clc_resp, bar(B_CLC));
+          pending = true;
+          ++n_req;
+        };
         const Item t = item_of(id);
+        if (t.n_iter <= 0) request();
         if (t.n_iter > 0) {
           const int b = kq & 1;
           const int qrow = t.qb * BT;
@@ -698,6 +706,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                           c * G::SPAN, t.sr.y(krow, t.hk), t.sr.z(krow, t.hk));
             }
             ++nkv;
+            if (j + 1 == t.n_iter) request();
           }
           if (!ok) break;
         }

@@ -556,13 +556,19 @@ __global__ void __launch_bounds__(one::THREADS, 2)
         slot[k & 1] = tile;
         mbar_arrive(bar(B_TF(k & 1)));          // release: the slot write is seen with the phase
         if (tile < 0) break;
-        // ask for the next tile now, so that it is known as soon as this tile's last
-        // loads are issued
-        mbar_arrive_expect_tx(bar(B_CLC), 16);
-        clc_try_cancel(clc_resp, bar(B_CLC));
-        pending = true;
-        ++n_req;
+        // ask for the next tile together with this tile's last loads: early enough that
+        // the answer is there when they complete, late enough that a CTA takes a tile
+        // only when it is nearly free (asking at a tile's start handed the last tiles to
+        // CTAs that still had most of a long tile ahead, and took tiles from CTAs that had
+        // not started yet when all would have fit at once)
+        auto request = [&]() {
+          mbar_arrive_expect_tx(bar(B_CLC), 16);
+          clc_try_cancel(clc_resp, bar(B_CLC));
+          pending = true;
+          ++n_req;
+        };
         const one::Tile1 t = tile_of(tile);
+        if (t.nt <= 0) request();
         if (t.nt > 0) {
           const int qb = kq & 1;
           if (!(ok = mbar_wait(bar(B_QE(qb)), ((kq >> 1) & 1) ^ 1, ctl))) break;
@@ -587,6 +593,7 @@ __global__ void __launch_bounds__(one::THREADS, 2)
               tma_load_3d(sb + C1::V_OFF + st * C1::TILE_BYTES + c * C::CHUNK_BYTES, &tmV,
                           bar(B_VF(st)), c * C::ATOM, t.sr.y(krow, t.hk), t.sr.z(krow, t.hk));
             ++nv;
+            if (j + 1 == t.nt) request();
           }
           if (!ok) break;
         }
