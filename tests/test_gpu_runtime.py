@@ -238,3 +238,64 @@ def test_cuda_graph_replay_matches_eager(B, H, N, d, dtype):
         for a, b in zip(ref, (o, lse, dq, dk, dv)):
             assert torch.equal(a, b)
     assert fa.device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,N,d,dtype", [(4, 16, 1000, 64, "fp16"), (8, 8, 777, 32, "bf16"),
+                                           (1, 8, 2048, 128, "bf16")])
+def test_back_to_back_steps_share_o_lse_workspace(B, H, N, d, dtype):
+    """Steps launched back to back, with no host synchronisation or other kernel between
+    them, as a training loop runs them.  Every kernel is a dependent launch: it may start
+    while the kernel before it drains, and waits (griddepcontrol.wait) before touching
+    global memory.  The steps share O, L and the workspace, which the next step's forward
+    and backward overwrite, but each writes dQ, dK and dV of its own; every step's
+    gradients must equal those of the same inputs run alone.  The inputs alternate
+    between two sets, so a step that read the next step's O, L or D would show it."""
+    fa = _fa()
+    sets = []
+    for seed in (11, 12):
+        x = inputs.make_inputs(B, H, N, d, dtype, seed=seed)
+        sets.append([x[n].cuda() for n in ("q", "k", "v", "do")])
+    ref = []
+    for q, k, v, do in sets:
+        o, lse = fa.fwd(q, k, v, causal=True)
+        ref.append([t.clone() for t in fa.bwd(q, k, v, o, lse, do, causal=True)])
+        torch.cuda.synchronize()
+    q0 = sets[0][0]
+    o = torch.empty_like(q0)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(fa.bwd_workspace_size(B, H, N, d, True), dtype=torch.uint8, device="cuda")
+    steps = 6
+    grads = [[torch.empty_like(q0) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        q, k, v, do = sets[i % 2]
+        dq, dk, dv = grads[i]
+        fa.fwd(q, k, v, causal=True, out=o, lse=lse)
+        fa.bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        for a, b in zip(ref[i % 2], grads[i]):
+            assert torch.equal(a, b), f"step {i}"
+    assert fa.device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,N,d", [(4, 16, 1000, 64), (1, 8, 2048, 128)])
+def test_traced_step_matches_untraced(B, H, N, d):
+    """The per-kernel CUDA-event trace records an event between every two kernels, which
+    makes each kernel wait for the previous one to finish before it starts; without it
+    the kernels overlap as dependent launches.  Both orderings give the same bits."""
+    fa = _fa()
+    x = inputs.make_inputs(B, H, N, d, "bf16", seed=13)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    outs = []
+    for traced in (False, True):
+        fa.trace_enable(traced)
+        try:
+            o, lse = fa.fwd(q, k, v, causal=True)
+            dq, dk, dv = fa.bwd(q, k, v, o, lse, do, causal=True)
+            torch.cuda.synchronize()
+        finally:
+            fa.trace_enable(False)
+        outs.append([t.clone() for t in (o, lse, dq, dk, dv)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
