@@ -132,6 +132,59 @@ def test_varlen_many_sequences():
     print(compare_varlen(lens, 8, 128, "bf16", True, Hkv=2, seed=19))
 
 
+def test_varlen_full_size_sampled():
+    """The packed workload the bench times (64 sequences of 256..8192 tokens drawn with
+    seed 2026, 270,160 tokens, 32 query heads over 8 K/V heads, d = 128 bf16, causal),
+    run whole; sampled against the oracle: the longest sequence with K/V head 0 and
+    its four query heads, the shortest with K/V head 7.  Sequences and K/V heads are
+    independent, so each sample is a dense GQA problem of its own, compared in full."""
+    import math
+    import numpy as np
+    import torch
+    import exact_io_aware_22_gb300 as fa
+    import oracle
+    from exact_io_aware_22_gb300 import inputs
+    from tests.parity_util import TOL_G, TOL_L, TOL_O
+    lens = [int(x) for x in np.random.default_rng(2026).integers(256, 8193, 64)]
+    H, Hkv, d = 32, 8, 128
+    grp = H // Hkv
+    scale = 1.0 / math.sqrt(d)
+    x = inputs.make_packed_inputs(lens, H, d, "bf16", seed=0, Hkv=Hkv)
+    cu = x["cu_seqlens"]
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    cug = cu.cuda()
+    o, lse = fa.fwd_varlen(q, k, v, cug, max(lens), causal=True, scale=scale)
+    dq, dk, dv = fa.bwd_varlen(q, k, v, o, lse, do, cug, max(lens), causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    got_all = {"o": o.cpu(), "lse": lse.cpu(), "dq": dq.cpu(), "dk": dk.cpu(), "dv": dv.cpu()}
+    for s_idx, g in ((int(np.argmax(lens)), 0), (int(np.argmin(lens)), Hkv - 1)):
+        a, b = int(cu[s_idx]), int(cu[s_idx + 1])
+        qh = slice(g * grp, (g + 1) * grp)
+        # (rows, heads, d) -> (1, heads, rows, d) in fp64
+        sel = lambda t, hs: t[a:b, hs].double().permute(1, 0, 2).unsqueeze(0).numpy()
+        qs, dos = sel(x["q"], qh), sel(x["do"], qh)
+        ks, vs = sel(x["k"], slice(g, g + 1)), sel(x["v"], slice(g, g + 1))
+        o_ref, l_ref = oracle.fwd_gqa(qs, ks, vs, True, scale)
+        dq_ref, dk_ref, dv_ref, _ = oracle.bwd_gqa(qs, ks, vs, dos, True, scale)
+        got = {"o": sel(got_all["o"], qh), "lse": got_all["lse"][qh, a:b].double().numpy(),
+               "dq": sel(got_all["dq"], qh), "dk": sel(got_all["dk"], slice(g, g + 1)),
+               "dv": sel(got_all["dv"], slice(g, g + 1))}
+        rep = {}
+        for name, ref in (("o", o_ref), ("lse", l_ref), ("dq", dq_ref), ("dk", dk_ref),
+                          ("dv", dv_ref)):
+            gv = got[name].reshape(ref.shape)
+            assert np.isfinite(gv).all(), name
+            err = float(np.max(np.abs(gv - ref)))
+            if name in ("dq", "dk", "dv"):
+                err /= float(np.max(np.abs(ref)))
+            rep[name] = err
+        print("sequence", s_idx, "length", b - a, "K/V head", g, rep)
+        assert rep["o"] <= TOL_O["bf16"] and rep["lse"] <= TOL_L, rep
+        for n in ("dq", "dk", "dv"):
+            assert rep[n] <= TOL_G["bf16"], rep
+
+
 def test_d64_full_size_sampled():
     # 1 x 16 x 8192 x 64 bf16 causal (the d = 64 backward on many query tiles per key
     # block); heads 0 and 15 compared in full
