@@ -23,15 +23,17 @@
 // Roles (640 threads, one CTA per SM):
 //   warp 0       TMA producer and scheduler: publishes each item in a two-slot ring,
 //                streams its tiles, then asks for the next item.
-//   warp 1       TMEM allocator; lane 0 issues the score MMAs (dK/dV: S^T, dP^T).
-//   warp 2       lane 0 issues the gradient MMAs (dK/dV: dV, dK).
+//   warp 1       TMEM allocator; lane 0 issues the score MMAs (dK/dV: S^T, dP^T; dQ:
+//                S, dP).
+//   warp 2       lane 0 issues the gradient MMAs (dK/dV: dV, dK; dQ: dQ).
+//   warp 3       idle; it completes the first warpgroup for the register split.
 //   warps 4-19   four compute warpgroups, one thread per TMEM lane (a key row in dK/dV,
 //                a query row in dQ) and 32 columns of each 128-column score tile.  The
 //                element-wise work of a tile (exponentials, dS) is the same at every head
 //                dim, while the products shrink with it; at d <= 64 a tile's compute,
 //                not its MMAs, set the pace with two warps per scheduler, so the tile is
 //                cut four ways.  The producer / MMA warpgroup hands registers to the
-//                compute warpgroups (setmaxnreg: 40 and 104 of the 96 per thread given
+//                compute warpgroups (setmaxnreg: 56 and 104 of the 96 per thread given
 //                at launch).
 #include "fa_bwd_tiles.cuh"
 #include "fa_internal.h"
