@@ -46,7 +46,8 @@ def test_nan_prefill_and_canaries(N, causal):
         assert (buf[count:].float() == stored).all()
 
 
-@pytest.mark.parametrize("B,H,N,d", [(2, 4, 777, 128), (4, 16, 1500, 64), (8, 8, 1000, 32)])
+@pytest.mark.parametrize("B,H,N,d", [(2, 4, 777, 128), (4, 16, 1500, 64), (8, 8, 1000, 32),
+                                     (4, 8, 1000, 32)])
 def test_deterministic(B, H, N, d):
     """Twice the same inputs, bit-identical results.  At d <= 64 the kernels are
     persistent and take tiles in whatever order the hardware hands them out; every
@@ -202,7 +203,8 @@ def test_fwd_fp8_outputs_guarded_and_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("B,H,N,d,dtype", [(8, 16, 1024, 64, "fp16"), (2, 8, 2048, 128, "bf16")])
+@pytest.mark.parametrize("B,H,N,d,dtype", [(8, 16, 1024, 64, "fp16"), (2, 8, 2048, 128, "bf16"),
+                                           (4, 8, 1000, 32, "fp16")])
 def test_cuda_graph_replay_matches_eager(B, H, N, d, dtype):
     """Every call is asynchronous on the caller's stream with no host synchronisation, so
     a whole step (forward, backward with a caller workspace) can be captured into a CUDA
@@ -241,7 +243,7 @@ def test_cuda_graph_replay_matches_eager(B, H, N, d, dtype):
 
 
 @pytest.mark.parametrize("B,H,N,d,dtype", [(4, 16, 1000, 64, "fp16"), (8, 8, 777, 32, "bf16"),
-                                           (1, 8, 2048, 128, "bf16")])
+                                           (1, 8, 2048, 128, "bf16"), (4, 8, 1000, 32, "fp16")])
 def test_back_to_back_steps_share_o_lse_workspace(B, H, N, d, dtype):
     """Steps launched back to back, with no host synchronisation or other kernel between
     them, as a training loop runs them.  Every kernel is a dependent launch: it may start
